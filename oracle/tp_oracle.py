@@ -1,0 +1,226 @@
+"""CPU oracle for the tensor-parallel sharded Linear (fp64).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module.  The CUDA
+library never calls it and shares no code with it.
+
+Every function is the plain definition of what the sharded Linear computes,
+written out in float64 with explicit per-rank partials.  Inputs are numpy
+``uint16`` arrays holding bfloat16 bit patterns (exactly what the GPU reads);
+they are widened exactly to float64.  A library matmul (numpy ``@`` in
+float64) is the only primitive; there is no blocking, fusion or reordering.
+
+Sources (web pages, cited by title and section):
+
+* [M027] "compute-communication fusion" knowledge-base article,
+  xuujii.github.io/ai-infra-kb/details/M027.html.
+  §01 row-parallel Linear on two ranks (Y = Y0 + Y1; AllReduce vs the
+  matching ReduceScatter layout; AllGather then MatMul), §02 chunked
+  MatMul->AllReduce and AllGather->MatMul, §03 the worked example and the
+  two-engine timeline, §07 the self-check exercises.
+* [TP] "PyTorch 2.x tensor parallelism" tutorial,
+  www.cnblogs.com/zuoyang/p/22340322.
+  §2.3 column parallel, §2.4 row parallel, §2.5-2.7 the collectives,
+  §四/§六 forward and backward of both layouts, §7.1 the MLP block
+  (column FC1 -> GeLU -> row FC2), §九 the MHA projections, §11.3 the
+  sequence-parallel pair.
+
+Readings where the pages are silent (each one is also listed in the design
+notes): partials are accumulated without intermediate rounding and summed in
+rank order r = 0..p-1; GeLU is the exact erf form; the ReduceScatter splits
+the rows of Y into p contiguous blocks; a bias is not part of any workload.
+"""
+from __future__ import annotations
+
+import math
+from typing import Sequence
+
+import numpy as np
+from scipy.special import erf as _erf
+
+
+# ---------------------------------------------------------------- bf16 helpers
+
+def widen(b16: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float64 (exact)."""
+    b = np.asarray(b16, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 -> bfloat16 bits, round to nearest even (via float32).
+
+    Used only where a chained check feeds the oracle's own intermediate
+    (for instance GeLU(H) between FC1 and FC2) into the next layer in the
+    same storage type the library hands over.
+    """
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    b = f.view(np.uint32)
+    r = b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))
+    return (r >> np.uint32(16)).astype(np.uint16)
+
+
+# ---------------------------------------------------------------- activations
+
+def gelu(h: np.ndarray) -> np.ndarray:
+    """GeLU(x) = x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)).  [TP §7.1]"""
+    h = np.asarray(h, dtype=np.float64)
+    return 0.5 * h * (1.0 + _erf(h / math.sqrt(2.0)))
+
+
+def gelu_prime(h: np.ndarray) -> np.ndarray:
+    """d/dx GeLU(x) = Phi(x) + x * phi(x).  [TP §6.5, §7.1 backward]"""
+    h = np.asarray(h, dtype=np.float64)
+    cdf = 0.5 * (1.0 + _erf(h / math.sqrt(2.0)))
+    pdf = np.exp(-0.5 * h * h) / math.sqrt(2.0 * math.pi)
+    return cdf + h * pdf
+
+
+# ---------------------------------------------------------------- row parallel
+
+def row_partials(xs: Sequence[np.ndarray], ws: Sequence[np.ndarray]) -> list[np.ndarray]:
+    """Per-rank partial products P_r = X_r . W_r.  [M027 §01; TP §2.4]
+
+    ``xs[r]`` is X_r [M, K_r] (rank r's column block of X), ``ws[r]`` is
+    W_r [K_r, N] (rank r's row block of W).
+    """
+    assert len(xs) == len(ws) and len(xs) >= 1
+    return [widen(x) @ widen(w) for x, w in zip(xs, ws)]
+
+
+def row_fwd_allreduce(xs, ws) -> np.ndarray:
+    """MatMul+AllReduce: full Y = sum_r X_r . W_r, summed r = 0, 1, ..., p-1.
+
+    [M027 §01: Y = Y0 + Y1; the AllReduce layout leaves the whole Y on
+    every rank.  TP §2.4 / §四: Y = sum_k X_k @ A_k.]
+    """
+    parts = row_partials(xs, ws)
+    y = parts[0].copy()
+    for p_r in parts[1:]:
+        y = y + p_r
+    return y
+
+
+def row_fwd_reducescatter(xs, ws) -> list[np.ndarray]:
+    """MatMul+ReduceScatter: rank j holds rows [j*M/p, (j+1)*M/p) of Y.
+
+    [M027 §01: ReduceScatter in the layout that matches what follows;
+    TP §2.7: reduce, then each rank keeps one slice.]
+    """
+    y = row_fwd_allreduce(xs, ws)
+    p = len(xs)
+    m = y.shape[0]
+    assert m % p == 0, "ReduceScatter needs M divisible by p"
+    mp = m // p
+    return [y[j * mp:(j + 1) * mp] for j in range(p)]
+
+
+def row_bwd_dx(ws, dy, preacts=None) -> list[np.ndarray]:
+    """Row-parallel backward, input gradient: dX_k = dY . A_k^T (no reduction).
+
+    With ``preacts`` (the MLP case, FC2 fed by GeLU(H_k)) the gradient is
+    carried through the activation: dH_k = (dY . A_k^T) * GeLU'(H_k).
+    [TP §四/§六: dX_k = dY @ A_k^T needs no communication; §7.1.]
+    """
+    g = widen(dy)
+    out = []
+    for k, w in enumerate(ws):
+        d = g @ widen(w).T
+        if preacts is not None:
+            d = d * gelu_prime(widen(preacts[k]))
+        out.append(d)
+    return out
+
+
+def row_bwd_dw(xs, dy) -> list[np.ndarray]:
+    """Row-parallel backward, weight gradient: dA_k = X_k^T . dY (local).  [TP §四]"""
+    g = widen(dy)
+    return [widen(x).T @ g for x in xs]
+
+
+# ---------------------------------------------------------------- column parallel
+
+def col_fwd(x, ws, apply_gelu: bool = False):
+    """Column-parallel forward: H_k = X . A_k for every shard k.  [TP §2.3, §三]
+
+    Returns ``(ys, hs)``: with ``apply_gelu`` ys[k] = GeLU(H_k) (the MLP
+    FC1, TP §7.1) and hs[k] = H_k; otherwise ys[k] = H_k and hs is None.
+    """
+    xf = widen(x)
+    hs = [xf @ widen(w) for w in ws]
+    if apply_gelu:
+        return [gelu(h) for h in hs], hs
+    return hs, None
+
+
+def col_bwd_dx(ws, dys) -> np.ndarray:
+    """Column-parallel backward, input gradient with its AllReduce:
+    dX = sum_k dY_k . A_k^T, summed k = 0, 1, ..., p-1.  [TP §三/§六]"""
+    parts = [widen(d) @ widen(w).T for d, w in zip(dys, ws)]
+    dx = parts[0].copy()
+    for q in parts[1:]:
+        dx = dx + q
+    return dx
+
+
+def col_bwd_dw(x, dys) -> list[np.ndarray]:
+    """Column-parallel backward, weight gradient: dA_k = X^T . dY_k (local;
+    X is replicated on every rank).  [TP §三]"""
+    xt = widen(x).T
+    return [xt @ widen(d) for d in dys]
+
+
+# ---------------------------------------------------------------- AllGather + MatMul
+
+def all_gather_rows(xs) -> np.ndarray:
+    """AllGather of row shards: X = [X_0; X_1; ...; X_{p-1}].  [TP §2.6]"""
+    return np.vstack([widen(x) for x in xs])
+
+
+def ag_matmul(xs, ws, apply_gelu: bool = False):
+    """AllGather+MatMul: Y_k = [X_0; ...; X_{p-1}] . A_k.  [M027 §01-§02; TP §11.3]
+
+    Returns ``(ys, hs, x_gathered)`` with ys/hs as in :func:`col_fwd`.
+    """
+    xg = all_gather_rows(xs)
+    hs = [xg @ widen(w) for w in ws]
+    if apply_gelu:
+        return [gelu(h) for h in hs], hs, xg
+    return hs, None, xg
+
+
+# ---------------------------------------------------------------- chunked pipeline
+
+def n_chunks(m: int, chunk_m: int) -> int:
+    """Chunks of ``chunk_m`` rows covering M rows; the last one may be short.
+    ``chunk_m`` larger than M is clamped to M.  [M027 §03: M=128 in 4 chunks of 32]"""
+    if m <= 0:
+        return 0
+    c = min(chunk_m, m)
+    return -(-m // c)
+
+
+def pipeline_time(c: float, m: float, n: int) -> float:
+    """Ideal two-engine timeline of n chunks, compute c and communication m
+    per chunk: the first compute, n-1 steps of the slower engine, the last
+    communication.  [M027 §03: 3 + 3*max(3, 2) + 2 = 14 ms]"""
+    if n <= 0:
+        return 0.0
+    return c + (n - 1) * max(c, m) + m
+
+
+def serial_time(c: float, m: float, n: int) -> float:
+    """Unpipelined timeline: every chunk computes then communicates.  [M027 §03: 20 ms]"""
+    return n * (c + m)
+
+
+# ---------------------------------------------------------------- collective volumes
+
+def allreduce_bytes(p: int, msg_bytes: float) -> float:
+    """Bandwidth-optimal AllReduce volume per rank, 2(p-1)/p * msg.  [TP §2.5]"""
+    return 2.0 * (p - 1) / p * msg_bytes
+
+
+def allgather_bytes(p: int, msg_bytes: float) -> float:
+    """AllGather (and ReduceScatter) volume per rank, (p-1)/p * msg.  [TP §2.6-2.7]"""
+    return (p - 1) / p * msg_bytes

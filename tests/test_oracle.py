@@ -1,0 +1,394 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+* brute force: pure-Python triple loops on tiny shapes (the 4 x 6, p = 2
+  layer of the TP tutorial §5.3) and exact int64 products on larger
+  integer-valued inputs, built from the *unsharded* layer and sliced the way
+  the pages define the shards;
+* closed forms: GeLU values from the normal CDF table, GeLU' against a
+  central difference, the chunk-timeline formula and the page's printed
+  timeline, the collective-volume factors and byte counts the pages print;
+* planted mistakes: deliberately broken copies of oracle functions must fail
+  the same pins, which shows the pins can see a dropped term, a wrong sign,
+  a transposed operand or a misrouted slice.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _ints(shape, seed, bound=4):
+    return synth.integer_bf16(shape, seed, bound)
+
+
+def _as_int(b16):
+    v = oracle.widen(b16)
+    assert np.all(v == np.round(v))
+    return v.astype(np.int64)
+
+
+def _brute(a, b):
+    """Textbook triple loop on Python ints."""
+    m, k = len(a), len(a[0])
+    n = len(b[0])
+    assert len(b) == k
+    return [[sum(int(a[i][t]) * int(b[t][j]) for t in range(k)) for j in range(n)] for i in range(m)]
+
+
+def _shard_cols(full, p):
+    n = full.shape[1] // p
+    return [np.ascontiguousarray(full[:, k * n:(k + 1) * n]) for k in range(p)]
+
+
+def _shard_rows(full, p):
+    n = full.shape[0] // p
+    return [np.ascontiguousarray(full[k * n:(k + 1) * n]) for k in range(p)]
+
+
+# --------------------------------------------------------------- invariant checks
+# Each returns True when the given implementation satisfies the pin; the
+# planted-mistake test below feeds them broken implementations.
+
+def check_row_fwd(row_fwd, p, m, k, n, seed):
+    x = _ints((m, k * p), seed)
+    a = _ints((k * p, n), seed + 1)
+    xs = _shard_cols(x, p)            # X_k = X[:, k*in/p:(k+1)*in/p]
+    ws = _shard_rows(a, p)            # A_k = A[k*in/p:(k+1)*in/p, :]
+    want = _as_int(x) @ _as_int(a)    # unsharded layer, exact
+    got = row_fwd(xs, ws)
+    return got.shape == want.shape and np.array_equal(got, want.astype(np.float64))
+
+
+def check_row_rs(row_rs, p, m, k, n, seed):
+    x = _ints((m, k * p), seed)
+    a = _ints((k * p, n), seed + 1)
+    want = _as_int(x) @ _as_int(a)
+    got = row_rs(_shard_cols(x, p), _shard_rows(a, p))
+    mp = m // p
+    return len(got) == p and all(
+        np.array_equal(got[j], want[j * mp:(j + 1) * mp].astype(np.float64)) for j in range(p))
+
+
+def check_col_fwd(col_fwd, p, m, k, n, seed):
+    x = _ints((m, k), seed)
+    a = _ints((k, n * p), seed + 1)
+    want = _as_int(x) @ _as_int(a)
+    ys, _ = col_fwd(x, _shard_cols(a, p))  # A_k = A[:, k*out/p:(k+1)*out/p]
+    return np.array_equal(np.hstack(ys), want.astype(np.float64))
+
+
+def check_col_bwd_dx(col_bwd_dx, p, m, k, n, seed):
+    a = _ints((k, n * p), seed)
+    dy = _ints((m, n * p), seed + 1)
+    want = _as_int(dy) @ _as_int(a).T   # gradient of the unsharded layer
+    got = col_bwd_dx(_shard_cols(a, p), _shard_cols(dy, p))
+    return got.shape == want.shape and np.array_equal(got, want.astype(np.float64))
+
+
+def check_col_bwd_dw(col_bwd_dw, p, m, k, n, seed):
+    x = _ints((m, k), seed)
+    dy = _ints((m, n * p), seed + 1)
+    want = _as_int(x).T @ _as_int(dy)
+    got = col_bwd_dw(x, _shard_cols(dy, p))
+    return np.array_equal(np.hstack(got), want.astype(np.float64))
+
+
+def check_row_bwd_dx(row_bwd_dx, p, m, k, n, seed):
+    a = _ints((k * p, n), seed)
+    dy = _ints((m, n), seed + 1)
+    want = _as_int(dy) @ _as_int(a).T
+    got = row_bwd_dx(_shard_rows(a, p), dy)
+    return np.array_equal(np.hstack(got), want.astype(np.float64))
+
+
+def check_row_bwd_dw(row_bwd_dw, p, m, k, n, seed):
+    x = _ints((m, k * p), seed)
+    dy = _ints((m, n), seed + 1)
+    want = _as_int(x).T @ _as_int(dy)
+    got = row_bwd_dw(_shard_cols(x, p), dy)
+    return np.array_equal(np.vstack(got), want.astype(np.float64))
+
+
+def check_ag(ag, p, m, k, n, seed):
+    x = _ints((m, k), seed)
+    a = _ints((k, n * p), seed + 1)
+    want = _as_int(x) @ _as_int(a)
+    ys, _, xg = ag(_shard_rows(x, p), _shard_cols(a, p))
+    return np.array_equal(xg, _as_int(x).astype(np.float64)) and \
+        np.array_equal(np.hstack(ys), want.astype(np.float64))
+
+
+SHAPES = [(1, 8, 5, 7), (2, 6, 4, 6), (3, 9, 5, 4), (4, 8, 16, 8), (8, 16, 8, 3)]  # p, m, k, n
+
+
+# --------------------------------------------------------------- brute force, tiny
+
+def test_tp_tutorial_4x6_example_brute_force():
+    """TP tutorial §5.3: in = 4, out = 6, p = 2; column shards 4x3, row shards 2x6."""
+    m, inn, out, p = 3, 4, 6, 2
+    x = _ints((m, inn), 11)
+    a = _ints((inn, out), 12)
+    xi, ai = _as_int(x), _as_int(a)
+    full = _brute(xi.tolist(), ai.tolist())
+
+    col_shards = _shard_cols(a, p)
+    assert [s.shape for s in col_shards] == [(4, 3), (4, 3)]
+    ys, _ = oracle.col_fwd(x, col_shards)
+    for k in range(p):
+        assert ys[k].tolist() == [row[3 * k:3 * k + 3] for row in full]
+
+    row_shards = _shard_rows(a, p)
+    assert [s.shape for s in row_shards] == [(2, 6), (2, 6)]
+    xs = _shard_cols(x, p)
+    parts = oracle.row_partials(xs, row_shards)
+    for k in range(p):
+        assert parts[k].tolist() == _brute(_as_int(xs[k]).tolist(), _as_int(row_shards[k]).tolist())
+    assert oracle.row_fwd_allreduce(xs, row_shards).tolist() == full
+    # summing, not concatenating, gives the layer output (M027 §07, first exercise)
+    assert np.hstack(parts).shape != (m, out) or not np.array_equal(np.hstack(parts), full)
+
+
+def test_p1_is_textbook_gemm():
+    x = _ints((5, 7), 21)
+    w = _ints((7, 3), 22)
+    want = _brute(_as_int(x).tolist(), _as_int(w).tolist())
+    assert oracle.row_fwd_allreduce([x], [w]).tolist() == want
+    assert oracle.col_fwd(x, [w])[0][0].tolist() == want
+    dy = _ints((5, 3), 23)
+    want_dx = _brute(_as_int(dy).tolist(), _as_int(w).T.tolist())
+    assert oracle.col_bwd_dx([w], [dy]).tolist() == want_dx
+    assert oracle.row_bwd_dx([w], dy)[0].tolist() == want_dx
+    want_dw = _brute(_as_int(x).T.tolist(), _as_int(dy).tolist())
+    assert oracle.col_bwd_dw(x, [dy])[0].tolist() == want_dw
+    assert oracle.row_bwd_dw([x], dy)[0].tolist() == want_dw
+
+
+# --------------------------------------------------------------- invariants, exact
+
+@pytest.mark.parametrize("p,m,k,n", SHAPES)
+def test_invariants_exact(p, m, k, n):
+    s = 1000 + 17 * p + m
+    assert check_row_fwd(oracle.row_fwd_allreduce, p, m, k, n, s)
+    assert check_row_rs(oracle.row_fwd_reducescatter, p, m, k, n, s)
+    assert check_col_fwd(oracle.col_fwd, p, m, k, n, s)
+    assert check_col_bwd_dx(oracle.col_bwd_dx, p, m, k, n, s)
+    assert check_col_bwd_dw(oracle.col_bwd_dw, p, m, k, n, s)
+    assert check_row_bwd_dx(oracle.row_bwd_dx, p, m, k, n, s)
+    assert check_row_bwd_dw(oracle.row_bwd_dw, p, m, k, n, s)
+    assert check_ag(oracle.ag_matmul, p, m, k, n, s)
+
+
+def test_rs_slices_concatenate_to_allreduce():
+    p, m = 4, 16
+    xs = [synth.normal_bf16((m, 24), synth.seed_for(9, r)) for r in range(p)]
+    ws = [synth.normal_bf16((24, 10), synth.seed_for(9, 8 + r)) for r in range(p)]
+    ar = oracle.row_fwd_allreduce(xs, ws)
+    rs = oracle.row_fwd_reducescatter(xs, ws)
+    assert np.array_equal(np.vstack(rs), ar)
+
+
+def test_rank_order_is_left_to_right():
+    """The reduction sums partials r = 0, 1, ... in that order (fp64)."""
+    # values chosen so that a different order rounds differently in fp64
+    big, small = 2.0 ** 60, 1.0
+    xs = [synth.f32_to_bf16_bits(np.array([[v]], np.float32)) for v in (big, small, -big)]
+    ws = [synth.f32_to_bf16_bits(np.array([[1.0]], np.float32))] * 3
+    y = oracle.row_fwd_allreduce(xs, ws)
+    assert y[0, 0] == ((big + small) + -big)  # == 0.0 in fp64; another order gives 1.0
+    assert y[0, 0] == 0.0
+
+
+# --------------------------------------------------------------- GeLU closed forms
+
+def test_gelu_closed_forms():
+    # GeLU(x) = x * Phi(x); Phi(1) = 0.8413447460685429 (normal CDF table)
+    assert oracle.gelu(np.array(0.0)) == 0.0
+    assert abs(oracle.gelu(np.array(1.0)) - 0.8413447460685429) < 1e-15
+    assert abs(oracle.gelu(np.array(-1.0)) + 0.15865525393145707) < 1e-15
+    assert abs(oracle.gelu(np.array(2.0)) - 2 * 0.9772498680518208) < 1e-14
+    x = np.linspace(-6, 6, 241)
+    assert np.allclose(oracle.gelu(x) - oracle.gelu(-x), x, atol=1e-14, rtol=0)  # x*Phi(x) - (-x)Phi(-x)
+    assert oracle.gelu(np.array(12.0)) == 12.0 and oracle.gelu(np.array(-12.0)) == 0.0
+
+
+def test_gelu_prime_closed_forms():
+    assert oracle.gelu_prime(np.array(0.0)) == 0.5
+    # phi(1) = 0.24197072451914337: GeLU'(1) = Phi(1) + phi(1)
+    assert abs(oracle.gelu_prime(np.array(1.0)) - (0.8413447460685429 + 0.24197072451914337)) < 1e-15
+    x = np.linspace(-5, 5, 201)
+    h = 1e-5
+    fd = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+    assert np.max(np.abs(fd - oracle.gelu_prime(x))) < 1e-9
+    assert oracle.gelu_prime(np.array(40.0)) == 1.0 and oracle.gelu_prime(np.array(-40.0)) == 0.0
+
+
+def test_gelu_epilogues_special_cases():
+    """Pins the epilogues wired into the layer functions, not only gelu()."""
+    p, m, k, n = 2, 6, 8, 5
+    a = _ints((k * p, n), 31)
+    dy = _ints((m, n), 32)
+    ws = _shard_rows(a, p)
+    base = _as_int(dy) @ _as_int(a).T
+    zero = [synth.f32_to_bf16_bits(np.zeros((m, k), np.float32))] * p
+    got = oracle.row_bwd_dx(ws, dy, preacts=zero)          # GeLU'(0) = 1/2
+    assert np.array_equal(np.hstack(got), base / 2.0)
+    far = [synth.f32_to_bf16_bits(np.full((m, k), 64.0, np.float32))] * p
+    assert np.array_equal(np.hstack(oracle.row_bwd_dx(ws, dy, preacts=far)), base.astype(np.float64))
+    neg = [synth.f32_to_bf16_bits(np.full((m, k), -64.0, np.float32))] * p
+    assert np.all(np.hstack(oracle.row_bwd_dx(ws, dy, preacts=neg)) == 0.0)
+
+    x = synth.f32_to_bf16_bits(np.full((3, 4), 4.0, np.float32))
+    w = synth.f32_to_bf16_bits(np.full((4, 2), 4.0, np.float32))   # H = 64 everywhere
+    ys, hs = oracle.col_fwd(x, [w], apply_gelu=True)
+    assert np.all(hs[0] == 64.0) and np.all(ys[0] == 64.0)
+    ys, hs = oracle.col_fwd(x, [synth.f32_to_bf16_bits(-np.full((4, 2), 4.0, np.float32))], apply_gelu=True)
+    assert np.all(hs[0] == -64.0) and np.all(ys[0] == 0.0)
+
+
+# --------------------------------------------------------------- chunk timeline
+
+def test_pipeline_timeline_golden():
+    for c, m, n, t, serial in _read_rows("pipeline_timeline.txt"):
+        assert oracle.pipeline_time(float(c), float(m), int(n)) == float(t)
+        assert oracle.serial_time(float(c), float(m), int(n)) == float(serial)
+    # -30 % as the page states
+    assert abs(1 - oracle.pipeline_time(3, 2, 4) / oracle.serial_time(3, 2, 4) - 0.30) < 1e-12
+
+
+def test_pipeline_timeline_exercise_and_edges():
+    # M027 §07 exercise: compute 1 ms, communication 5 ms, 4 chunks.  By the
+    # page's timeline rule: 1 + 3 x 5 + 5 = 21 ms against 4 x 6 = 24 ms serial.
+    assert oracle.pipeline_time(1, 5, 4) == 21
+    assert oracle.serial_time(1, 5, 4) == 24
+    assert oracle.pipeline_time(2, 7, 1) == 9 == oracle.serial_time(2, 7, 1)  # one chunk: no overlap
+    assert oracle.pipeline_time(3, 3, 5) == 18                                 # c = m: (n + 1) c
+    assert oracle.pipeline_time(3, 2, 0) == 0
+
+
+def test_worked_example_shapes_and_bytes():
+    g = {r[0]: [int(v) for v in r[1:]] for r in _read_rows("worked_example.txt")}
+    (m, n), (chunk_m,), (eb,) = g["y_r"], g["chunk_m"], g["elem_bytes"]
+    assert oracle.n_chunks(m, chunk_m) == g["n_chunks"][0]
+    assert m * n * eb == g["local_output_kib"][0] * 1024
+    assert chunk_m * n * eb == g["chunk_kib"][0] * 1024
+    assert g["x_r"][0] == m and g["x_r"][1] == g["w_r"][0] and g["w_r"][1] == n
+    # the computation itself at these shapes: the sum of the two partials equals
+    # the unsharded product (exact on integer inputs), chunk by chunk
+    p = g["p"][0]
+    k = g["x_r"][1]
+    assert check_row_fwd(oracle.row_fwd_allreduce, p, m, k, 64, 77)
+
+
+def test_n_chunks_rules():
+    assert oracle.n_chunks(128, 32) == 4
+    assert oracle.n_chunks(130, 32) == 5        # last chunk short
+    assert oracle.n_chunks(16, 2048) == 1       # chunk_m > M is clamped to M
+    assert [oracle.n_chunks(2048, c) for c in (16, 64, 256, 1024, 2048)] == [128, 32, 8, 2, 1]
+    assert oracle.n_chunks(0, 32) == 0
+
+
+def test_collective_volumes_golden():
+    for p, f in _read_rows("allreduce_volume.txt"):
+        assert oracle.allreduce_bytes(int(p), 1.0) == float(f)
+        # AllGather + ReduceScatter carry the same volume as one AllReduce (TP §2.7)
+        assert 2 * oracle.allgather_bytes(int(p), 1.0) == float(f)
+    g = {r[0]: int(r[1]) for r in _read_rows("mlp_example.txt")}
+    msg = g["b"] * g["s"] * g["h"] * g["elem_bytes"]
+    assert oracle.allreduce_bytes(g["p"], msg) == g["allreduce_bytes"]
+    assert g["h"] * g["ffn"] * g["elem_bytes"] == g["w1_mib"] << 20
+    assert g["h"] * (g["ffn"] // g["p"]) * g["elem_bytes"] == g["w1_shard_mib"] << 20
+
+
+# --------------------------------------------------------------- bf16 and the generator
+
+def test_round_bf16_values():
+    vals = np.array([1.0, 1.0 / 3.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -2.0, 0.0])
+    assert oracle.round_bf16(vals).tolist() == [0x3F80, 0x3EAB, 0x3F80, 0x3F82, 0xC000, 0x0000]
+    assert synth.f32_to_bf16_bits(vals.astype(np.float32)).tolist() == [0x3F80, 0x3EAB, 0x3F80, 0x3F82, 0xC000, 0]
+
+
+def test_splitmix64_published_vectors():
+    # Vigna's reference splitmix64 outputs for seeds 0 and 1234567
+    assert [int(v) for v in synth.splitmix64(0, 0, 3)] == [
+        0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    assert [int(v) for v in synth.splitmix64(1234567, 0, 5)] == [
+        6457827717110365317, 3203168211198807973, 9817491932198370423,
+        4593380528125082431, 16408922859458223821]
+
+
+def test_normal_generator_statistics_and_determinism():
+    a = synth.normal_bf16((1 << 20,), 5, sigma=0.02)
+    b = synth.normal_bf16((1 << 20,), 5, sigma=0.02)
+    assert np.array_equal(a, b)
+    v = oracle.widen(a)
+    assert abs(v.mean()) < 1e-4 and abs(v.std() - 0.02) < 2e-4
+    # chunked / threaded generation equals one long stream
+    c = synth.normal_bf16((3, (1 << 21) + 7), 6)
+    d = synth.normal_bf16(((1 << 21) * 3 + 21,), 6, threads=1)
+    assert np.array_equal(c.reshape(-1), d)
+
+
+# --------------------------------------------------------------- planted mistakes
+
+def _drop_last(xs, ws):
+    return oracle.row_fwd_allreduce(xs[:-1], ws[:-1]) if len(xs) > 1 else -oracle.row_fwd_allreduce(xs, ws)
+
+
+def _wrong_sign(xs, ws):
+    parts = oracle.row_partials(xs, ws)
+    y = parts[0].copy()
+    for q in parts[1:]:
+        y = y - q
+    return y if len(parts) > 1 else y + 1
+
+
+def _misrouted_rs(xs, ws):
+    s = oracle.row_fwd_reducescatter(xs, ws)
+    return s[::-1] if len(s) > 1 else [s[0] * 2]
+
+
+def _untransposed_dx(ws, dys):
+    parts = [oracle.widen(d) @ oracle.widen(w).T[::-1] for d, w in zip(dys, ws)]
+    return sum(parts[1:], parts[0])
+
+
+def _col_shifted(x, ws):
+    ys, hs = oracle.col_fwd(x, ws)
+    return ys[1:] + ys[:1], hs
+
+
+def _dw_no_transpose_fix(x, dys):
+    return [oracle.widen(x).T @ oracle.widen(d)[::-1] for d in dys]
+
+
+def _ag_wrong_order(xs, ws):
+    return oracle.ag_matmul(xs[::-1], ws)
+
+
+def test_planted_mistakes_are_caught():
+    p, m, k, n = 2, 8, 6, 5
+    assert not check_row_fwd(_drop_last, p, m, k, n, 3)
+    assert not check_row_fwd(_wrong_sign, p, m, k, n, 3)
+    assert not check_row_rs(_misrouted_rs, p, m, k, n, 3)
+    assert not check_col_bwd_dx(_untransposed_dx, p, m, k, n, 3)
+    assert not check_col_fwd(_col_shifted, p, m, k, n, 3)
+    assert not check_col_bwd_dw(_dw_no_transpose_fix, p, m, k, n, 3)
+    assert not check_ag(_ag_wrong_order, p, m, k, n, 3)
+    bad_gelu = lambda h: 0.5 * h * (1.0 + np.tanh(h))  # noqa: E731 (wrong activation)
+    assert abs(bad_gelu(1.0) - 0.8413447460685429) > 1e-3
