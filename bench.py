@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the tensor-parallel MLP block on one GB300 (per GPU).
+
+Workload (one "step" = one pass of the whole hot path): the Megatron MLP
+block, forward and backward, with p = 4 shards held in one GPU's memory,
+4096 tokens, h = 4096, ffn = 16384 -- FC1 column-parallel [4096, 4096] per
+shard with GeLU, FC2 row-parallel [4096, 4096] per shard with the fused
+AllReduce, then FC2's backward (dZ_k = dY W2_k^T * GeLU'(H_k), dW2_k) and
+FC1's backward (the fused dX = sum_k dZ_k W1_k^T, dW1_k).  Six GEMM launches,
+3.30 TFLOP per step.  Inputs: X N(0,1), dY N(0,1), weights N(0, 0.02), bf16,
+drawn by the seeded generator.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --sweep      # chunk_m sweep report (GPT-3-scale FC pair)
+
+Prints one JSON line.  ``value`` is TFLOP/s of the whole job with inputs
+resident in HBM; ``e2e`` is the same through the C-ABI with host buffers
+(pinned H2D of the step's inputs and D2H of its outputs inside the timed
+region).  ``--impl reference`` times the CPU oracle on a bounded token sample
+of the same workload instead.  With N > 1 (torchrun, one rank per GPU) every
+rank runs an independent replica (the path has no cross-GPU exchange on one
+box) and ``value`` is the sum over ranks of the work divided by the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded GEMM+reduce TFLOP/s and % of GB300 dense BF16 peak (1 GPU)"
+P, M, H, FFN = 4, 4096, 4096, 16384
+NK = FFN // P
+GEMM_FLOPS = 2.0 * M * H * NK * P            # every one of the six launches
+STEP_FLOPS = 6 * GEMM_FLOPS
+WORKLOAD = (f"Megatron MLP block fwd+bwd, p={P}: tokens {M}, h={H}, ffn={FFN}; FC1 column-parallel "
+            f"[{H},{NK}]/shard + GeLU, FC2 row-parallel [{NK},{H}]/shard with fused AllReduce; "
+            f"backward: FC2 dZ (GeLU') + dW2, FC1 fused dX reduce + dW1")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["gemm_reduce_fusion_gb300/csrc/gemm_kernel.cuh", "gemm_reduce_fusion_gb300/csrc/ptx.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(kernel)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_init(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ the step
+
+class MLPStep:
+    """Device buffers and the six ABI calls of one MLP fwd+bwd step."""
+
+    def __init__(self, tp, torch, host):
+        bf = dict(dtype=torch.bfloat16, device="cuda")
+        self.tp = tp
+        self.torch = torch
+        self.X = torch.empty((M, H), **bf)
+        self.W1 = [torch.empty((H, NK), **bf) for _ in range(P)]
+        self.W2 = [torch.empty((NK, H), **bf) for _ in range(P)]
+        self.DY = torch.empty((M, H), **bf)
+        self.Z = [torch.empty((M, NK), **bf) for _ in range(P)]
+        self.Hp = [torch.empty((M, NK), **bf) for _ in range(P)]
+        self.Y = torch.empty((M, H), **bf)
+        self.DZ = [torch.empty((M, NK), **bf) for _ in range(P)]
+        self.DW2 = [torch.empty((NK, H), **bf) for _ in range(P)]
+        self.DX = torch.empty((M, H), **bf)
+        self.DW1 = [torch.empty((H, NK), **bf) for _ in range(P)]
+        need = max(tp.tp_workspace_size(op, P, mm, nn, kk, 0) for op, mm, nn, kk in [
+            (tp.TP_OP_COL_FWD, M, NK, H), (tp.TP_OP_ROW_AR, M, H, NK),
+            (tp.TP_OP_ROW_BWD, M, H, NK), (tp.TP_OP_COL_BWD, M, NK, H)])
+        self.ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        self.upload(host)
+
+    def inputs(self):
+        return [self.X, *self.W1, *self.W2, self.DY]
+
+    def outputs(self):
+        return [self.Y, self.DX, *self.DW1, *self.DW2]
+
+    def upload(self, host):
+        for d, h in zip(self.inputs(), host):
+            d.copy_(h, non_blocking=True)
+
+    def calls(self):
+        tp, ws = self.tp, self.ws
+        return [
+            ("col_fwd_gelu", lambda: tp.tp_col_linear_fwd(self.X, self.W1, self.Z, ws, epi=tp.TP_EPI_GELU,
+                                                          preact=self.Hp)),
+            ("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(self.Z, self.W2, [self.Y], ws)),
+            ("row_bwd_dx_dgelu", lambda: tp.tp_row_linear_bwd(None, self.W2, self.DY, self.DZ, None, ws,
+                                                              preact=self.Hp)),
+            ("row_bwd_dw", lambda: tp.tp_row_linear_bwd(self.Z, self.W2, self.DY, None, self.DW2, ws)),
+            ("col_bwd_dx", lambda: tp.tp_col_linear_bwd(None, self.W1, self.DZ, self.DX, None, ws)),
+            ("col_bwd_dw", lambda: tp.tp_col_linear_bwd(self.X, self.W1, self.DZ, None, self.DW1, ws)),
+        ]
+
+
+# which kernel variant each call launches (one launch per call at these sizes)
+CALL_KERNEL = {
+    "col_fwd_gelu": "tp_gemm_kernel<K-major A, MN-major B, 128x256> (X.W)",
+    "row_fwd_allreduce": "tp_gemm_kernel<K-major A, MN-major B, 128x256> (X.W)",
+    "row_bwd_dx_dgelu": "tp_gemm_kernel<K-major A, K-major B, 128x256> (dY.W^T)",
+    "col_bwd_dx": "tp_gemm_kernel<K-major A, K-major B, 128x256> (dY.W^T)",
+    "row_bwd_dw": "tp_gemm_kernel<MN-major A, MN-major B, 128x256> (X^T.dY)",
+    "col_bwd_dw": "tp_gemm_kernel<MN-major A, MN-major B, 128x256> (X^T.dY)",
+}
+
+
+def host_inputs(torch):
+    import synth
+    gen = [synth.normal_bf16((M, H), synth.seed_for(1, 0), 1.0)]
+    gen += [synth.normal_bf16((H, NK), synth.seed_for(1, 1 + k), 0.02) for k in range(P)]
+    gen += [synth.normal_bf16((NK, H), synth.seed_for(1, 5 + k), 0.02) for k in range(P)]
+    gen += [synth.normal_bf16((M, H), synth.seed_for(1, 9), 1.0)]
+    import numpy as np
+    out = []
+    for a in gen:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        out.append(t.pin_memory() if torch.cuda.is_available() else t)
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_step(x, w1, w2, dy):
+    """The same MLP step in the fp64 oracle on the given token sample."""
+    import oracle
+    z, h = oracle.col_fwd(x, w1, apply_gelu=True)
+    zb = [oracle.round_bf16(a) for a in z]
+    hb = [oracle.round_bf16(a) for a in h]
+    oracle.row_fwd_allreduce(zb, w2)
+    dz = oracle.row_bwd_dx(w2, dy, preacts=hb)
+    oracle.row_bwd_dw(zb, dy)
+    dzb = [oracle.round_bf16(a) for a in dz]
+    oracle.col_bwd_dx(w1, dzb)
+    oracle.col_bwd_dw(x, dzb)
+
+
+def cpu_inputs(tokens):
+    import synth
+    x = synth.normal_bf16((M, H), synth.seed_for(1, 0), 1.0)[:tokens]
+    w1 = [synth.normal_bf16((H, NK), synth.seed_for(1, 1 + k), 0.02) for k in range(P)]
+    w2 = [synth.normal_bf16((NK, H), synth.seed_for(1, 5 + k), 0.02) for k in range(P)]
+    dy = synth.normal_bf16((M, H), synth.seed_for(1, 9), 1.0)[:tokens]
+    return x, w1, w2, dy
+
+
+def cpu_baseline(target_s=10.0):
+    """Time the oracle on a token sample sized for about `target_s` seconds."""
+    tokens = 64
+    x, w1, w2, dy = cpu_inputs(M)
+    t0 = time.perf_counter()
+    oracle_step(x[:tokens], w1, w2, dy[:tokens])
+    dt = time.perf_counter() - t0
+    tokens = int(min(M, max(64, tokens * target_s / max(dt, 1e-3))) // 64 * 64)
+    t0 = time.perf_counter()
+    oracle_step(x[:tokens], w1, w2, dy[:tokens])
+    dt = time.perf_counter() - t0
+    flops = STEP_FLOPS * tokens / M
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one MLP fwd+bwd step over {tokens} of the {M} tokens with the full weights "
+                      f"(fp64 numpy oracle, {dt:.1f} s, {flops / 1e9:.0f} GFLOP)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    tokens = 64
+    x, w1, w2, dy = cpu_inputs(tokens)
+    for _ in range(args.warmup):
+        oracle_step(x, w1, w2, dy)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(x, w1, w2, dy)
+    dt = time.perf_counter() - t0
+    flops = STEP_FLOPS * tokens / M
+    v = flops * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded splitmix64 normals)",
+            "config": {"workload": WORKLOAD, "sample_tokens": tokens},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"each step: the MLP fwd+bwd over {tokens} of the {M} tokens, full weights"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_init(args.gpus)
+    torch.cuda.set_device(local)
+    import gemm_reduce_fusion_gb300 as tp
+
+    host = host_inputs(torch)
+    step = MLPStep(tp, torch, host)
+    calls = step.calls()
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    st = tp.tp_get_device_status(step.ws)
+    if st != tp.TP_OK:
+        raise RuntimeError(f"device status after warm-up: {tp.tp_status_string(st)}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(K):
+            ev[k][0].record(stream)
+            for i, (_, fn) in enumerate(calls):
+                fn()
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = clk.summary()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][len(calls)])
+    per_call = {name: 0.0 for name, _ in calls}
+    for k in range(K):
+        for i, (name, _) in enumerate(calls):
+            per_call[name] += ev[k][i].elapsed_time(ev[k][i + 1])
+    st = tp.tp_get_device_status(step.ws)
+    if st != tp.TP_OK:
+        raise RuntimeError(f"device status after timing: {tp.tp_status_string(st)}")
+
+    t_max = max_over_ranks(total_ms, world)
+    value = STEP_FLOPS * K * world / (t_max / 1e3) / 1e12
+
+    # dominant kernel variant: the one with the largest total time
+    per_kernel = {}
+    for name, ms in per_call.items():
+        kname = CALL_KERNEL[name]
+        d = per_kernel.setdefault(kname, {"ms": 0.0, "launches": 0})
+        d["ms"] += ms
+        d["launches"] += K
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
+    dom_avg_s = per_kernel[dom]["ms"] / per_kernel[dom]["launches"] / 1e3
+    pk, src = peaks()
+    peak = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    achieved = GEMM_FLOPS / dom_avg_s / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{src} bf16 dense, sustained (timed inside a long step)",
+                "traffic": dram_traffic(dom),
+                "per_call_ms": {n: per_call[n] / K for n in per_call},
+                "value_frac_of_peak": value / world / peak}
+
+    # end to end through the ABI with host buffers
+    E = max(1, args.e2e_steps)
+    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.outputs()]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in houts)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        step.upload(host)
+        for _, fn in calls:
+            fn()
+        for h, d in zip(houts, step.outputs()):
+            h.copy_(d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = {"value": STEP_FLOPS * E * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E}
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": t_max / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded splitmix64 normals: X, dY N(0,1); weights N(0,0.02))",
+            "config": {"workload": WORKLOAD, "p": P, "tokens": M, "h": H, "ffn": FFN,
+                       "flops_per_step": STEP_FLOPS, "chunk_m": "scheduler (0)",
+                       "l2": "no flush: every step streams inputs larger than L2 "
+                             "(X 32 MiB, W1 128 MiB, W2 128 MiB, dY 32 MiB, 129 MB L2)",
+                       "parallelism": f"{world} independent replica(s), all {P} ranks on each GPU"},
+            "roofline": roofline, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": len(calls) * K}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.sweep:
+        raise SystemExit("--sweep: not built yet")
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+"""Python binding of the tp_fused C-ABI (argument marshalling only).
+
+Every function here has the name of the C entry point it calls
+(``include/tp_fused.h``).  It reads shapes from the torch tensors it is
+given, passes their device pointers and the current CUDA stream to the
+shared library, and raises :class:`TPError` on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback: if the
+library is missing the import fails.
+
+Tensors are torch CUDA tensors, contiguous, row-major; inputs bfloat16,
+outputs bfloat16 or float32.  Lists hold one tensor per rank/shard.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtpfused.so")
+
+# tp_status
+TP_OK = 0
+TP_ERR_INVALID_ARG = 1
+TP_ERR_ALIGNMENT = 2
+TP_ERR_UNSUPPORTED_SHAPE = 3
+TP_ERR_WORKSPACE_TOO_SMALL = 4
+TP_ERR_ARCH = 5
+TP_ERR_CUDA = 6
+TP_ERR_DEVICE_TIMEOUT = 7
+# tp_dtype
+TP_BF16 = 0
+TP_FP32 = 1
+# tp_epilogue
+TP_EPI_NONE = 0
+TP_EPI_GELU = 1
+TP_EPI_DGELU = 2
+# tp_op
+TP_OP_ROW_AR = 0
+TP_OP_ROW_RS = 1
+TP_OP_COL_FWD = 2
+TP_OP_COL_BWD = 3
+TP_OP_ROW_BWD = 4
+TP_OP_AG_MM = 5
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tp_status_string(status)} (status {status})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python gemm_reduce_fusion_gb300/build.py` "
+            "(nvcc, sm_103a); there is no non-CUDA fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    I = ctypes.c_int
+    L = ctypes.c_int64
+    S = ctypes.c_size_t
+    sig = {
+        "tp_workspace_size": (S, [I, I, L, L, L, L]),
+        "tp_row_linear_fwd_allreduce": (I, [PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_fwd_reducescatter": (I, [PP, PP, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_col_linear_fwd": (I, [P, PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
+        "tp_col_linear_bwd": (I, [P, PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_bwd": (I, [PP, PP, P, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_ag_matmul": (I, [PP, PP, PP, P, I, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_pipeline_time": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, L]),
+        "tp_num_chunks": (L, [L, L]),
+        "tp_choose_chunk_m": (L, [I, I, L, L, L]),
+        "tp_get_device_status": (I, [P, P]),
+        "tp_status_string": (ctypes.c_char_p, [I]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous (row-major)")
+    return t.data_ptr()
+
+
+def _arr(ts) -> ctypes.Array | None:
+    if ts is None:
+        return None
+    return (ctypes.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return TP_BF16
+    if t.dtype == torch.float32:
+        return TP_FP32
+    raise ValueError(f"unsupported output dtype {t.dtype}")
+
+
+def _ws(ws):
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def _check(status: int, where: str) -> None:
+    if status != TP_OK:
+        raise TPError(status, where)
+
+
+# ------------------------------------------------------------------ host-only calls
+
+def tp_status_string(status: int) -> str:
+    return _lib.tp_status_string(int(status)).decode()
+
+
+def tp_workspace_size(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0) -> int:
+    return int(_lib.tp_workspace_size(op, p, M, N, K, chunk_m))
+
+
+def tp_pipeline_time(c: float, m: float, n_chunks: int) -> float:
+    return float(_lib.tp_pipeline_time(c, m, n_chunks))
+
+
+def tp_num_chunks(M: int, chunk_m: int) -> int:
+    return int(_lib.tp_num_chunks(M, chunk_m))
+
+
+def tp_choose_chunk_m(op: int, p: int, M: int, N: int, K: int) -> int:
+    return int(_lib.tp_choose_chunk_m(op, p, M, N, K))
+
+
+def workspace(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0, device="cuda"):
+    """A zero-filled device workspace of tp_workspace_size(...) bytes (torch-allocated)."""
+    import torch
+    n = tp_workspace_size(op, p, M, N, K, chunk_m)
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def tp_get_device_status(ws, stream=None) -> int:
+    """Latched device status of ``ws`` (synchronises the stream, clears it)."""
+    return int(_lib.tp_get_device_status(_ptr(ws), _stream(stream)))
+
+
+# ------------------------------------------------------------------ the sharded Linear
+
+def tp_row_linear_fwd_allreduce(x: Sequence, w: Sequence, y: Sequence, ws, chunk_m: int = 0,
+                                stream=None) -> None:
+    """Y = sum_r X_r W_r written once (len(y) == 1) or as p replicas (len(y) == p)."""
+    p = len(x)
+    M, K = x[0].shape
+    N = w[0].shape[1]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_row_linear_fwd_allreduce(_arr(x), _arr(w), _arr(y), len(y), p, M, N, K, chunk_m,
+                                            _dtype_code(y[0]), wp, wb, _stream(stream)),
+           "tp_row_linear_fwd_allreduce")
+
+
+def tp_row_linear_fwd_reducescatter(x: Sequence, w: Sequence, y: Sequence, ws, chunk_m: int = 0,
+                                    stream=None) -> None:
+    """Rank j's y[j] = rows [j M/p, (j+1) M/p) of sum_r X_r W_r."""
+    p = len(x)
+    M, K = x[0].shape
+    N = w[0].shape[1]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_row_linear_fwd_reducescatter(_arr(x), _arr(w), _arr(y), p, M, N, K, chunk_m,
+                                                _dtype_code(y[0]), wp, wb, _stream(stream)),
+           "tp_row_linear_fwd_reducescatter")
+
+
+def tp_col_linear_fwd(x, w: Sequence, y: Sequence, ws, epi: int = TP_EPI_NONE, preact=None,
+                      chunk_m: int = 0, stream=None) -> None:
+    """y[k] = X A_k (or GeLU(X A_k), with H_k into preact[k])."""
+    p = len(w)
+    M, K = x.shape
+    N = w[0].shape[1]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_col_linear_fwd(_ptr(x), _arr(w), _arr(y), _arr(preact), epi, p, M, N, K, chunk_m,
+                                  _dtype_code(y[0]), wp, wb, _stream(stream)), "tp_col_linear_fwd")
+
+
+def tp_col_linear_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0,
+                      stream=None) -> None:
+    """dX = sum_k dY_k A_k^T; dw[k] = X^T dY_k (dw may be None)."""
+    p = len(w)
+    K, N = w[0].shape
+    M = dy[0].shape[0]
+    out = dx if dx is not None else dw[0]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_col_linear_bwd(_ptr(x), _arr(w), _arr(dy), _ptr(dx), _arr(dw), p, M, N, K, chunk_m,
+                                  _dtype_code(out), wp, wb, _stream(stream)), "tp_col_linear_bwd")
+
+
+def tp_row_linear_bwd(x, w: Sequence, dy, dx, dw, ws, preact=None, chunk_m: int = 0,
+                      stream=None) -> None:
+    """dx[k] = dY A_k^T (times GeLU'(preact[k])); dw[k] = X_k^T dY."""
+    p = len(w)
+    K, N = w[0].shape
+    M = dy.shape[0]
+    out = dx[0] if dx is not None else dw[0]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_row_linear_bwd(_arr(x), _arr(w), _ptr(dy), _arr(dx), _arr(dw), _arr(preact), p,
+                                  M, N, K, chunk_m, _dtype_code(out), wp, wb, _stream(stream)),
+           "tp_row_linear_bwd")
+
+
+def tp_ag_matmul(x: Sequence, w: Sequence, y: Sequence, ws, x_gathered=None,
+                 epi: int = TP_EPI_NONE, preact=None, chunk_m: int = 0, stream=None) -> None:
+    """y[k] = [X_0; ...; X_{p-1}] A_k (optionally GeLU, H_k, gathered X)."""
+    p = len(x)
+    Mp, K = x[0].shape
+    N = w[0].shape[1]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
+                             Mp * p, N, K, chunk_m, _dtype_code(y[0]), wp, wb, _stream(stream)),
+           "tp_ag_matmul")

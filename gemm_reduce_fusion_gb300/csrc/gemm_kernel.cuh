@@ -1,0 +1,538 @@
+// Persistent, warp-specialised tcgen05 GEMM for the sharded Linear.
+//
+// One launch covers a whole sharded-Linear call.  Its tile space is
+//   groups along M (Gm) x groups along N (Gn) x m-tiles x n-tiles x splits,
+// and its K loop walks S "segments" -- one per rank whose partial product is
+// being reduced -- in rank order, each segment being K/64 k-blocks.  All
+// segments of a tile accumulate into the same fp32 tensor-memory
+// accumulator, so the cross-rank reduction happens in TMEM and the reduced
+// tile is written once.
+//
+// Roles (192 threads):
+//   warp 0     one thread issues TMA loads of A and B k-blocks into a
+//              STAGES-deep shared-memory ring (full/empty mbarriers);
+//   warp 1     allocates tensor memory; one thread issues tcgen05.mma into
+//              one of two TMEM accumulators and commits to the ring's
+//              empty barriers and to the accumulator-full barrier;
+//   warps 2-5  epilogue: tcgen05.ld the finished accumulator (warp w reads
+//              TMEM lanes 32*(w%4)..+31), apply GeLU / GeLU' / cast, store,
+//              then release the accumulator -- overlapping the next tile's
+//              MMAs on the other accumulator.
+//
+// Tiles are visited chunk-major: all tiles of rows chunk c (over every
+// N-tile) precede those of chunk c+1, m fastest within a chunk, so a chunk's
+// write-out overlaps the next chunk's MMAs ("ai-infra-kb M027", §02-§03).
+//
+// Every mbarrier wait is bounded in time: on expiry the kernel latches an
+// error bit in the status word, tells the other roles to stop, waits (again
+// bounded) for its own TMA loads and MMAs in flight, frees TMEM and returns.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace tpf {
+
+constexpr int BM = 128;           // tile rows (UMMA M)
+constexpr int BK = 64;            // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
+constexpr int MAX_MAPS = 8;
+constexpr int MAX_GROUPS = 64;
+constexpr int NUM_THREADS = 192;
+
+enum Epi : int32_t { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
+
+// Status word bits (workspace word 0).
+constexpr uint32_t ST_TIMEOUT = 1u;
+
+struct GemmParams {
+  CUtensorMap tmA[MAX_MAPS];
+  CUtensorMap tmB[MAX_MAPS];
+  void* out[MAX_GROUPS];  // per-group output base (group g = gm * Gn + gn)
+  void* aux[MAX_GROUPS];  // GELU: H out (nullable); DGELU: H in (bf16)
+  int32_t Gm, Gn;
+  int32_t m_tiles, n_tiles;  // per group
+  int32_t chunk_tiles;       // tiles per chunk along the chunked axis
+  int32_t chunk_on_n;        // chunks run along GEMM N (operand-swapped kernels)
+  int32_t num_units;         // Gm*Gn*m_tiles*n_tiles*n_split
+  int32_t S;                 // K segments (ranks reduced)
+  int32_t kb_per_seg;        // k-blocks per segment
+  int32_t n_split;           // split-K factor
+  int32_t kb_per_split;      // k-blocks per split over the S*kb_per_seg space
+  int32_t a_idx_gm, a_idx_gn, a_idx_s;
+  int32_t b_idx_gm, b_idx_gn, b_idx_s;
+  int32_t a_row_gm;          // GEMM-M coordinate offset of group gm in its A map
+  int32_t b_col_gn;          // GEMM-N coordinate offset of group gn in its B map
+  int32_t rows_g, cols_g;    // valid GEMM rows / cols of one group
+  int64_t ld_out, ld_aux;    // row pitch (elements) of out / aux
+  int32_t out_f32;           // output is fp32 (else bf16)
+  int32_t epi;
+  int32_t n_rep;             // replicas of a single-group output (out[0..n_rep))
+  float* partial;            // split-K fp32 partials, dense, output orientation
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+struct Unit {
+  int32_t gm, gn, mt, nt, q0, q1;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& P, int32_t t) {
+  Unit u;
+  const int32_t sp = t % P.n_split;
+  const int32_t v = t / P.n_split;
+  const int32_t TM = P.Gm * P.m_tiles;
+  const int32_t TN = P.Gn * P.n_tiles;
+  // chunked axis C (token rows), other axis O; C runs fastest inside a chunk
+  const int32_t TC = P.chunk_on_n ? TN : TM;
+  const int32_t TO = P.chunk_on_n ? TM : TN;
+  const int32_t per_chunk = P.chunk_tiles * TO;
+  const int32_t c = v / per_chunk;
+  const int32_t r = v % per_chunk;
+  const int32_t lo = c * P.chunk_tiles;
+  const int32_t cnt = min(P.chunk_tiles, TC - lo);
+  const int32_t O = r / cnt;
+  const int32_t C = lo + r % cnt;
+  const int32_t GM = P.chunk_on_n ? O : C;
+  const int32_t GN = P.chunk_on_n ? C : O;
+  u.gm = GM / P.m_tiles;
+  u.mt = GM % P.m_tiles;
+  u.gn = GN / P.n_tiles;
+  u.nt = GN % P.n_tiles;
+  const int32_t kb_total = P.S * P.kb_per_seg;
+  u.q0 = sp * P.kb_per_split;
+  u.q1 = min(kb_total, u.q0 + P.kb_per_split);
+  return u;
+}
+
+// Bounded wait; false on timeout (latched) or when another role aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const GemmParams& P,
+                                         volatile int32_t* abort_flag, uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 127u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > P.timeout_ns) {
+        *abort_flag = 1;
+        atomicOr(P.status, ST_TIMEOUT | (role << 4));
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used while shutting down: never latches, never aborts others.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+__device__ __forceinline__ float gelu_f(float h) {
+  return 0.5f * h * (1.0f + erff(h * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ float gelu_prime_f(float h) {
+  const float cdf = 0.5f * (1.0f + erff(h * 0.70710678118654752f));
+  const float pdf = 0.39894228040143268f * expf(-0.5f * h * h);
+  return cdf + h * pdf;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Epilogue transform of 8 consecutive values; `aux` points at the matching 8
+// elements of H (DGELU reads them, GELU writes them when non-null).
+__device__ __forceinline__ void epi8(const GemmParams& P, float (&v)[8], void* aux) {
+  if (P.epi == EPI_GELU) {
+    if (aux != nullptr) {
+      if (P.out_f32) {
+        float4* a = reinterpret_cast<float4*>(aux);
+        a[0] = make_float4(v[0], v[1], v[2], v[3]);
+        a[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        *reinterpret_cast<uint4*>(aux) =
+            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                       pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = gelu_f(v[i]);
+  } else if (P.epi == EPI_DGELU) {
+    const uint4 h = *reinterpret_cast<const uint4*>(aux);
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[i] & 0xFFFFu)));
+      v[2 * i + 1] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[i] >> 16)));
+    }
+  }
+}
+
+__device__ __forceinline__ void store8(void* dst, bool f32, const float (&v)[8]) {
+  if (f32) {
+    float4* d = reinterpret_cast<float4*>(dst);
+    d[0] = make_float4(v[0], v[1], v[2], v[3]);
+    d[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+  }
+}
+
+// Scalar epilogue for the transposed (operand-swapped) orientation.
+__device__ __forceinline__ void epi_store1(const GemmParams& P, float v, void* out, void* aux,
+                                           int64_t off_out, int64_t off_aux) {
+  if (P.epi == EPI_GELU) {
+    if (aux != nullptr) {
+      if (P.out_f32) reinterpret_cast<float*>(aux)[off_aux] = v;
+      else reinterpret_cast<__nv_bfloat16*>(aux)[off_aux] = __float2bfloat16_rn(v);
+    }
+    v = gelu_f(v);
+  } else if (P.epi == EPI_DGELU) {
+    const uint16_t h = reinterpret_cast<const uint16_t*>(aux)[off_aux];
+    v *= gelu_prime_f(bf16_bits_to_f(h));
+  }
+  if (P.out_f32) reinterpret_cast<float*>(out)[off_out] = v;
+  else reinterpret_cast<__nv_bfloat16*>(out)[off_out] = __float2bfloat16_rn(v);
+}
+
+template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
+struct GemmCfg {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+  static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-wide boxes");
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
+                                      : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  // +1024 so the ring can be aligned to 1024 bytes inside dynamic smem
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int CW = BN < 32 ? BN : 32;  // epilogue columns per TMEM load
+};
+
+template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tp_gemm_kernel(const __grid_constant__ GemmParams P) {
+  using Cfg = GemmCfg<A_MN, B_MN, BN, OUT_T, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + STAGES * Cfg::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * Cfg::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < P.num_units && ok; t += gridDim.x) {
+        const Unit u = decode_unit(P, t);
+        const int32_t arow = P.a_row_gm * u.gm + u.mt * BM;
+        const int32_t bcol = P.b_col_gn * u.gn + u.nt * BN;
+        for (int32_t q = u.q0; q < u.q1; ++q) {
+          const int32_t s = q / P.kb_per_seg;
+          const int32_t kc = (q % P.kb_per_seg) * BK;
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* am = &P.tmA[P.a_idx_gm * u.gm + P.a_idx_gn * u.gn + P.a_idx_s * s];
+          const CUtensorMap* bm = &P.tmB[P.b_idx_gm * u.gm + P.b_idx_gn * u.gn + P.b_idx_s * s];
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+          const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
+          const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
+          if (A_MN) {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kc);
+          } else {
+            tma_load_2d(sa, am, fb, kc, arow);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kc);
+          } else {
+            tma_load_2d(sb, bm, fb, kc, bcol);
+          }
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every armed stage's last phase completes once its bytes have landed.
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) drain_wait(full_bar(s), (armed_parity >> s) & 1u, P.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < P.num_units && ok; t += gridDim.x) {
+        const Unit u = decode_unit(P, t);
+        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, P, abort_flag, 2u)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int32_t q = u.q0; q < u.q1; ++q) {
+          if (!wait_bar(full_bar(stage), phase, P, abort_flag, 3u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
+          const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t ad = A_MN ? make_sw128_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                     : make_sw128_desc(sa + kk * (UMMA_K * 2), 16, 1024);
+            const uint64_t bd = B_MN ? make_sw128_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                     : make_sw128_desc(sb + kk * (UMMA_K * 2), 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (q > u.q0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs issued by this thread complete before TMEM is freed.
+      umma_commit(drain_bar);
+      drain_wait(drain_bar, 0, P.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = 32 * q + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int32_t t = blockIdx.x; t < P.num_units; t += gridDim.x) {
+      const Unit u = decode_unit(P, t);
+      bool ok = wait_bar(tfull_bar(acc), acc_phase, P, abort_flag, 4u);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      tc_fence_after();
+
+      const int32_t g = u.gm * P.Gn + u.gn;
+      const int32_t gi = u.mt * BM + row_in_tile;  // GEMM row within the group
+      const bool row_ok = gi < P.rows_g;
+      const int32_t sp = t % P.n_split;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += Cfg::CW) {
+        uint32_t r[32];
+        if constexpr (Cfg::CW == 32) {
+          tmem_ld_32x32b_x32(t_row + c0, r);
+        } else {
+          tmem_ld_32x32b_x16(t_row + c0, r);
+        }
+        tmem_wait_ld();
+        if (!row_ok) continue;
+        const int32_t gj0 = u.nt * BN + c0;
+        if (P.n_split > 1) {
+          // raw fp32 partial, dense, in output orientation
+          float* part = P.partial + static_cast<int64_t>(sp * P.Gm * P.Gn + g) *
+                                        static_cast<int64_t>(P.rows_g) * P.cols_g;
+          if (OUT_T) {
+#pragma unroll
+            for (int i = 0; i < Cfg::CW; ++i) {
+              const int32_t gj = gj0 + i;
+              if (gj < P.cols_g) part[static_cast<int64_t>(gj) * P.rows_g + gi] = __uint_as_float(r[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < Cfg::CW; i += 4) {
+              const int32_t gj = gj0 + i;
+              if (gj < P.cols_g)
+                *reinterpret_cast<float4*>(part + static_cast<int64_t>(gi) * P.cols_g + gj) =
+                    make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+            }
+          }
+          continue;
+        }
+        if (OUT_T) {
+#pragma unroll
+          for (int i = 0; i < Cfg::CW; ++i) {
+            const int32_t gj = gj0 + i;
+            if (gj < P.cols_g) {
+              const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
+              const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
+              for (int rep = 0; rep < P.n_rep; ++rep)
+                epi_store1(P, __uint_as_float(r[i]), P.out[g + rep], P.aux[g], off_o, off_a);
+            }
+          }
+        } else {
+          const size_t esz = P.out_f32 ? 4 : 2;
+#pragma unroll
+          for (int i = 0; i < Cfg::CW; i += 8) {
+            const int32_t gj = gj0 + i;
+            if (gj >= P.cols_g) continue;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[i + e]);
+            void* auxp = nullptr;
+            if (P.epi != EPI_NONE && P.aux[g] != nullptr) {
+              const size_t aesz = (P.epi == EPI_DGELU) ? 2 : esz;
+              auxp = static_cast<uint8_t*>(P.aux[g]) +
+                     (static_cast<int64_t>(gi) * P.ld_aux + gj) * static_cast<int64_t>(aesz);
+            }
+            epi8(P, v, auxp);
+            for (int rep = 0; rep < P.n_rep; ++rep) {
+              uint8_t* dst = static_cast<uint8_t*>(P.out[g + rep]) +
+                             (static_cast<int64_t>(gi) * P.ld_out + gj) * static_cast<int64_t>(esz);
+              store8(dst, P.out_f32 != 0, v);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------- split-K stage 2
+
+struct ReduceParams {
+  void* out[MAX_GROUPS];
+  void* aux[MAX_GROUPS];
+  const float* partial;
+  int32_t G;          // groups
+  int32_t A, B;       // output-orientation extents of one group (B contiguous)
+  int64_t ld_out, ld_aux;
+  int32_t out_f32, epi, n_split, n_rep;
+};
+
+// out[g][a, b] = epilogue( sum_{s=0}^{n_split-1} partial[s][g][a][b] ), the
+// partials summed in split order; 4 consecutive b per thread.
+__global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) {
+  const int64_t per_group = static_cast<int64_t>(R.A) * R.B;
+  const int64_t total4 = static_cast<int64_t>(R.G) * per_group / 4;
+  const int64_t split_stride = static_cast<int64_t>(R.G) * per_group;
+  for (int64_t i4 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i4 < total4;
+       i4 += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i4 * 4;
+    float4 acc = *reinterpret_cast<const float4*>(R.partial + e);
+    for (int s = 1; s < R.n_split; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(R.partial + s * split_stride + e);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int32_t g = static_cast<int32_t>(e / per_group);
+    const int64_t rem = e % per_group;
+    const int64_t a = rem / R.B;
+    const int64_t b = rem % R.B;
+    float v[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (R.epi == EPI_GELU) {
+      if (R.aux[g] != nullptr) {
+        if (R.out_f32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(R.aux[g]) + a * R.ld_aux + b) = acc;
+        } else {
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(R.aux[g]) + a * R.ld_aux + b) =
+              make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = gelu_f(v[i]);
+    } else if (R.epi == EPI_DGELU) {
+      const uint2 h = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(R.aux[g]) +
+                                                      a * R.ld_aux + b);
+      v[0] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(h.x & 0xFFFFu)));
+      v[1] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(h.x >> 16)));
+      v[2] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(h.y & 0xFFFFu)));
+      v[3] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(h.y >> 16)));
+    }
+    for (int rep = 0; rep < R.n_rep; ++rep) {
+      if (R.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(R.out[g + rep]) + a * R.ld_out + b) =
+            make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(R.out[g + rep]) + a * R.ld_out + b) =
+            make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+      }
+    }
+  }
+}
+
+}  // namespace tpf

@@ -1,0 +1,849 @@
+// C-ABI of the sharded-Linear library: argument checks, launch plans
+// (tensor maps, tile space, chunk order, split-K), launches, the chunk
+// scheduler and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/tp_fused.h"
+#include "gemm_kernel.cuh"
+
+using namespace tpf;
+
+namespace {
+
+// ------------------------------------------------------------------ constants
+
+constexpr int kMaxP = 8;
+constexpr int kPlanSMs = 152;            // SM count the split-K plan assumes (GB300)
+constexpr size_t kStatusBytes = 256;     // workspace head: status word, padded
+constexpr int kStagesWide = 4;           // 128x256 tiles: 48 KiB per stage
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// ------------------------------------------------------------------ small helpers
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t device_timeout_ns() {
+  static uint64_t v = []() -> uint64_t {
+    const char* e = std::getenv("TP_DEVICE_TIMEOUT_MS");
+    if (e != nullptr) {
+      const long long ms = std::atoll(e);
+      if (ms > 0) return static_cast<uint64_t>(ms) * 1000000ull;
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct DevInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+tp_status device_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return TP_ERR_CUDA;
+  if (major != 10 || minor != 3) return TP_ERR_ARCH;
+  out->sms = sms;
+  out->ok = true;
+  return TP_OK;
+}
+
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per
+// row, `outer` rows, row pitch `ld` elements; box = 64 x box_outer.
+bool encode_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
+                int box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ kernel variants
+
+enum Variant : int {
+  V_KN = 0,    // A K-major, B MN-major (X . W forward), 128x256
+  V_KK = 1,    // A K-major, B K-major (dY . W^T), 128x256
+  V_MM = 2,    // A MN-major, B MN-major (X^T . dY weight gradient), 128x256
+  V_SW_MK16,   // swapped: A = W (MN-major), B = tokens (K-major), token tile 16/32/64
+  V_SW_MK32,
+  V_SW_MK64,
+  V_SW_KK16,   // swapped: A = W (K-major), B = tokens (K-major)
+  V_SW_KK32,
+  V_SW_KK64,
+};
+
+template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
+cudaError_t launch_t(const GemmParams& P, int grid, cudaStream_t s) {
+  using Cfg = GemmCfg<A_MN, B_MN, BN, OUT_T, STAGES>;
+  auto k = tp_gemm_kernel<A_MN, B_MN, BN, OUT_T, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  k<<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(P);
+  return cudaGetLastError();
+}
+
+constexpr int stages_for(int bn) { return std::min(12, (220 * 1024) / (128 * 128 + bn * 128)); }
+
+cudaError_t launch_variant(int v, const GemmParams& P, int grid, cudaStream_t s) {
+  switch (v) {
+    case V_KN: return launch_t<false, true, 256, false, kStagesWide>(P, grid, s);
+    case V_KK: return launch_t<false, false, 256, false, kStagesWide>(P, grid, s);
+    case V_MM: return launch_t<true, true, 256, false, kStagesWide>(P, grid, s);
+    case V_SW_MK16: return launch_t<true, false, 16, true, stages_for(16)>(P, grid, s);
+    case V_SW_MK32: return launch_t<true, false, 32, true, stages_for(32)>(P, grid, s);
+    case V_SW_MK64: return launch_t<true, false, 64, true, stages_for(64)>(P, grid, s);
+    case V_SW_KK16: return launch_t<false, false, 16, true, stages_for(16)>(P, grid, s);
+    case V_SW_KK32: return launch_t<false, false, 32, true, stages_for(32)>(P, grid, s);
+    case V_SW_KK64: return launch_t<false, false, 64, true, stages_for(64)>(P, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ launch shapes
+
+// Shape of one GEMM launch; everything the split-K and workspace decisions
+// need, computed from sizes alone (no pointers).
+struct Shape {
+  bool swap = false;     // operand-swapped: tokens are the GEMM N axis
+  int bn = 256;          // tile N (token tile when swapped)
+  int Gm = 1, Gn = 1, S = 1;
+  int64_t rows_g = 0, cols_g = 0, kseg = 0;
+  int64_t chunk_tiles = 1;
+  int64_t m_tiles = 0, n_tiles = 0, units0 = 0, kb_total = 0;
+  int n_split = 1;
+  int64_t kb_per_split = 0;
+  bool empty() const { return rows_g == 0 || cols_g == 0; }
+  size_t partial_bytes() const {
+    return n_split > 1 ? static_cast<size_t>(n_split) * Gm * Gn * rows_g * cols_g * 4u : 0;
+  }
+};
+
+void finish_shape(Shape* s) {
+  s->m_tiles = cdiv(s->rows_g, BM);
+  s->n_tiles = cdiv(s->cols_g, s->bn);
+  s->units0 = static_cast<int64_t>(s->Gm) * s->Gn * s->m_tiles * s->n_tiles;
+  s->kb_total = s->S * cdiv(s->kseg, BK);
+  s->n_split = 1;
+  s->kb_per_split = s->kb_total;
+  if (s->units0 == 0 || s->kb_total == 0) return;
+  if (s->units0 < kPlanSMs) {
+    // Deterministic split-K: choose the split that fills the SMs best, with
+    // at least 4 k-blocks per split and at most 16 splits.
+    double best_eff = 0.0;
+    int best = 1;
+    for (int ns = 1; ns <= 16; ++ns) {
+      if (ns > 1 && s->kb_total / ns < 4) break;
+      const int64_t u = s->units0 * ns;
+      const double eff = static_cast<double>(u) / (cdiv(u, kPlanSMs) * kPlanSMs);
+      if (eff > best_eff + 0.02) {
+        best_eff = eff;
+        best = ns;
+      }
+    }
+    if (best > 1) {
+      s->kb_per_split = cdiv(s->kb_total, best);
+      s->n_split = static_cast<int>(cdiv(s->kb_total, s->kb_per_split));
+    }
+  }
+}
+
+// Chunk used by a call: 0 -> scheduler; clamp to M.
+int64_t resolve_chunk(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m) {
+  if (chunk_m == 0) chunk_m = tp_choose_chunk_m(op, p, M, N, K);
+  return std::max<int64_t>(1, std::min<int64_t>(chunk_m, std::max<int64_t>(M, 1)));
+}
+
+// Token-axis tiling of a chunk: swapped kernel below 128 rows.
+void apply_chunk(Shape* s, int64_t chunk) {
+  if (chunk < BM) {
+    s->swap = true;
+    s->bn = chunk <= 16 ? 16 : chunk <= 32 ? 32 : 64;
+  } else {
+    s->swap = false;
+    s->bn = 256;
+    s->chunk_tiles = cdiv(chunk, BM);
+  }
+}
+
+// Shapes of the launches an op makes, in launch order.
+std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m) {
+  std::vector<Shape> v;
+  const int64_t chunk = resolve_chunk(op, p, M, N, K, chunk_m);
+  const int64_t Mp = (p > 0) ? M / p : 0;
+  Shape s;
+  auto tok = [&](int64_t rows_tok, int64_t other, int gtok, int goth) {
+    // tokens along GEMM M (standard) or GEMM N (swapped)
+    apply_chunk(&s, chunk);
+    if (!s.swap) {
+      s.rows_g = rows_tok; s.cols_g = other; s.Gm = gtok; s.Gn = goth;
+    } else {
+      s.rows_g = other; s.cols_g = rows_tok; s.Gm = goth; s.Gn = gtok;
+    }
+  };
+  switch (op) {
+    case TP_OP_ROW_AR:
+      s.S = p; s.kseg = K; tok(M, N, 1, 1); break;
+    case TP_OP_ROW_RS:
+      s.S = p; s.kseg = K; tok(Mp, N, p, 1); break;
+    case TP_OP_COL_FWD:
+      s.S = 1; s.kseg = K; tok(M, N, 1, p); break;
+    case TP_OP_AG_MM:
+      s.S = 1; s.kseg = K; tok(Mp, N, p, p); break;
+    case TP_OP_COL_BWD: {
+      s.S = p; s.kseg = N; tok(M, K, 1, 1);
+      finish_shape(&s);
+      v.push_back(s);
+      Shape w;  // dA_k = X^T . dY_k : [K, N] per k, contraction over M
+      w.S = 1; w.kseg = M; w.rows_g = K; w.cols_g = N; w.Gm = 1; w.Gn = p;
+      w.chunk_tiles = cdiv(K, BM);
+      finish_shape(&w);
+      v.push_back(w);
+      return v;
+    }
+    case TP_OP_ROW_BWD: {
+      s.S = 1; s.kseg = N; tok(M, K, 1, p);
+      finish_shape(&s);
+      v.push_back(s);
+      Shape w;  // dA_k = X_k^T . dY : [K, N] per k
+      w.S = 1; w.kseg = M; w.rows_g = K; w.cols_g = N; w.Gm = p; w.Gn = 1;
+      w.chunk_tiles = cdiv(K, BM);
+      finish_shape(&w);
+      v.push_back(w);
+      return v;
+    }
+  }
+  finish_shape(&s);
+  v.push_back(s);
+  return v;
+}
+
+size_t workspace_for(const std::vector<Shape>& shapes) {
+  size_t need = 0;
+  for (const Shape& s : shapes) need = std::max(need, s.partial_bytes());
+  return kStatusBytes + need;
+}
+
+// ------------------------------------------------------------------ launching a plan
+
+struct Launch {
+  Shape shape;
+  GemmParams P;
+  int variant = V_KN;
+};
+
+void init_params(GemmParams* P) { std::memset(P, 0, sizeof(*P)); }
+
+void fill_common(GemmParams* P, const Shape& s) {
+  P->Gm = s.Gm;
+  P->Gn = s.Gn;
+  P->m_tiles = static_cast<int32_t>(s.m_tiles);
+  P->n_tiles = static_cast<int32_t>(s.n_tiles);
+  P->chunk_tiles = static_cast<int32_t>(s.swap ? 1 : std::min<int64_t>(s.chunk_tiles, s.Gm * s.m_tiles));
+  P->chunk_on_n = s.swap ? 1 : 0;
+  P->S = s.S;
+  P->kb_per_seg = static_cast<int32_t>(cdiv(s.kseg, BK));
+  P->n_split = s.n_split;
+  P->kb_per_split = static_cast<int32_t>(s.kb_per_split);
+  P->num_units = static_cast<int32_t>(s.units0 * s.n_split);
+  P->rows_g = static_cast<int32_t>(s.rows_g);
+  P->cols_g = static_cast<int32_t>(s.cols_g);
+  P->n_rep = 1;
+  P->timeout_ns = device_timeout_ns();
+}
+
+size_t esize(tp_dtype d) { return d == TP_FP32 ? 4 : 2; }
+
+tp_status run_launch(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
+                     const DevInfo& di) {
+  const Shape& s = L.shape;
+  if (s.empty()) return TP_OK;
+  GemmParams& P = L.P;
+  P.status = static_cast<uint32_t*>(ws);
+  P.out_f32 = out_dtype == TP_FP32 ? 1 : 0;
+  if (s.kb_total == 0) {
+    // K == 0: the product is zero; GeLU(0) = 0 and G * GeLU'(.) = 0 too.
+    const int G = s.Gm * s.Gn;
+    const int64_t A = s.swap ? s.cols_g : s.rows_g;
+    const int64_t B = s.swap ? s.rows_g : s.cols_g;
+    for (int g = 0; g < G; ++g) {
+      for (int r = 0; r < (g == 0 ? P.n_rep : 1); ++r) {
+        if (cudaMemset2DAsync(P.out[g + r], P.ld_out * esize(out_dtype), 0, B * esize(out_dtype), A,
+                              stream) != cudaSuccess)
+          return TP_ERR_CUDA;
+      }
+      if (P.epi == EPI_GELU && P.aux[g] != nullptr) {
+        if (cudaMemset2DAsync(P.aux[g], P.ld_aux * esize(out_dtype), 0, B * esize(out_dtype), A,
+                              stream) != cudaSuccess)
+          return TP_ERR_CUDA;
+      }
+    }
+    return TP_OK;
+  }
+  if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  const int grid = static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
+  if (launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
+  if (s.n_split > 1) {
+    ReduceParams R;
+    std::memset(&R, 0, sizeof(R));
+    for (int g = 0; g < MAX_GROUPS; ++g) {
+      R.out[g] = P.out[g];
+      R.aux[g] = P.aux[g];
+    }
+    R.partial = P.partial;
+    R.G = s.Gm * s.Gn;
+    R.A = static_cast<int32_t>(s.swap ? s.cols_g : s.rows_g);
+    R.B = static_cast<int32_t>(s.swap ? s.rows_g : s.cols_g);
+    R.ld_out = P.ld_out;
+    R.ld_aux = P.ld_aux;
+    R.out_f32 = P.out_f32;
+    R.epi = P.epi;
+    R.n_split = s.n_split;
+    R.n_rep = P.n_rep;
+    const int64_t total4 = static_cast<int64_t>(R.G) * R.A * R.B / 4;
+    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(total4, 256), di.sms * 8)));
+    tp_splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(R);
+    if (cudaGetLastError() != cudaSuccess) return TP_ERR_CUDA;
+  }
+  return TP_OK;
+}
+
+// ------------------------------------------------------------------ validation
+
+struct Range {
+  const void* p;
+  size_t bytes;
+};
+
+bool overlap(const Range& a, const Range& b) {
+  if (a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool any_overlap(const std::vector<Range>& outs, const std::vector<Range>& ins) {
+  for (size_t i = 0; i < outs.size(); ++i) {
+    for (const Range& r : ins)
+      if (overlap(outs[i], r)) return true;
+    for (size_t j = i + 1; j < outs.size(); ++j)
+      if (overlap(outs[i], outs[j])) return true;
+  }
+  return false;
+}
+
+tp_status check_sizes(int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype dt) {
+  if (p < 1 || p > kMaxP) return TP_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || chunk_m < 0) return TP_ERR_INVALID_ARG;
+  if (dt != TP_BF16 && dt != TP_FP32) return TP_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (M > lim || N > lim || K > lim || static_cast<int64_t>(p) * K > lim) return TP_ERR_UNSUPPORTED_SHAPE;
+  if (N % 8 != 0 || K % 8 != 0) return TP_ERR_ALIGNMENT;
+  return TP_OK;
+}
+
+tp_status check_ptrs(const void* const* a, int n, bool need) {
+  if (!need) return TP_OK;
+  if (a == nullptr) return TP_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (a[i] == nullptr) return TP_ERR_INVALID_ARG;
+    if (!aligned16(a[i])) return TP_ERR_ALIGNMENT;
+  }
+  return TP_OK;
+}
+
+tp_status check_ptr(const void* a, bool need) {
+  if (!need) return TP_OK;
+  if (a == nullptr) return TP_ERR_INVALID_ARG;
+  return aligned16(a) ? TP_OK : TP_ERR_ALIGNMENT;
+}
+
+tp_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr) return TP_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return TP_ERR_ALIGNMENT;
+  if (ws_bytes < need) return TP_ERR_WORKSPACE_TOO_SMALL;
+  return TP_OK;
+}
+
+#define TP_TRY(expr)                     \
+  do {                                   \
+    tp_status _st = (expr);              \
+    if (_st != TP_OK) return _st;        \
+  } while (0)
+
+void add_ranges(std::vector<Range>* v, const void* const* a, int n, size_t bytes) {
+  if (a == nullptr) return;
+  for (int i = 0; i < n; ++i)
+    if (a[i] != nullptr) v->push_back({a[i], bytes});
+}
+
+int sw_variant_mk(int bn) { return bn == 16 ? V_SW_MK16 : bn == 32 ? V_SW_MK32 : V_SW_MK64; }
+int sw_variant_kk(int bn) { return bn == 16 ? V_SW_KK16 : bn == 32 ? V_SW_KK32 : V_SW_KK64; }
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* tp_status_string(tp_status s) {
+  switch (s) {
+    case TP_OK: return "ok";
+    case TP_ERR_INVALID_ARG: return "invalid argument (p, size, null pointer, aliasing or enum)";
+    case TP_ERR_ALIGNMENT: return "pointer or row pitch not 16-byte aligned (K and N must be multiples of 8)";
+    case TP_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (M must be divisible by p for ReduceScatter/AllGather; sizes < 2^31)";
+    case TP_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than tp_workspace_size()";
+    case TP_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case TP_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case TP_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out (latched in the workspace)";
+  }
+  return "unknown status";
+}
+
+double tp_pipeline_time(double c, double m, int64_t n_chunks) {
+  if (n_chunks <= 0) return 0.0;
+  return c + static_cast<double>(n_chunks - 1) * std::max(c, m) + m;
+}
+
+int64_t tp_num_chunks(int64_t M, int64_t chunk_m) {
+  if (M <= 0) return 0;
+  if (chunk_m <= 0) chunk_m = M;
+  const int64_t c = std::min(chunk_m, M);
+  return cdiv(M, c);
+}
+
+int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K) {
+  if (M <= 0) return 0;
+  if (p < 1) p = 1;
+  // Model constants: dense bf16 tensor rate and HBM copy rate of a GB300,
+  // and the L2 capacity below which a weight set is streamed once per call.
+  const double peak = 1.9e15, bw = 6.7e12, l2 = 96.0 * (1 << 20);
+  double flops = 0, wbytes = 0, in_row = 0, out_row = 0;
+  switch (op) {
+    case TP_OP_ROW_AR: case TP_OP_ROW_RS:
+      flops = 2.0 * M * N * K * p; wbytes = 2.0 * K * N * p; in_row = 2.0 * K * p; out_row = 2.0 * N; break;
+    case TP_OP_COL_FWD: case TP_OP_AG_MM:
+      flops = 2.0 * M * N * K * p; wbytes = 2.0 * K * N * p; in_row = 2.0 * K; out_row = 2.0 * N * p; break;
+    case TP_OP_COL_BWD:
+      flops = 2.0 * M * N * K * p; wbytes = 2.0 * K * N * p; in_row = 2.0 * N * p; out_row = 2.0 * K; break;
+    case TP_OP_ROW_BWD:
+      flops = 2.0 * M * N * K * p; wbytes = 2.0 * K * N * p; in_row = 2.0 * N; out_row = 2.0 * K * p; break;
+  }
+  std::vector<int64_t> cand;
+  for (int64_t c = 16; c < M; c *= 2) cand.push_back(c);
+  cand.push_back(M);
+  int64_t best = M;
+  double best_t = 1e300;
+  for (int64_t c : cand) {
+    const int64_t rows = std::min(c, M);
+    const int64_t n = cdiv(M, rows);
+    const double eff = rows >= BM ? 1.0 : static_cast<double>(cdiv(rows, 16) * 16) / BM;
+    const double wb = wbytes > l2 ? wbytes : wbytes / n;
+    const double cc = std::max(flops * rows / M / (peak * eff), (wb + rows * in_row) / bw);
+    const double mm = rows * out_row / bw;
+    const double t = tp_pipeline_time(cc, mm, n);
+    if (t < best_t * (1.0 - 1e-9)) {
+      best_t = t;
+      best = c;
+    }
+  }
+  return std::min(best, M);
+}
+
+size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m) {
+  if (p < 1 || p > kMaxP || M < 0 || N < 0 || K < 0 || chunk_m < 0) return kStatusBytes;
+  if ((op == TP_OP_ROW_RS || op == TP_OP_AG_MM) && M % p != 0) return kStatusBytes;
+  return workspace_for(op_shapes(op, p, M, N, K, chunk_m));
+}
+
+tp_status tp_get_device_status(void* ws, cudaStream_t stream) {
+  if (ws == nullptr) return TP_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TP_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TP_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return TP_ERR_CUDA;
+    return TP_ERR_DEVICE_TIMEOUT;
+  }
+  return TP_OK;
+}
+
+// ---------------------------------------------------------------- row parallel
+
+static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* w, void* const* y,
+                              int n_out, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                              tp_dtype dt, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, dt));
+  if (rs) {
+    if (M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
+    n_out = p;
+  } else if (n_out != 1 && n_out != p) {
+    return TP_ERR_INVALID_ARG;
+  }
+  const bool work = M > 0 && N > 0;
+  TP_TRY(check_ptrs(x, p, work && K > 0));
+  TP_TRY(check_ptrs(w, p, work && K > 0));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(y), n_out, work));
+  const tp_op op = rs ? TP_OP_ROW_RS : TP_OP_ROW_AR;
+  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  if (!work) return TP_OK;
+  const int64_t Mp = M / p;
+  {
+    std::vector<Range> ins, outs;
+    add_ranges(&ins, x, p, M * K * 2);
+    add_ranges(&ins, w, p, K * N * 2);
+    add_ranges(&outs, const_cast<const void* const*>(y), n_out, (rs ? Mp : M) * N * esize(dt));
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  Launch L;
+  L.shape = shapes[0];
+  init_params(&L.P);
+  fill_common(&L.P, L.shape);
+  GemmParams& P = L.P;
+  const Shape& s = L.shape;
+  if (K > 0) {
+    for (int r = 0; r < p; ++r) {
+      if (!s.swap) {
+        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM) || !encode_map(&P.tmB[r], w[r], N, K, N, 64))
+          return TP_ERR_CUDA;
+      } else {
+        if (!encode_map(&P.tmA[r], w[r], N, K, N, 64) || !encode_map(&P.tmB[r], x[r], K, M, K, s.bn))
+          return TP_ERR_CUDA;
+      }
+    }
+  }
+  P.a_idx_s = 1;
+  P.b_idx_s = 1;
+  P.ld_out = N;
+  P.epi = EPI_NONE;
+  if (!rs) {
+    for (int i = 0; i < n_out; ++i) P.out[i] = y[i];
+    P.n_rep = n_out;
+  } else {
+    for (int j = 0; j < p; ++j) P.out[j] = y[j];
+    if (!s.swap) P.a_row_gm = static_cast<int32_t>(Mp);
+    else P.b_col_gn = static_cast<int32_t>(Mp);
+  }
+  L.variant = s.swap ? sw_variant_mk(s.bn) : V_KN;
+  return run_launch(L, dt, ws, stream, di);
+}
+
+tp_status tp_row_linear_fwd_allreduce(const void* const* x, const void* const* w, void* const* y,
+                                      int n_out, int p, int64_t M, int64_t N, int64_t K,
+                                      int64_t chunk_m, tp_dtype out_dtype, void* ws,
+                                      size_t ws_bytes, cudaStream_t stream) {
+  return row_fwd_impl(false, x, w, y, n_out, p, M, N, K, chunk_m, out_dtype, ws, ws_bytes, stream);
+}
+
+tp_status tp_row_linear_fwd_reducescatter(const void* const* x, const void* const* w,
+                                          void* const* y, int p, int64_t M, int64_t N, int64_t K,
+                                          int64_t chunk_m, tp_dtype out_dtype, void* ws,
+                                          size_t ws_bytes, cudaStream_t stream) {
+  return row_fwd_impl(true, x, w, y, p, p, M, N, K, chunk_m, out_dtype, ws, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------- column parallel
+
+static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, const void* const* w,
+                              void* const* y, void* const* preact, tp_epilogue epi, int p,
+                              int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype dt,
+                              void* ws, size_t ws_bytes, cudaStream_t stream, void* x_gathered) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, dt));
+  if (epi != TP_EPI_NONE && epi != TP_EPI_GELU) return TP_ERR_INVALID_ARG;
+  if (ag && M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
+  const bool work = M > 0 && N > 0;
+  if (ag) TP_TRY(check_ptrs(xs, p, M > 0 && (K > 0) && (work || x_gathered != nullptr)));
+  else TP_TRY(check_ptr(x1, work && K > 0));
+  TP_TRY(check_ptrs(w, p, work && K > 0));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(y), p, work));
+  const bool want_h = epi == TP_EPI_GELU && preact != nullptr;
+  TP_TRY(check_ptrs(const_cast<const void* const*>(preact), p, work && want_h));
+  TP_TRY(check_ptr(x_gathered, x_gathered != nullptr));
+  const tp_op op = ag ? TP_OP_AG_MM : TP_OP_COL_FWD;
+  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  const int64_t Mp = M / p;
+  {
+    std::vector<Range> ins, outs;
+    if (ag) add_ranges(&ins, xs, p, Mp * K * 2);
+    else if (x1 != nullptr) ins.push_back({x1, static_cast<size_t>(M * K * 2)});
+    add_ranges(&ins, w, p, K * N * 2);
+    add_ranges(&outs, const_cast<const void* const*>(y), p, M * N * esize(dt));
+    if (want_h) add_ranges(&outs, const_cast<const void* const*>(preact), p, M * N * esize(dt));
+    if (x_gathered != nullptr) outs.push_back({x_gathered, static_cast<size_t>(M * K * 2)});
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  if (!work && x_gathered == nullptr) return TP_OK;
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  if (ag && x_gathered != nullptr && M > 0 && K > 0) {
+    for (int s = 0; s < p; ++s)
+      if (cudaMemcpyAsync(static_cast<uint8_t*>(x_gathered) + s * Mp * K * 2, xs[s], Mp * K * 2,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return TP_ERR_CUDA;
+  }
+  if (!work) return TP_OK;
+  Launch L;
+  L.shape = shapes[0];
+  init_params(&L.P);
+  fill_common(&L.P, L.shape);
+  GemmParams& P = L.P;
+  const Shape& s = L.shape;
+  const size_t es = esize(dt);
+  if (K > 0) {
+    for (int k = 0; k < p; ++k) {
+      // weights: MN-major in both orientations ([K, N] row-major)
+      CUtensorMap* wm = s.swap ? &P.tmA[k] : &P.tmB[k];
+      if (!encode_map(wm, w[k], N, K, N, 64)) return TP_ERR_CUDA;
+    }
+    const int tok_box = s.swap ? s.bn : BM;
+    if (!ag) {
+      CUtensorMap* xm = s.swap ? &P.tmB[0] : &P.tmA[0];
+      if (!encode_map(xm, x1, K, M, K, tok_box)) return TP_ERR_CUDA;
+    } else {
+      for (int t = 0; t < p; ++t) {
+        CUtensorMap* xm = s.swap ? &P.tmB[t] : &P.tmA[t];
+        if (!encode_map(xm, xs[t], K, Mp, K, tok_box)) return TP_ERR_CUDA;
+      }
+    }
+  }
+  P.ld_out = N;
+  P.ld_aux = N;
+  P.epi = epi == TP_EPI_GELU ? EPI_GELU : EPI_NONE;
+  if (!ag) {
+    if (!s.swap) P.b_idx_gn = 1;   // groups along N are the shards k
+    else P.a_idx_gm = 1;           // groups along M are the shards k
+    for (int k = 0; k < p; ++k) {
+      P.out[k] = y[k];
+      P.aux[k] = want_h ? preact[k] : nullptr;
+    }
+  } else {
+    // group (gm, gn): standard gm = source shard s, gn = shard k;
+    //                 swapped  gm = shard k,        gn = source shard s.
+    if (!s.swap) { P.a_idx_gm = 1; P.b_idx_gn = 1; }
+    else { P.a_idx_gm = 1; P.b_idx_gn = 1; }
+    for (int gm = 0; gm < p; ++gm) {
+      for (int gn = 0; gn < p; ++gn) {
+        const int k = s.swap ? gm : gn;
+        const int src = s.swap ? gn : gm;
+        const int64_t off = static_cast<int64_t>(src) * Mp * N * es;
+        P.out[gm * p + gn] = static_cast<uint8_t*>(y[k]) + off;
+        P.aux[gm * p + gn] = want_h ? static_cast<uint8_t*>(preact[k]) + off : nullptr;
+      }
+    }
+  }
+  L.variant = s.swap ? sw_variant_mk(s.bn) : V_KN;
+  return run_launch(L, dt, ws, stream, di);
+}
+
+tp_status tp_col_linear_fwd(const void* x, const void* const* w, void* const* y,
+                            void* const* preact, tp_epilogue epi, int p, int64_t M, int64_t N,
+                            int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  return col_like_fwd(false, nullptr, x, w, y, preact, epi, p, M, N, K, chunk_m, out_dtype, ws,
+                      ws_bytes, stream, nullptr);
+}
+
+tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* y,
+                       void* x_gathered, tp_epilogue epi, void* const* preact, int p, int64_t M,
+                       int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  return col_like_fwd(true, x, nullptr, w, y, preact, epi, p, M, N, K, chunk_m, out_dtype, ws,
+                      ws_bytes, stream, x_gathered);
+}
+
+// ---------------------------------------------------------------- backward
+
+// Weight gradient dA_g = Xsrc_g^T . dYsrc_g for g = 0..p-1 ([K, N] each,
+// contraction over the M tokens); both operands MN-major.
+static tp_status weight_grad(const Shape& s, const void* const* xk, const void* x1,
+                             const void* const* dyk, const void* dy1, void* const* dw, int p,
+                             int64_t M, int64_t N, int64_t K, tp_dtype dt, void* ws,
+                             cudaStream_t stream, const DevInfo& di) {
+  Launch L;
+  L.shape = s;
+  init_params(&L.P);
+  fill_common(&L.P, s);
+  GemmParams& P = L.P;
+  if (M > 0) {
+    for (int k = 0; k < (xk ? p : 1); ++k)
+      if (!encode_map(&P.tmA[k], xk ? xk[k] : x1, K, M, K, 64)) return TP_ERR_CUDA;
+    for (int k = 0; k < (dyk ? p : 1); ++k)
+      if (!encode_map(&P.tmB[k], dyk ? dyk[k] : dy1, N, M, N, 64)) return TP_ERR_CUDA;
+  }
+  // the p problems are the groups (along N for the column case, along M for the row case)
+  if (s.Gn == p && s.Gm == 1) {
+    P.a_idx_gn = xk ? 1 : 0;
+    P.b_idx_gn = dyk ? 1 : 0;
+  } else {
+    P.a_idx_gm = xk ? 1 : 0;
+    P.b_idx_gm = dyk ? 1 : 0;
+  }
+  for (int k = 0; k < p; ++k) P.out[k] = dw[k];
+  P.ld_out = N;
+  P.epi = EPI_NONE;
+  L.variant = V_MM;
+  return run_launch(L, dt, ws, stream, di);
+}
+
+tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* const* dy, void* dx,
+                            void* const* dw, int p, int64_t M, int64_t N, int64_t K,
+                            int64_t chunk_m, tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
+  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  const bool dx_work = dx != nullptr && M > 0 && K > 0;
+  const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  TP_TRY(check_ptr(dx, dx_work));
+  TP_TRY(check_ptrs(w, p, dx_work && N > 0));
+  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptr(x, dw_work && M > 0));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
+  std::vector<Shape> shapes = op_shapes(TP_OP_COL_BWD, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  {
+    std::vector<Range> ins, outs;
+    if (x) ins.push_back({x, static_cast<size_t>(M * K * 2)});
+    add_ranges(&ins, w, p, K * N * 2);
+    add_ranges(&ins, dy, p, M * N * 2);
+    if (dx) outs.push_back({dx, static_cast<size_t>(M * K * esize(out_dtype))});
+    if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  if (!dx_work && !dw_work) return TP_OK;
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  if (dx_work) {
+    Launch L;
+    L.shape = shapes[0];
+    init_params(&L.P);
+    fill_common(&L.P, L.shape);
+    GemmParams& P = L.P;
+    const Shape& s = L.shape;
+    if (N > 0) {
+      for (int k = 0; k < p; ++k) {
+        if (!s.swap) {
+          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM) || !encode_map(&P.tmB[k], w[k], N, K, N, 256))
+            return TP_ERR_CUDA;
+        } else {
+          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM) || !encode_map(&P.tmB[k], dy[k], N, M, N, s.bn))
+            return TP_ERR_CUDA;
+        }
+      }
+    }
+    P.a_idx_s = 1;
+    P.b_idx_s = 1;
+    P.out[0] = dx;
+    P.ld_out = K;
+    P.epi = EPI_NONE;
+    L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
+    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
+  }
+  if (dw_work) TP_TRY(weight_grad(shapes[1], nullptr, x, dy, nullptr, dw, p, M, N, K, out_dtype, ws, stream, di));
+  return TP_OK;
+}
+
+tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const void* dy,
+                            void* const* dx, void* const* dw, const void* const* preact, int p,
+                            int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype,
+                            void* ws, size_t ws_bytes, cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
+  const bool dx_work = dx != nullptr && M > 0 && K > 0;
+  const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dx), p, dx_work));
+  TP_TRY(check_ptrs(w, p, dx_work && N > 0));
+  TP_TRY(check_ptr(dy, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptrs(x, p, dw_work && M > 0));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
+  TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
+  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_BWD, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  {
+    std::vector<Range> ins, outs;
+    add_ranges(&ins, x, p, M * K * 2);
+    add_ranges(&ins, w, p, K * N * 2);
+    if (dy) ins.push_back({dy, static_cast<size_t>(M * N * 2)});
+    add_ranges(&ins, preact, p, M * K * 2);
+    if (dx) add_ranges(&outs, const_cast<const void* const*>(dx), p, M * K * esize(out_dtype));
+    if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  if (!dx_work && !dw_work) return TP_OK;
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  if (dx_work) {
+    Launch L;
+    L.shape = shapes[0];
+    init_params(&L.P);
+    fill_common(&L.P, L.shape);
+    GemmParams& P = L.P;
+    const Shape& s = L.shape;
+    if (N > 0) {
+      for (int k = 0; k < p; ++k) {
+        if (!s.swap) {
+          if (!encode_map(&P.tmB[k], w[k], N, K, N, 256)) return TP_ERR_CUDA;
+        } else {
+          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM)) return TP_ERR_CUDA;
+        }
+      }
+      if (!s.swap) {
+        if (!encode_map(&P.tmA[0], dy, N, M, N, BM)) return TP_ERR_CUDA;
+      } else {
+        if (!encode_map(&P.tmB[0], dy, N, M, N, s.bn)) return TP_ERR_CUDA;
+      }
+    }
+    if (!s.swap) P.b_idx_gn = 1;
+    else P.a_idx_gm = 1;
+    for (int k = 0; k < p; ++k) {
+      P.out[k] = dx[k];
+      P.aux[k] = preact ? const_cast<void*>(preact[k]) : nullptr;
+    }
+    P.ld_out = K;
+    P.ld_aux = K;
+    P.epi = preact ? EPI_DGELU : EPI_NONE;
+    L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
+    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
+  }
+  if (dw_work) TP_TRY(weight_grad(shapes[1], x, nullptr, nullptr, dy, dw, p, M, N, K, out_dtype, ws, stream, di));
+  return TP_OK;
+}
+
+}  // extern "C"

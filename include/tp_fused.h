@@ -1,0 +1,185 @@
+/*
+ * tp_fused.h -- tensor-parallel sharded Linear on one GB300 (sm_103a).
+ *
+ * All p "ranks" of a tensor-parallel Linear live in one GPU's memory; rank
+ * r's shards are plain device pointers.  Each entry point runs the per-rank
+ * partial GEMMs fused with their cross-shard reduction (or gather): the p
+ * partials of an output tile are accumulated in one fp32 tensor-memory
+ * accumulator in rank order r = 0..p-1 and the tile is written once.  Rows
+ * are processed chunk by chunk along M (chunk-major tile order), and a
+ * tile's write-out overlaps the next tile's MMAs.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [M027] ai-infra-kb M027 "compute-communication fusion":
+ *          §01 row-parallel Linear, AllReduce vs ReduceScatter layouts,
+ *          AllGather then MatMul; §02-§03 the chunked pipeline and its
+ *          timeline; §05 small (decode) matrices.
+ *   [TP]   cnblogs zuoyang/p/22340322 "PyTorch 2.x tensor parallelism":
+ *          §2.3 column parallel, §2.4 row parallel, §2.5-2.7 collectives,
+ *          §三/§四/§六 forward and backward, §7.1 MLP block, §11.3 SP pair.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Matrices are row-major.  Weights are [in, out] (Y = X . A, [TP] §2.3).
+ *  - Tensor pointers are DEVICE pointers owned by the caller.  Pointer
+ *    arrays (x, w, y, ...) are HOST arrays of length p (or n_out); they are
+ *    read during the call only.  The library never allocates or frees
+ *    device memory on a call; all work is enqueued on `stream`.
+ *  - Inputs are bfloat16.  Outputs are bfloat16 (rounded to nearest even,
+ *    once) or float32, chosen by `out_dtype`.  Accumulation is fp32.
+ *  - 1 <= p <= 8.  Every base pointer is 16-byte aligned; every row pitch is
+ *    a multiple of 16 bytes, i.e. K and N are multiples of 8.
+ *  - `chunk_m`: rows per pipeline chunk.  0 lets the scheduler choose
+ *    (tp_choose_chunk_m); a value above M is clamped to M; the last chunk
+ *    may be short.  Chunks of 128 rows or more run on 128-row tiles; chunks
+ *    below 128 rows run the operand-swapped kernel whose token tile is the
+ *    chunk (rounded up to a multiple of 16).
+ *  - Outputs must not overlap inputs (checked; TP_ERR_INVALID_ARG).
+ *  - `ws` is a device workspace of at least tp_workspace_size(...) bytes,
+ *    16-byte aligned.  It holds the device status word and, for the split-K
+ *    path, fp32 partials.  Calls that share a workspace must be ordered
+ *    on the same stream.
+ *  - Errors: argument checks run on the host before anything is enqueued
+ *    and return a tp_status; on error nothing is launched.  A device-side
+ *    wait that runs out of time latches TP_ERR_DEVICE_TIMEOUT into the
+ *    workspace status word; tp_get_device_status() reads (and clears) it.
+ *  - Determinism: identical inputs give bitwise-identical outputs.
+ *  - Degenerate sizes: M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ */
+#ifndef TP_FUSED_H_
+#define TP_FUSED_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1,        /* bad p, size, null pointer, aliasing, enum */
+  TP_ERR_ALIGNMENT = 2,          /* base pointer or row pitch not 16-byte aligned */
+  TP_ERR_UNSUPPORTED_SHAPE = 3,  /* e.g. M % p != 0 for ReduceScatter / AllGather */
+  TP_ERR_WORKSPACE_TOO_SMALL = 4,
+  TP_ERR_ARCH = 5,               /* device is not sm_103 / sm_100 family */
+  TP_ERR_CUDA = 6,               /* a CUDA runtime or driver call failed */
+  TP_ERR_DEVICE_TIMEOUT = 7      /* a device wait ran out of time (latched) */
+} tp_status;
+
+typedef enum { TP_BF16 = 0, TP_FP32 = 1 } tp_dtype;
+
+typedef enum {
+  TP_EPI_NONE = 0,   /* write the GEMM result */
+  TP_EPI_GELU = 1,   /* write GeLU(H) (exact erf form) and optionally H */
+  TP_EPI_DGELU = 2   /* write G * GeLU'(H), H read from `preact` */
+} tp_epilogue;
+
+typedef enum {
+  TP_OP_ROW_AR = 0,  /* tp_row_linear_fwd_allreduce */
+  TP_OP_ROW_RS = 1,  /* tp_row_linear_fwd_reducescatter */
+  TP_OP_COL_FWD = 2, /* tp_col_linear_fwd */
+  TP_OP_COL_BWD = 3, /* tp_col_linear_bwd */
+  TP_OP_ROW_BWD = 4, /* tp_row_linear_bwd */
+  TP_OP_AG_MM = 5    /* tp_ag_matmul */
+} tp_op;
+
+/* Bytes of device workspace the call (op, p, M, N, K, chunk_m) needs, with
+ * M, N, K meant as in that call.  Always >= 256 (the status word). */
+size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m);
+
+/* Row-parallel forward, MatMul+AllReduce layout.  [M027 §01; TP §2.4, §四]
+ *   Y = sum_{r=0}^{p-1} X_r . W_r, accumulated in rank order, written once.
+ *   x[r]: X_r [M, K] (rank r's column block of the layer input)
+ *   w[r]: W_r [K, N] (rank r's row block of the weight)
+ *   y[i]: Y [M, N] for i < n_out.  n_out == 1 writes the full Y once;
+ *         n_out == p writes p bit-identical replicas (one per rank).    */
+tp_status tp_row_linear_fwd_allreduce(const void* const* x, const void* const* w,
+                                      void* const* y, int n_out, int p,
+                                      int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                      tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/* Row-parallel forward, MatMul+ReduceScatter layout.  [M027 §01; TP §2.7]
+ *   Same reduction; rank j receives rows [j*M/p, (j+1)*M/p) of Y.
+ *   y[j]: [M/p, N].  Requires M % p == 0.                                */
+tp_status tp_row_linear_fwd_reducescatter(const void* const* x, const void* const* w,
+                                          void* const* y, int p,
+                                          int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                          tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream);
+
+/* Column-parallel forward.  [TP §2.3, §三, §7.1]
+ *   H_k = X . A_k for k = 0..p-1 (one grouped launch, no reduction).
+ *   x: X [M, K] (replicated input); w[k]: A_k [K, N]; y[k]: [M, N].
+ *   epi == TP_EPI_NONE: y[k] = H_k.
+ *   epi == TP_EPI_GELU: y[k] = GeLU(H_k); if preact != NULL, preact[k]
+ *   ([M, N], same dtype as y) receives H_k for the backward pass.         */
+tp_status tp_col_linear_fwd(const void* x, const void* const* w, void* const* y,
+                            void* const* preact, tp_epilogue epi, int p,
+                            int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                            tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/* Column-parallel backward.  [TP §三, §六]
+ *   dX = sum_{k=0}^{p-1} dY_k . A_k^T  (the backward AllReduce, fused,
+ *        accumulated in rank order, written once) -> dx [M, K] if dx != NULL
+ *   dA_k = X^T . dY_k (local)                     -> dw[k] [K, N] if dw != NULL
+ *   x: X [M, K] (only read when dw != NULL); w[k]: A_k [K, N] (only read
+ *   when dx != NULL); dy[k]: dY_k [M, N].  At least one of dx, dw is given. */
+tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* const* dy,
+                            void* dx, void* const* dw, int p,
+                            int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                            tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/* Row-parallel backward (no reduction).  [TP §四, §六, §7.1]
+ *   dX_k = dY . A_k^T, times GeLU'(H_k) when preact != NULL -> dx[k] [M, K]
+ *   dA_k = X_k^T . dY                                        -> dw[k] [K, N]
+ *   x[k]: X_k [M, K] (only read when dw != NULL); w[k]: A_k [K, N];
+ *   dy: dY [M, N]; preact[k]: H_k [M, K] bf16 or NULL.                   */
+tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const void* dy,
+                            void* const* dx, void* const* dw, const void* const* preact,
+                            int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                            tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/* AllGather+MatMul.  [M027 §01-§02; TP §2.6, §11.3]
+ *   Y_k = [X_0; X_1; ...; X_{p-1}] . A_k.  The M-tiles of rank s's rows read
+ *   X_s directly, in shard order; the gathered X is written to x_gathered
+ *   ([M, K]) only when that pointer is non-NULL.
+ *   x[s]: X_s [M/p, K]; w[k]: A_k [K, N]; y[k]: [M, N];
+ *   epi / preact as in tp_col_linear_fwd.  Requires M % p == 0.           */
+tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* y,
+                       void* x_gathered, tp_epilogue epi, void* const* preact, int p,
+                       int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                       tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* Two-engine chunk timeline: c + (n-1) * max(c, m) + m for n >= 1, 0 for
+ * n <= 0; c = per-chunk compute time, m = per-chunk reduce time.  [M027 §03] */
+double tp_pipeline_time(double c, double m, int64_t n_chunks);
+
+/* Number of chunks ceil(M / min(chunk_m, M)) (0 when M <= 0).  [M027 §03] */
+int64_t tp_num_chunks(int64_t M, int64_t chunk_m);
+
+/* The scheduler's chunk size for a call: the candidate with the smallest
+ * modelled tp_pipeline_time, where a chunk's compute time is the larger of
+ * its tensor-core time (with the MMA-width efficiency of its tile) and its
+ * operand-streaming time, and its reduce time is the write-out of its
+ * reduced rows.  Host only; never fails (returns >= 1, or 0 when M <= 0). */
+int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K);
+
+/* Synchronises `stream`, returns the latched device status of `ws`
+ * (TP_OK or TP_ERR_DEVICE_TIMEOUT) and clears it.                         */
+tp_status tp_get_device_status(void* ws, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* tp_status_string(tp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_FUSED_H_ */

@@ -1,0 +1,149 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports
+every symbol the header declares, and its argument checks and host-only
+functions behave as documented.  No call here reaches the GPU: every error
+case is rejected by the host checks before anything is enqueued."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp_fused.h")
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import gemm_reduce_fusion_gb300 as tp
+    return tp
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["tp_row_linear_fwd_allreduce", "tp_row_linear_fwd_reducescatter", "tp_col_linear_fwd",
+              "tp_col_linear_bwd", "tp_ag_matmul", "tp_row_linear_bwd", "tp_workspace_size",
+              "tp_pipeline_time", "tp_choose_chunk_m", "tp_get_device_status", "tp_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(tp):
+    lib = ctypes.CDLL(tp.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", tp.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (tp_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_status_strings(tp):
+    for s in range(8):
+        assert tp.tp_status_string(s)
+    assert "unknown" in tp.tp_status_string(99)
+
+
+def test_pipeline_time_matches_oracle(tp):
+    for c, m, n in [(3, 2, 4), (1, 5, 4), (2, 2, 1), (0.5, 0.25, 128), (3, 2, 0)]:
+        assert tp.tp_pipeline_time(c, m, n) == oracle.pipeline_time(c, m, n)
+    assert tp.tp_pipeline_time(3, 2, 4) == 14.0   # M027 §03
+
+
+def test_num_chunks_matches_oracle(tp):
+    for M, c in [(128, 32), (130, 32), (16, 2048), (2048, 16), (2048, 64), (0, 32), (7, 7)]:
+        assert tp.tp_num_chunks(M, c) == oracle.n_chunks(M, c)
+
+
+def test_choose_chunk_m_is_valid(tp):
+    for op in range(6):
+        for p, M, N, K in [(2, 128, 2048, 1024), (4, 4096, 4096, 4096), (8, 16, 6144, 12288),
+                           (8, 2048, 12288, 6144), (1, 1, 8, 8)]:
+            c = tp.tp_choose_chunk_m(op, p, M, N, K)
+            assert 1 <= c <= M
+    assert tp.tp_choose_chunk_m(0, 2, 0, 8, 8) == 0
+    assert tp.tp_choose_chunk_m(tp.TP_OP_COL_FWD, 8, 16, 6144, 12288) == 16
+
+
+def test_workspace_size(tp):
+    assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0) >= 256
+    # a skinny call plans a split-K and needs room for fp32 partials
+    small = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 8, 16, 12288, 6144, 16)
+    assert small > 256 and (small - 256) % (16 * 12288 * 4) == 0
+    # invalid requests still return the minimum
+    assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 0, 16, 16, 16, 0) == 256
+
+
+# ---------------------------------------------------------------- host argument checks
+
+A = 1 << 20          # fake, 16-byte aligned "device" addresses: never dereferenced
+B = 1 << 30
+
+
+def arr(*ptrs):
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+def row_ar(tp, x, w, y, n_out, p, M, N, K, chunk=0, dt=0, ws=B + (1 << 28), wsb=1 << 20):
+    return tp._lib.tp_row_linear_fwd_allreduce(x, w, y, n_out, p, M, N, K, chunk, dt, ws, wsb, None)
+
+
+def test_row_ar_argument_checks(tp):
+    x = arr(A, A + 4096)
+    w = arr(A + 8192, A + 12288)
+    y = arr(A + (1 << 24))
+    M, N, K = 16, 8, 8
+    assert row_ar(tp, x, w, y, 1, 0, M, N, K) == tp.TP_ERR_INVALID_ARG          # p = 0
+    assert row_ar(tp, x, w, y, 1, 9, M, N, K) == tp.TP_ERR_INVALID_ARG          # p > 8
+    assert row_ar(tp, x, w, y, 1, 2, -1, N, K) == tp.TP_ERR_INVALID_ARG         # negative M
+    assert row_ar(tp, x, w, y, 1, 2, M, 12, K) == tp.TP_ERR_ALIGNMENT           # N % 8
+    assert row_ar(tp, x, w, y, 1, 2, M, N, 4) == tp.TP_ERR_ALIGNMENT            # K % 8
+    assert row_ar(tp, x, w, y, 3, 2, M, N, K) == tp.TP_ERR_INVALID_ARG          # n_out not 1 or p
+    assert row_ar(tp, x, w, y, 1, 2, M, N, K, dt=5) == tp.TP_ERR_INVALID_ARG    # dtype
+    assert row_ar(tp, arr(A, 0), w, y, 1, 2, M, N, K) == tp.TP_ERR_INVALID_ARG  # null shard
+    assert row_ar(tp, arr(A, A + 3), w, y, 1, 2, M, N, K) == tp.TP_ERR_ALIGNMENT
+    assert row_ar(tp, x, w, y, 1, 2, M, N, K, ws=0) == tp.TP_ERR_INVALID_ARG
+    assert row_ar(tp, x, w, y, 1, 2, M, N, K, ws=B + 8) == tp.TP_ERR_ALIGNMENT
+    assert row_ar(tp, x, w, y, 1, 2, M, N, K, wsb=16) == tp.TP_ERR_WORKSPACE_TOO_SMALL
+    # output overlapping an input shard
+    assert row_ar(tp, x, w, arr(A + 4096 + 64), 1, 2, M, N, K) == tp.TP_ERR_INVALID_ARG
+    # M == 0: nothing to do, accepted without touching the device
+    assert row_ar(tp, x, w, y, 1, 2, 0, N, K) == tp.TP_OK
+
+
+def test_rs_and_ag_need_m_divisible_by_p(tp):
+    x = arr(A, A + 4096, A + 8192)
+    w = arr(A + 65536, A + 69632, A + 73728)
+    y = arr(B, B + 4096, B + 8192)
+    st = tp._lib.tp_row_linear_fwd_reducescatter(x, w, y, 3, 16, 8, 8, 0, 0, B + (1 << 28), 1 << 20, None)
+    assert st == tp.TP_ERR_UNSUPPORTED_SHAPE
+    st = tp._lib.tp_ag_matmul(x, w, y, None, 0, None, 3, 16, 8, 8, 0, 0, B + (1 << 28), 1 << 20, None)
+    assert st == tp.TP_ERR_UNSUPPORTED_SHAPE
+
+
+def test_col_and_bwd_argument_checks(tp):
+    w = arr(A, A + 4096)
+    y = arr(B, B + 4096)
+    ws = B + (1 << 28)
+    # bad epilogue for the forward
+    assert tp._lib.tp_col_linear_fwd(A + 65536, w, y, None, 2, 2, 16, 8, 8, 0, 0, ws, 1 << 20, None) \
+        == tp.TP_ERR_INVALID_ARG
+    # GeLU with a preact list holding a null pointer
+    assert tp._lib.tp_col_linear_fwd(A + 65536, w, y, arr(B + 65536, 0), 1, 2, 16, 8, 8, 0, 0, ws,
+                                     1 << 20, None) == tp.TP_ERR_INVALID_ARG
+    # column backward without dx
+    assert tp._lib.tp_col_linear_bwd(A + 65536, w, arr(A + 131072, A + 135168), None, None, 2, 16, 8, 8,
+                                     0, 0, ws, 1 << 20, None) == tp.TP_ERR_INVALID_ARG
+    # row backward with neither output
+    assert tp._lib.tp_row_linear_bwd(None, w, A + 65536, None, None, None, 2, 16, 8, 8, 0, 0, ws,
+                                     1 << 20, None) == tp.TP_ERR_INVALID_ARG
+    # status query needs a workspace
+    assert tp._lib.tp_get_device_status(None, None) == tp.TP_ERR_INVALID_ARG

@@ -1,0 +1,350 @@
+"""GPU parity of every entry point against the CPU oracle, through the C-ABI.
+
+Sizes span several 128x256 tiles, several 64-wide k-blocks and ragged tails
+in M, N and K, for p = 1..8, both tile orientations (chunks of >= 128 rows
+and the operand-swapped kernel for chunks of 16/32/64 rows) and split-K.
+
+* integer-valued bf16 inputs (|v| <= 4): every fp32 partial sum is an exact
+  integer, so fp32 outputs must equal the oracle exactly and bf16 outputs
+  must equal the oracle's value rounded to bf16 bit for bit -- this pins
+  shard offsets, RS slices, AG routing, chunk order and tile bounds;
+* normal inputs through GeLU / GeLU': max|d|/max|ref| <= 5e-3 (bf16) or
+  1e-5 (fp32);
+* outputs sit between NaN guard bands that must survive the call.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import BF16_TOL, assert_close, dev, host_bits, host_f64
+
+pytestmark = pytest.mark.gpu
+
+PAD = 4096
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import gemm_reduce_fusion_gb300 as tp
+    return tp
+
+
+class Guarded:
+    """An output tensor with NaN guard bands on both sides."""
+
+    def __init__(self, shape, f32=False):
+        import torch
+        n = int(np.prod(shape))
+        self.full = torch.full((n + 2 * PAD,), float("nan"),
+                               dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
+        self.t = self.full[PAD:PAD + n].view(*shape)
+        self.n = n
+
+    def check_bands(self):
+        import torch
+        lo = self.full[:PAD]
+        hi = self.full[PAD + self.n:]
+        assert bool(torch.isnan(lo).all()) and bool(torch.isnan(hi).all()), "write outside the output"
+
+
+def outs(shapes, f32):
+    return [Guarded(s, f32) for s in shapes]
+
+
+def ints(shape, seed):
+    return synth.integer_bf16(shape, seed, 4)
+
+
+def check_exact(g, ref, f32):
+    g.check_bands()
+    if f32:
+        got = host_f64(g.t)
+        assert np.array_equal(got, ref), f"max|d| = {np.max(np.abs(got - ref))}"
+    else:
+        assert np.array_equal(host_bits(g.t), oracle.round_bf16(ref))
+
+
+def ws_for(tp, op, p, M, N, K, chunk):
+    return tp.workspace(op, p, M, N, K, chunk)
+
+
+ROW_CASES = [  # p, M, N, K, chunk_m
+    (1, 128, 256, 64, 0),
+    (2, 300, 520, 200, 0),
+    (3, 300, 520, 200, 128),
+    (4, 257, 264, 136, 256),
+    (2, 300, 520, 200, 32),
+    (2, 100, 264, 200, 16),
+    (3, 77, 136, 72, 64),
+    (8, 130, 72, 64, 0),
+    (2, 128, 2048, 1024, 32),   # the worked example's shape, 4 chunks of 32 rows
+]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", ROW_CASES)
+def test_row_allreduce_exact(tp, p, M, N, K, chunk, f32):
+    xs = [ints((M, K), 100 + r) for r in range(p)]
+    ws = [ints((K, N), 200 + r) for r in range(p)]
+    ref = oracle.row_fwd_allreduce(xs, ws)
+    y = outs([(M, N)], f32)
+    ws_ = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, chunk)
+    tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(b) for b in ws], [y[0].t], ws_, chunk)
+    check_exact(y[0], ref, f32)
+    assert tp.tp_get_device_status(ws_) == tp.TP_OK
+
+
+@pytest.mark.parametrize("p,M,N,K,chunk", [(2, 300, 520, 200, 0), (4, 130, 136, 72, 32)])
+def test_row_allreduce_replicas_identical(tp, p, M, N, K, chunk):
+    xs = [ints((M, K), 110 + r) for r in range(p)]
+    ws = [ints((K, N), 210 + r) for r in range(p)]
+    y = outs([(M, N)] * p, False)
+    ws_ = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, chunk)
+    tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(b) for b in ws], [g.t for g in y], ws_, chunk)
+    ref = oracle.row_fwd_allreduce(xs, ws)
+    first = host_bits(y[0].t)
+    for g in y:
+        check_exact(g, ref, False)
+        assert np.array_equal(host_bits(g.t), first)
+
+
+RS_CASES = [(2, 128, 2048, 1024, 32), (2, 300, 520, 200, 0), (4, 520, 264, 136, 128),
+            (3, 450, 136, 72, 16), (8, 512, 72, 64, 64), (4, 4 * 150, 264, 200, 256)]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", RS_CASES)
+def test_row_reducescatter_exact(tp, p, M, N, K, chunk, f32):
+    xs = [ints((M, K), 120 + r) for r in range(p)]
+    ws = [ints((K, N), 220 + r) for r in range(p)]
+    refs = oracle.row_fwd_reducescatter(xs, ws)
+    y = outs([(M // p, N)] * p, f32)
+    ws_ = ws_for(tp, tp.TP_OP_ROW_RS, p, M, N, K, chunk)
+    tp.tp_row_linear_fwd_reducescatter([dev(a) for a in xs], [dev(b) for b in ws], [g.t for g in y], ws_, chunk)
+    for g, r in zip(y, refs):
+        check_exact(g, r, f32)
+    # the slices concatenate to the AllReduce output, bit for bit
+    y_ar = outs([(M, N)], f32)
+    tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(b) for b in ws], [y_ar[0].t],
+                                   ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, chunk), chunk)
+    import torch
+    assert torch.equal(torch.cat([g.t for g in y], 0), y_ar[0].t)
+
+
+COL_CASES = [(1, 128, 256, 64, 0), (3, 300, 264, 136, 0), (4, 257, 520, 200, 128), (2, 100, 136, 200, 16),
+             (3, 64, 72, 72, 32), (8, 130, 264, 64, 64), (2, 513, 256, 128, 256)]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", COL_CASES)
+def test_col_fwd_exact(tp, p, M, N, K, chunk, f32):
+    x = ints((M, K), 130)
+    ws = [ints((K, N), 230 + k) for k in range(p)]
+    refs, _ = oracle.col_fwd(x, ws)
+    y = outs([(M, N)] * p, f32)
+    ws_ = ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, chunk)
+    tp.tp_col_linear_fwd(dev(x), [dev(b) for b in ws], [g.t for g in y], ws_, chunk_m=chunk)
+    for g, r in zip(y, refs):
+        check_exact(g, r, f32)
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", [(3, 300, 264, 136, 0), (2, 100, 136, 200, 16), (4, 260, 520, 72, 64)])
+def test_col_fwd_gelu(tp, p, M, N, K, chunk, f32):
+    # H ~ N(0, 1): the GeLU curve itself is exercised
+    x = synth.normal_bf16((M, K), 131, sigma=1.0 / np.sqrt(K))
+    ws = [synth.normal_bf16((K, N), 231 + k) for k in range(p)]
+    refs, hs = oracle.col_fwd(x, ws, apply_gelu=True)
+    y = outs([(M, N)] * p, f32)
+    h = outs([(M, N)] * p, f32)
+    ws_ = ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, chunk)
+    tp.tp_col_linear_fwd(dev(x), [dev(b) for b in ws], [g.t for g in y], ws_, epi=tp.TP_EPI_GELU,
+                         preact=[g.t for g in h], chunk_m=chunk)
+    for k in range(p):
+        y[k].check_bands()
+        h[k].check_bands()
+        assert_close(host_f64(y[k].t), refs[k], f32, f"gelu y[{k}]")
+        assert_close(host_f64(h[k].t), hs[k], f32, f"preact h[{k}]")
+    # GeLU applied to the kernel's own H: the epilogue, not the GEMM, is what is checked
+    if f32:
+        for k in range(p):
+            assert_close(host_f64(y[k].t), oracle.gelu(host_f64(h[k].t)), True, "gelu(H)")
+
+
+COLB_CASES = [(1, 128, 256, 64, 0), (3, 300, 136, 264, 0), (4, 257, 72, 520, 128), (2, 100, 200, 136, 16),
+              (3, 77, 72, 72, 64), (2, 64, 64, 256, 32)]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", COLB_CASES)
+def test_col_bwd_exact(tp, p, M, N, K, chunk, f32):
+    x = ints((M, K), 140)
+    ws = [ints((K, N), 240 + k) for k in range(p)]
+    dys = [ints((M, N), 340 + k) for k in range(p)]
+    ref_dx = oracle.col_bwd_dx(ws, dys)
+    ref_dw = oracle.col_bwd_dw(x, dys)
+    dx = outs([(M, K)], f32)
+    dw = outs([(K, N)] * p, f32)
+    ws_ = ws_for(tp, tp.TP_OP_COL_BWD, p, M, N, K, chunk)
+    tp.tp_col_linear_bwd(dev(x), [dev(b) for b in ws], [dev(d) for d in dys], dx[0].t, [g.t for g in dw],
+                         ws_, chunk)
+    check_exact(dx[0], ref_dx, f32)
+    for g, r in zip(dw, ref_dw):
+        check_exact(g, r, f32)
+
+
+ROWB_CASES = [(1, 128, 256, 64, 0), (3, 300, 136, 264, 0), (4, 257, 520, 72, 128), (2, 100, 136, 200, 16),
+              (2, 64, 72, 256, 32), (8, 130, 64, 72, 64)]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", ROWB_CASES)
+def test_row_bwd_exact(tp, p, M, N, K, chunk, f32):
+    xs = [ints((M, K), 150 + k) for k in range(p)]
+    ws = [ints((K, N), 250 + k) for k in range(p)]
+    dy = ints((M, N), 350)
+    ref_dx = oracle.row_bwd_dx(ws, dy)
+    ref_dw = oracle.row_bwd_dw(xs, dy)
+    dx = outs([(M, K)] * p, f32)
+    dw = outs([(K, N)] * p, f32)
+    ws_ = ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, chunk)
+    tp.tp_row_linear_bwd([dev(a) for a in xs], [dev(b) for b in ws], dev(dy), [g.t for g in dx],
+                         [g.t for g in dw], ws_, chunk_m=chunk)
+    for g, r in zip(dx, ref_dx):
+        check_exact(g, r, f32)
+    for g, r in zip(dw, ref_dw):
+        check_exact(g, r, f32)
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", [(3, 300, 136, 264, 0), (2, 100, 136, 200, 16), (4, 130, 64, 72, 64)])
+def test_row_bwd_dgelu(tp, p, M, N, K, chunk, f32):
+    ws = [synth.normal_bf16((K, N), 251 + k, sigma=1.0 / np.sqrt(N)) for k in range(p)]
+    dy = synth.normal_bf16((M, N), 351)
+    hs = [synth.normal_bf16((M, K), 451 + k) for k in range(p)]
+    refs = oracle.row_bwd_dx(ws, dy, preacts=hs)
+    dx = outs([(M, K)] * p, f32)
+    ws_ = ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, chunk)
+    tp.tp_row_linear_bwd(None, [dev(b) for b in ws], dev(dy), [g.t for g in dx], None, ws_,
+                         preact=[dev(h) for h in hs], chunk_m=chunk)
+    for g, r in zip(dx, refs):
+        g.check_bands()
+        assert_close(host_f64(g.t), r, f32, "dgelu dx")
+
+
+AG_CASES = [(2, 256, 264, 136, 0), (4, 512, 136, 200, 128), (4, 400, 72, 72, 0), (3, 300, 264, 64, 16),
+            (8, 512, 64, 128, 64), (2, 128, 256, 64, 32)]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", AG_CASES)
+def test_ag_matmul_exact(tp, p, M, N, K, chunk, f32):
+    Mp = M // p
+    xs = [ints((Mp, K), 160 + s) for s in range(p)]
+    ws = [ints((K, N), 260 + k) for k in range(p)]
+    refs, _, xg_ref = oracle.ag_matmul(xs, ws)
+    y = outs([(M, N)] * p, f32)
+    xg = outs([(M, K)], False)
+    ws_ = ws_for(tp, tp.TP_OP_AG_MM, p, M, N, K, chunk)
+    tp.tp_ag_matmul([dev(a) for a in xs], [dev(b) for b in ws], [g.t for g in y], ws_, x_gathered=xg[0].t,
+                    chunk_m=chunk)
+    for g, r in zip(y, refs):
+        check_exact(g, r, f32)
+    check_exact(xg[0], xg_ref, False)
+
+
+@pytest.mark.parametrize("p,M,N,K,chunk", [(4, 512, 264, 136, 0), (2, 100, 136, 64, 16)])
+def test_ag_matmul_gelu(tp, p, M, N, K, chunk):
+    Mp = M // p
+    xs = [synth.normal_bf16((Mp, K), 161 + s, sigma=1.0 / np.sqrt(K)) for s in range(p)]
+    ws = [synth.normal_bf16((K, N), 261 + k) for k in range(p)]
+    refs, hs, _ = oracle.ag_matmul(xs, ws, apply_gelu=True)
+    y = outs([(M, N)] * p, False)
+    h = outs([(M, N)] * p, False)
+    ws_ = ws_for(tp, tp.TP_OP_AG_MM, p, M, N, K, chunk)
+    tp.tp_ag_matmul([dev(a) for a in xs], [dev(b) for b in ws], [g.t for g in y], ws_, epi=tp.TP_EPI_GELU,
+                    preact=[g.t for g in h], chunk_m=chunk)
+    for k in range(p):
+        assert_close(host_f64(y[k].t), refs[k], False, "ag gelu")
+        assert_close(host_f64(h[k].t), hs[k], False, "ag preact")
+
+
+# ------------------------------------------------------------------ coordinate encoding
+
+def test_onehot_routing_row_ar(tp):
+    """X_r one-hot: Y[i] = sum_r W_r[c_r(i)] -- a transposed or misrouted tile
+    would pick wrong rows."""
+    p, M, N, K = 3, 260, 264, 200
+    xs = [synth.onehot_bf16(M, K, 170 + r) for r in range(p)]
+    ws = [synth.ramp_bf16(K, N, scale=float(r + 1)) for r in range(p)]
+    ref = oracle.row_fwd_allreduce(xs, ws)
+    for chunk in (0, 32):
+        y = outs([(M, N)], True)
+        tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(b) for b in ws], [y[0].t],
+                                       ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, chunk), chunk)
+        check_exact(y[0], ref, True)
+
+
+# ------------------------------------------------------------------ determinism and chunking
+
+def test_deterministic_and_chunk_invariant(tp):
+    import torch
+    p, M, N, K = 4, 520, 520, 264
+    xs = [dev(synth.normal_bf16((M, K), 180 + r)) for r in range(p)]
+    ws = [dev(synth.normal_bf16((K, N), 280 + r, 0.02)) for r in range(p)]
+    res = {}
+    for chunk in (0, 128, 256, 512, 32, 16):
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        tp.tp_row_linear_fwd_allreduce(xs, ws, [y], tp.workspace(tp.TP_OP_ROW_AR, p, M, N, K, chunk), chunk)
+        y2 = torch.empty_like(y)
+        tp.tp_row_linear_fwd_allreduce(xs, ws, [y2], tp.workspace(tp.TP_OP_ROW_AR, p, M, N, K, chunk), chunk)
+        assert torch.equal(y, y2), f"run-to-run difference at chunk_m={chunk}"
+        res[chunk] = y
+    # chunks of >= 128 rows only reorder tiles: identical bits
+    for c in (256, 512):
+        assert torch.equal(res[c], res[128])
+    ref = oracle.row_fwd_allreduce([host_bits(a) for a in xs], [host_bits(b) for b in ws])
+    for c, y in res.items():
+        assert_close(host_f64(y), ref, False, f"chunk {c}")
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_edge_sizes(tp):
+    import torch
+    p, N, K = 2, 72, 64
+    # M == 0: accepted, nothing written
+    w = [dev(ints((K, N), 5 + r)) for r in range(p)]
+    x0 = [torch.empty((0, K), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    y0 = torch.empty((0, N), dtype=torch.bfloat16, device="cuda")
+    tp.tp_row_linear_fwd_allreduce(x0, w, [y0], tp.workspace(0, p, 0, N, K, 0))
+    # K == 0: zeros
+    xk = [torch.empty((5, 0), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    wk = [torch.empty((0, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    yk = torch.full((5, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    st = tp._lib.tp_row_linear_fwd_allreduce(tp._arr(xk), tp._arr(wk), tp._arr([yk]), 1, p, 5, N, 0, 0, 0,
+                                             tp._ptr(tp.workspace(0, p, 5, N, 0)), 256,
+                                             torch.cuda.current_stream().cuda_stream)
+    assert st == tp.TP_OK
+    assert bool((yk == 0).all())
+    # M == 1, N == 8, K == 8, p == 8, chunk_m far above M
+    p, M, N, K = 8, 1, 8, 8
+    xs = [ints((M, K), 60 + r) for r in range(p)]
+    ws = [ints((K, N), 70 + r) for r in range(p)]
+    y = outs([(M, N)], True)
+    tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(b) for b in ws], [y[0].t],
+                                   tp.workspace(0, p, M, N, K, 4096), 4096)
+    check_exact(y[0], oracle.row_fwd_allreduce(xs, ws), True)
+
+
+def test_misaligned_pointer_rejected_on_device(tp):
+    import torch
+    p, M, N, K = 2, 16, 8, 8
+    buf = torch.zeros(M * K + 8, dtype=torch.bfloat16, device="cuda")
+    bad = buf[1:1 + M * K].view(M, K)    # 2-byte offset: not 16-byte aligned
+    w = [torch.zeros((K, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_row_linear_fwd_allreduce([bad, bad], w, [y], tp.workspace(0, p, M, N, K, 0))
+    assert e.value.status == tp.TP_ERR_ALIGNMENT
