@@ -46,7 +46,8 @@ WORKLOAD = (f"Megatron MLP block fwd+bwd, p={P}: tokens {M}, h={H}, ffn={FFN}; F
             f"[{H},{NK}]/shard + GeLU, FC2 row-parallel [{NK},{H}]/shard with fused AllReduce; "
             f"backward: FC2 dZ (GeLU') + dW2, FC1 fused dX reduce + dW1")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["gemm_reduce_fusion_gb300/csrc/gemm_kernel.cuh", "gemm_reduce_fusion_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = ["gemm_reduce_fusion_gb300/csrc/gemm_kernel.cuh", "gemm_reduce_fusion_gb300/csrc/ptx.cuh",
+                  "gemm_reduce_fusion_gb300/csrc/tp_fused.cu"]
 
 
 def parse():
@@ -58,6 +59,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run each GEMM variant of the step twice at the step's shapes (for ncu)")
     return ap.parse_args()
 
 
@@ -425,8 +428,38 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_case():
+    """Two launches of each kernel variant of the step, at the step's shapes,
+    with about 0.5 GB resident: a bounded case for ncu captures."""
+    import torch
+    import gemm_reduce_fusion_gb300 as tp
+    import synth
+    import numpy as np
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    x = [dev(synth.normal_bf16((M, NK), synth.seed_for(2, r))) for r in range(P)]
+    w = [dev(synth.normal_bf16((NK, H), synth.seed_for(2, 4 + r), 0.02)) for r in range(P)]
+    y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    g = [torch.empty((M, NK), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        tp.tp_row_linear_fwd_allreduce(x, w, [y], ws)                 # K-major A, MN-major B
+        tp.tp_row_linear_bwd(None, w, y, g, None, ws)                  # K-major A, K-major B
+    wgrad = [torch.empty((NK, H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    for _ in range(2):
+        tp.tp_row_linear_bwd(x, w, y, None, wgrad, ws)                 # MN-major A, MN-major B
+    torch.cuda.synchronize()
+    assert tp.tp_get_device_status(ws) == tp.TP_OK
+    print("profile case done")
+
+
 def main():
     args = parse()
+    if args.profile_case:
+        profile_case()
+        return
     if args.impl == "reference":
         run_reference(args)
         return
