@@ -236,3 +236,19 @@ def tp_ag_matmul(x: Sequence, w: Sequence, y: Sequence, ws, x_gathered=None,
     _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
                              Mp * p, N, K, chunk_m, _dtype_code(y[0]), wp, wb, _stream(stream)),
            "tp_ag_matmul")
+
+
+def tp_row_linear_fwd_allreduce_noalloc(x: Sequence, w: Sequence, y: Sequence, chunk_m: int = 0,
+                                        stream=None) -> None:
+    """tp_row_linear_fwd_allreduce without a workspace: for callers that
+    cannot allocate device memory (the library uses its static scratch)."""
+    fn = _lib.tp_row_linear_fwd_allreduce_noalloc
+    fn.restype = ctypes.c_int
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    L = ctypes.c_int64
+    fn.argtypes = [PP, PP, PP, ctypes.c_int, ctypes.c_int, L, L, L, L, ctypes.c_int, ctypes.c_void_p]
+    p = len(x)
+    M, K = x[0].shape
+    N = w[0].shape[1]
+    _check(fn(_arr(x), _arr(w), _arr(y), len(y), p, M, N, K, chunk_m, _dtype_code(y[0]), _stream(stream)),
+           "tp_row_linear_fwd_allreduce_noalloc")

@@ -847,3 +847,51 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
 }
 
 }  // extern "C"
+
+// ====================================================================== no-allocation entry point
+//
+// Scratch of tp_row_linear_fwd_allreduce_noalloc: a static device array, so
+// that callers which cannot allocate device memory still get the split-K
+// path.  Host code must not pass `g_noalloc_scratch` itself to a kernel --
+// on the host that name is only a stand-in for the device symbol -- but the
+// device address looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+tp_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return TP_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return TP_OK;
+}
+
+}  // namespace
+
+extern "C" tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* const* w,
+                                                         void* const* y, int n_out, int p,
+                                                         int64_t M, int64_t N, int64_t K,
+                                                         int64_t chunk_m, tp_dtype out_dtype,
+                                                         cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
+  if (workspace_for(op_shapes(TP_OP_ROW_AR, p, M, N, K, chunk_m)) > TP_NOALLOC_SCRATCH_BYTES)
+    return TP_ERR_WORKSPACE_TOO_SMALL;
+  if (M == 0 || N == 0) return TP_OK;
+  void* scratch = nullptr;
+  TP_TRY(noalloc_scratch(&scratch));
+  return row_fwd_impl(false, x, w, y, n_out, p, M, N, K, chunk_m, out_dtype, scratch,
+                      TP_NOALLOC_SCRATCH_BYTES, stream);
+}

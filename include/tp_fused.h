@@ -175,6 +175,38 @@ int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K);
  * (TP_OK or TP_ERR_DEVICE_TIMEOUT) and clears it.                         */
 tp_status tp_get_device_status(void* ws, cudaStream_t stream);
 
+/* Row-parallel MatMul+AllReduce for callers that cannot allocate device
+ * memory.  The paper has no counterpart: this is a library convenience.
+ *
+ * Some callers have no way to hand the library a workspace: a host plugin
+ * interface that passes only input and output buffers, or an engine that
+ * has reserved all of device memory up front for its own pool, so a
+ * cudaMalloc from inside a call would fail or stall every stream (it
+ * synchronises the device).  This entry point computes exactly what
+ * tp_row_linear_fwd_allreduce computes, with the same arguments minus the
+ * workspace, and allocates nothing.  Its scratch (the status word and the
+ * split-K fp32 partials) lives in one static device array of
+ * TP_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library holds
+ * until the process exits.
+ *
+ *  - A call whose scratch need (tp_workspace_size(TP_OP_ROW_AR, ...))
+ *    exceeds TP_NOALLOC_SCRATCH_BYTES is rejected with
+ *    TP_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array.  Calls that may overlap on
+ *    the GPU (different streams without ordering between them) race on it;
+ *    order them on one stream.  Nothing in the array has to start at zero:
+ *    every partial a call reads was written earlier by that same call.
+ *  - Device-side timeouts are latched in the array but not reported; use
+ *    tp_row_linear_fwd_allreduce with a workspace to read them.            */
+#define TP_NOALLOC_SCRATCH_BYTES (16u << 20)
+tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* const* w,
+                                              void* const* y, int n_out, int p,
+                                              int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                              tp_dtype out_dtype, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* tp_status_string(tp_status s);
 
