@@ -42,6 +42,7 @@ TP_OP_COL_FWD = 2
 TP_OP_COL_BWD = 3
 TP_OP_ROW_BWD = 4
 TP_OP_AG_MM = 5
+TP_OP_ROW_AR_UNFUSED = 6
 
 
 class TPError(RuntimeError):
@@ -69,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "tp_col_linear_bwd": (I, [P, PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
         "tp_row_linear_bwd": (I, [PP, PP, P, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_ag_matmul": (I, [PP, PP, PP, P, I, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_fwd_unfused": (I, [PP, PP, P, I, L, L, L, L, I, I, P, S, P]),
         "tp_pipeline_time": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, L]),
         "tp_num_chunks": (L, [L, L]),
         "tp_choose_chunk_m": (L, [I, I, L, L, L]),
@@ -236,6 +238,17 @@ def tp_ag_matmul(x: Sequence, w: Sequence, y: Sequence, ws, x_gathered=None,
     _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
                              Mp * p, N, K, chunk_m, _dtype_code(y[0]), wp, wb, _stream(stream)),
            "tp_ag_matmul")
+
+
+def tp_row_linear_fwd_unfused(x: Sequence, w: Sequence, y, ws, chunk_m: int = 0, phases: int = 3,
+                              stream=None) -> None:
+    """Unfused baseline: per-rank fp32 partials (phase 1), rank-order reduce into y (phase 2)."""
+    p = len(x)
+    M, K = x[0].shape
+    N = w[0].shape[1]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_row_linear_fwd_unfused(_arr(x), _arr(w), _ptr(y), p, M, N, K, chunk_m, _dtype_code(y),
+                                          phases, wp, wb, _stream(stream)), "tp_row_linear_fwd_unfused")
 
 
 def tp_row_linear_fwd_allreduce_noalloc(x: Sequence, w: Sequence, y: Sequence, chunk_m: int = 0,

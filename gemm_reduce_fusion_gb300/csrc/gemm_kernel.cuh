@@ -8,16 +8,17 @@
 // accumulator, so the cross-rank reduction happens in TMEM and the reduced
 // tile is written once.
 //
-// Roles (192 threads):
+// Roles (320 threads):
 //   warp 0     one thread issues TMA loads of A and B k-blocks into a
 //              STAGES-deep shared-memory ring (full/empty mbarriers);
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma into
 //              one of two TMEM accumulators and commits to the ring's
 //              empty barriers and to the accumulator-full barrier;
-//   warps 2-5  epilogue: tcgen05.ld the finished accumulator (warp w reads
-//              TMEM lanes 32*(w%4)..+31), apply GeLU / GeLU' / cast, store,
-//              then release the accumulator -- overlapping the next tile's
-//              MMAs on the other accumulator.
+//   warps 2-9  epilogue: tcgen05.ld the finished accumulator (warp w reads
+//              TMEM lanes 32*(w%4)..+31; warps 2-5 take the left half of the
+//              columns, warps 6-9 the right half), apply GeLU / GeLU' / cast,
+//              store, then release the accumulator -- overlapping the next
+//              tile's MMAs on the other accumulator.
 //
 // Tiles are visited chunk-major: all tiles of rows chunk c (over every
 // N-tile) precede those of chunk c+1, m fastest within a chunk, so a chunk's
@@ -39,7 +40,8 @@ constexpr int BK = 64;            // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int MAX_MAPS = 8;
 constexpr int MAX_GROUPS = 64;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 
 enum Epi : int32_t { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
 
@@ -55,6 +57,7 @@ struct GemmParams {
   int32_t m_tiles, n_tiles;  // per group
   int32_t chunk_tiles;       // tiles per chunk along the chunked axis
   int32_t chunk_on_n;        // chunks run along GEMM N (operand-swapped kernels)
+  int32_t band;              // other-axis tiles per raster band inside a chunk
   int32_t num_units;         // Gm*Gn*m_tiles*n_tiles*n_split
   int32_t S;                 // K segments (ranks reduced)
   int32_t kb_per_seg;        // k-blocks per segment
@@ -84,7 +87,10 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& P, int32_t t) {
   const int32_t v = t / P.n_split;
   const int32_t TM = P.Gm * P.m_tiles;
   const int32_t TN = P.Gn * P.n_tiles;
-  // chunked axis C (token rows), other axis O; C runs fastest inside a chunk
+  // Chunked axis C (token rows), other axis O.  Inside a chunk the tiles
+  // are rastered in bands of `band` O-tiles: band by band, C then O within
+  // the band, so the ~#SM tiles in flight form a (#SM/band) x band block
+  // that shares both its A rows and its B columns through L2.
   const int32_t TC = P.chunk_on_n ? TN : TM;
   const int32_t TO = P.chunk_on_n ? TM : TN;
   const int32_t per_chunk = P.chunk_tiles * TO;
@@ -92,8 +98,11 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& P, int32_t t) {
   const int32_t r = v % per_chunk;
   const int32_t lo = c * P.chunk_tiles;
   const int32_t cnt = min(P.chunk_tiles, TC - lo);
-  const int32_t O = r / cnt;
-  const int32_t C = lo + r % cnt;
+  const int32_t nb = r / (cnt * P.band);
+  const int32_t rem = r % (cnt * P.band);
+  const int32_t width = min(P.band, TO - nb * P.band);
+  const int32_t O = nb * P.band + rem % width;
+  const int32_t C = lo + rem / width;
   const int32_t GM = P.chunk_on_n ? O : C;
   const int32_t GN = P.chunk_on_n ? C : O;
   u.gm = GM / P.m_tiles;
@@ -220,7 +229,8 @@ struct GemmCfg {
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
   // +1024 so the ring can be aligned to 1024 bytes inside dynamic smem
   static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
-  static constexpr int CW = BN < 32 ? BN : 32;  // epilogue columns per TMEM load
+  static constexpr int HALF = BN / 2;                 // columns per epilogue warp
+  static constexpr int CW = HALF < 32 ? HALF : 32;  // epilogue columns per TMEM load
 };
 
 template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), NUM_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -367,6 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) / 4;
     const int row_in_tile = 32 * q + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -384,12 +395,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += Cfg::CW) {
+      for (int c0 = half * Cfg::HALF; c0 < (half + 1) * Cfg::HALF; c0 += Cfg::CW) {
         uint32_t r[32];
         if constexpr (Cfg::CW == 32) {
           tmem_ld_32x32b_x32(t_row + c0, r);
-        } else {
+        } else if constexpr (Cfg::CW == 16) {
           tmem_ld_32x32b_x16(t_row + c0, r);
+        } else {
+          tmem_ld_32x32b_x8(t_row + c0, r);
         }
         tmem_wait_ld();
         if (!row_ok) continue;

@@ -219,6 +219,15 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
   switch (op) {
     case TP_OP_ROW_AR:
       s.S = p; s.kseg = K; tok(M, N, 1, 1); break;
+    case TP_OP_ROW_AR_UNFUSED:
+      s.S = p; s.kseg = K; tok(M, N, 1, 1);
+      finish_shape(&s);
+      if (s.units0 > 0 && s.kb_total > 0) {  // one split per rank: fp32 partial per rank
+        s.n_split = p;
+        s.kb_per_split = cdiv(K, BK);
+      }
+      v.push_back(s);
+      return v;
     case TP_OP_ROW_RS:
       s.S = p; s.kseg = K; tok(Mp, N, p, 1); break;
     case TP_OP_COL_FWD:
@@ -276,6 +285,11 @@ void fill_common(GemmParams* P, const Shape& s) {
   P->n_tiles = static_cast<int32_t>(s.n_tiles);
   P->chunk_tiles = static_cast<int32_t>(s.swap ? 1 : std::min<int64_t>(s.chunk_tiles, s.Gm * s.m_tiles));
   P->chunk_on_n = s.swap ? 1 : 0;
+  // raster band: 8 N-tiles for 128x256 tiles (about 19 m-tiles x 8 n-tiles
+  // in flight on 152 SMs, which minimises A+B bytes per wave); the swapped
+  // kernels stream distinct weight tiles anyway.
+  const int64_t TO = s.swap ? s.Gm * s.m_tiles : s.Gn * s.n_tiles;
+  P->band = static_cast<int32_t>(std::max<int64_t>(1, s.swap ? TO : std::min<int64_t>(8, TO)));
   P->S = s.S;
   P->kb_per_seg = static_cast<int32_t>(cdiv(s.kseg, BK));
   P->n_split = s.n_split;
@@ -289,14 +303,25 @@ void fill_common(GemmParams* P, const Shape& s) {
 
 size_t esize(tp_dtype d) { return d == TP_FP32 ? 4 : 2; }
 
+tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
+                            const DevInfo& di, int phases);
+
 tp_status run_launch(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
                      const DevInfo& di) {
+  return run_launch_phases(L, out_dtype, ws, stream, di, 3);
+}
+
+// phases: bit 0 = the GEMM launch (or the K == 0 fill), bit 1 = the split-K
+// second stage.
+tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
+                            const DevInfo& di, int phases) {
   const Shape& s = L.shape;
   if (s.empty()) return TP_OK;
   GemmParams& P = L.P;
   P.status = static_cast<uint32_t*>(ws);
   P.out_f32 = out_dtype == TP_FP32 ? 1 : 0;
   if (s.kb_total == 0) {
+    if (!(phases & 1)) return TP_OK;
     // K == 0: the product is zero; GeLU(0) = 0 and G * GeLU'(.) = 0 too.
     const int G = s.Gm * s.Gn;
     const int64_t A = s.swap ? s.cols_g : s.rows_g;
@@ -317,8 +342,8 @@ tp_status run_launch(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t strea
   }
   if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
   const int grid = static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
-  if (launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
-  if (s.n_split > 1) {
+  if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
+  if (s.n_split > 1 && (phases & 2)) {
     ReduceParams R;
     std::memset(&R, 0, sizeof(R));
     for (int g = 0; g < MAX_GROUPS; ++g) {
@@ -463,20 +488,31 @@ int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K) {
     case TP_OP_ROW_BWD:
       flops = 2.0 * M * N * K * p; wbytes = 2.0 * K * N * p; in_row = 2.0 * N; out_row = 2.0 * K * p; break;
   }
+  // Candidates from one chunk (M rows) down to 16 rows.  A chunk's compute
+  // time c is its MMA time at the tile's MMA-width efficiency or its
+  // compulsory streaming time, whichever is larger, plus the time to stream
+  // the weights again when they do not stay in L2 across chunks (the
+  // pipeline stalls on those re-reads).  Its reduce time m is the write-out
+  // of its rows.  A smaller chunk must beat the best so far by more than 2 %
+  // to be chosen: fewer chunks keep more operand reuse in flight.
   std::vector<int64_t> cand;
-  for (int64_t c = 16; c < M; c *= 2) cand.push_back(c);
   cand.push_back(M);
+  int64_t top = 16;
+  while (top * 2 < M) top *= 2;
+  for (int64_t c = top; c >= 16; c /= 2)
+    if (c < M) cand.push_back(c);
   int64_t best = M;
   double best_t = 1e300;
   for (int64_t c : cand) {
     const int64_t rows = std::min(c, M);
     const int64_t n = cdiv(M, rows);
     const double eff = rows >= BM ? 1.0 : static_cast<double>(cdiv(rows, 16) * 16) / BM;
-    const double wb = wbytes > l2 ? wbytes : wbytes / n;
-    const double cc = std::max(flops * rows / M / (peak * eff), (wb + rows * in_row) / bw);
+    const double first = wbytes / n + rows * (in_row + out_row);
+    const double again = (wbytes > l2 && n > 1) ? wbytes * (n - 1) / n : 0.0;
+    const double cc = std::max(flops * rows / M / (peak * eff), first / bw) + again / bw;
     const double mm = rows * out_row / bw;
     const double t = tp_pipeline_time(cc, mm, n);
-    if (t < best_t * (1.0 - 1e-9)) {
+    if (t < best_t * 0.98) {
       best_t = t;
       best = c;
     }
@@ -847,6 +883,56 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
 }
 
 }  // extern "C"
+
+// ====================================================================== unfused baseline
+
+extern "C" tp_status tp_row_linear_fwd_unfused(const void* const* x, const void* const* w, void* y,
+                                               int p, int64_t M, int64_t N, int64_t K,
+                                               int64_t chunk_m, tp_dtype out_dtype, int phases,
+                                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
+  if (phases < 1 || phases > 3) return TP_ERR_INVALID_ARG;
+  const bool work = M > 0 && N > 0;
+  TP_TRY(check_ptrs(x, p, work && K > 0));
+  TP_TRY(check_ptrs(w, p, work && K > 0));
+  TP_TRY(check_ptr(y, work));
+  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  if (!work) return TP_OK;
+  {
+    std::vector<Range> ins, outs;
+    add_ranges(&ins, x, p, M * K * 2);
+    add_ranges(&ins, w, p, K * N * 2);
+    outs.push_back({y, static_cast<size_t>(M * N * esize(out_dtype))});
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  Launch L;
+  L.shape = shapes[0];
+  init_params(&L.P);
+  fill_common(&L.P, L.shape);
+  GemmParams& P = L.P;
+  const Shape& s = L.shape;
+  if (K > 0) {
+    for (int r = 0; r < p; ++r) {
+      if (!s.swap) {
+        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM) || !encode_map(&P.tmB[r], w[r], N, K, N, 64))
+          return TP_ERR_CUDA;
+      } else {
+        if (!encode_map(&P.tmA[r], w[r], N, K, N, 64) || !encode_map(&P.tmB[r], x[r], K, M, K, s.bn))
+          return TP_ERR_CUDA;
+      }
+    }
+  }
+  P.a_idx_s = 1;
+  P.b_idx_s = 1;
+  P.ld_out = N;
+  P.epi = EPI_NONE;
+  P.out[0] = y;
+  L.variant = s.swap ? sw_variant_mk(s.bn) : V_KN;
+  return run_launch_phases(L, out_dtype, ws, stream, di, phases);
+}
 
 // ====================================================================== no-allocation entry point
 //

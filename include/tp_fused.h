@@ -82,7 +82,8 @@ typedef enum {
   TP_OP_COL_FWD = 2, /* tp_col_linear_fwd */
   TP_OP_COL_BWD = 3, /* tp_col_linear_bwd */
   TP_OP_ROW_BWD = 4, /* tp_row_linear_bwd */
-  TP_OP_AG_MM = 5    /* tp_ag_matmul */
+  TP_OP_AG_MM = 5,   /* tp_ag_matmul */
+  TP_OP_ROW_AR_UNFUSED = 6  /* tp_row_linear_fwd_unfused */
 } tp_op;
 
 /* Bytes of device workspace the call (op, p, M, N, K, chunk_m) needs, with
@@ -156,6 +157,20 @@ tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* 
                        int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                        tp_dtype out_dtype, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
+
+/* Unfused baseline of the row-parallel MatMul+AllReduce, for measurement.
+ * [M027 §04: time the MatMul and the collective separately]
+ *   phase bit 0: every rank's partial P_r = X_r . W_r into its own fp32
+ *                buffer in the workspace (one launch over all ranks);
+ *   phase bit 1: Y = P_0 + P_1 + ... + P_{p-1} in rank order, cast, -> y.
+ *   phases = 3 runs both.  Arguments as in tp_row_linear_fwd_allreduce with
+ *   n_out = 1; the workspace holds p fp32 copies of Y
+ *   (tp_workspace_size(TP_OP_ROW_AR_UNFUSED, ...)).  Phase 1 without a
+ *   later phase 2 leaves y untouched.                                    */
+tp_status tp_row_linear_fwd_unfused(const void* const* x, const void* const* w, void* y, int p,
+                                    int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                    tp_dtype out_dtype, int phases, void* ws, size_t ws_bytes,
+                                    cudaStream_t stream);
 
 /* Two-engine chunk timeline: c + (n-1) * max(c, m) + m for n >= 1, 0 for
  * n <= 0; c = per-chunk compute time, m = per-chunk reduce time.  [M027 §03] */

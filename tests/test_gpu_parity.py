@@ -348,3 +348,24 @@ def test_misaligned_pointer_rejected_on_device(tp):
     with pytest.raises(tp.TPError) as e:
         tp.tp_row_linear_fwd_allreduce([bad, bad], w, [y], tp.workspace(0, p, M, N, K, 0))
     assert e.value.status == tp.TP_ERR_ALIGNMENT
+
+
+# ------------------------------------------------------------------ unfused baseline
+
+@pytest.mark.parametrize("p,M,N,K,chunk", [(2, 300, 520, 200, 0), (4, 130, 136, 72, 32), (3, 64, 264, 64, 16)])
+def test_unfused_baseline_exact(tp, p, M, N, K, chunk):
+    """Per-rank fp32 partials then the rank-order reduce: run whole, and as
+    its two phases separately; both equal the oracle exactly."""
+    xs = [ints((M, K), 190 + r) for r in range(p)]
+    ws = [ints((K, N), 290 + r) for r in range(p)]
+    ref = oracle.row_fwd_allreduce(xs, ws)
+    dx, dw = [dev(a) for a in xs], [dev(b) for b in ws]
+    for split in (False, True):
+        y = outs([(M, N)], True)
+        wsp = ws_for(tp, tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk)
+        if split:
+            tp.tp_row_linear_fwd_unfused(dx, dw, y[0].t, wsp, chunk, phases=1)
+            tp.tp_row_linear_fwd_unfused(dx, dw, y[0].t, wsp, chunk, phases=2)
+        else:
+            tp.tp_row_linear_fwd_unfused(dx, dw, y[0].t, wsp, chunk, phases=3)
+        check_exact(y[0], ref, True)
