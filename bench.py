@@ -53,7 +53,7 @@ KERNEL_SOURCES = ["gemm_reduce_fusion_gb300/csrc/gemm_kernel.cuh", "gemm_reduce_
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -114,6 +114,11 @@ def dist_init(n_gpus):
     return rank, world, local
 
 
+def aggregate_value(flops_per_step: float, steps: int, world: int, t_max_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
+    return flops_per_step * steps * world / (t_max_ms / 1e3) / 1e12
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -148,7 +153,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -370,7 +375,7 @@ def run_ours(args):
         raise RuntimeError(f"device status after timing: {tp.tp_status_string(st)}")
 
     t_max = max_over_ranks(total_ms, world)
-    value = STEP_FLOPS * K * world / (t_max / 1e3) / 1e12
+    value = aggregate_value(STEP_FLOPS, K, world, t_max)
 
     # dominant kernel variant: the one with the largest total time
     per_kernel = {}
@@ -410,7 +415,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e = {"value": STEP_FLOPS * E * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+    e2e = {"value": aggregate_value(STEP_FLOPS, E, world, e2e_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E}
 
     if rank != 0:

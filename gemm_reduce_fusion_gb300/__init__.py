@@ -43,6 +43,9 @@ TP_OP_COL_BWD = 3
 TP_OP_ROW_BWD = 4
 TP_OP_AG_MM = 5
 TP_OP_ROW_AR_UNFUSED = 6
+# tp_debug_key
+TP_DEBUG_TIMEOUT_MS = 0
+TP_DEBUG_DROP_LOAD = 1
 
 
 class TPError(RuntimeError):
@@ -76,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "tp_choose_chunk_m": (L, [I, I, L, L, L]),
         "tp_get_device_status": (I, [P, P]),
         "tp_status_string": (ctypes.c_char_p, [I]),
+        "tp_debug_set": (I, [I, L]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -159,6 +163,11 @@ def workspace(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0, device=
     import torch
     n = tp_workspace_size(op, p, M, N, K, chunk_m)
     return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def tp_debug_set(key: int, value: int) -> int:
+    """Test hook of the failure-detection path (see tp_fused.h)."""
+    return int(_lib.tp_debug_set(key, value))
 
 
 def tp_get_device_status(ws, stream=None) -> int:

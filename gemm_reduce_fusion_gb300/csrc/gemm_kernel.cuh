@@ -75,6 +75,8 @@ struct GemmParams {
   float* partial;            // split-K fp32 partials, dense, output orientation
   uint32_t* status;
   uint64_t timeout_ns;
+  int32_t debug_drop_q;      // test hook: CTA 0's producer never arms its k-block number
+                             // debug_drop_q (-1: off), so a wait runs out of time
 };
 
 struct Unit {
@@ -285,6 +287,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
+      int32_t n_issued = 0;
       bool ok = true;
       for (int32_t t = blockIdx.x; t < P.num_units && ok; t += gridDim.x) {
         const Unit u = decode_unit(P, t);
@@ -296,6 +299,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
             ok = false;
             break;
+          }
+          if (blockIdx.x == 0 && n_issued++ == P.debug_drop_q) {
+            // test hook: leave this stage unarmed; its consumer's wait runs out
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           const CUtensorMap* am = &P.tmA[P.a_idx_gm * u.gm + P.a_idx_gn * u.gn + P.a_idx_s * s];
           const CUtensorMap* bm = &P.tmB[P.b_idx_gm * u.gm + P.b_idx_gn * u.gn + P.b_idx_s * s];

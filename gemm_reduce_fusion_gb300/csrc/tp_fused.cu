@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -33,7 +34,14 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device wait limit: TP_DEVICE_TIMEOUT_MS from the environment (read once),
+// else 2 s; tp_debug_set(TP_DEBUG_TIMEOUT_MS, ...) overrides it.
+std::atomic<uint64_t> g_timeout_override_ns{0};
+std::atomic<int64_t> g_debug_drop_q{-1};
+
 uint64_t device_timeout_ns() {
+  const uint64_t o = g_timeout_override_ns.load();
+  if (o != 0) return o;
   static uint64_t v = []() -> uint64_t {
     const char* e = std::getenv("TP_DEVICE_TIMEOUT_MS");
     if (e != nullptr) {
@@ -299,6 +307,7 @@ void fill_common(GemmParams* P, const Shape& s) {
   P->cols_g = static_cast<int32_t>(s.cols_g);
   P->n_rep = 1;
   P->timeout_ns = device_timeout_ns();
+  P->debug_drop_q = static_cast<int32_t>(g_debug_drop_q.load());
 }
 
 size_t esize(tp_dtype d) { return d == TP_FP32 ? 4 : 2; }
@@ -457,6 +466,20 @@ const char* tp_status_string(tp_status s) {
     case TP_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out (latched in the workspace)";
   }
   return "unknown status";
+}
+
+tp_status tp_debug_set(tp_debug_key key, int64_t value) {
+  switch (key) {
+    case TP_DEBUG_TIMEOUT_MS:
+      if (value < 0) return TP_ERR_INVALID_ARG;
+      g_timeout_override_ns.store(static_cast<uint64_t>(value) * 1000000ull);
+      return TP_OK;
+    case TP_DEBUG_DROP_LOAD:
+      if (value < -1 || value > INT32_MAX) return TP_ERR_INVALID_ARG;
+      g_debug_drop_q.store(value);
+      return TP_OK;
+  }
+  return TP_ERR_INVALID_ARG;
 }
 
 double tp_pipeline_time(double c, double m, int64_t n_chunks) {

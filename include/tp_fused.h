@@ -222,6 +222,19 @@ tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* 
                                               int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                                               tp_dtype out_dtype, cudaStream_t stream);
 
+/* Test hooks of the failure-detection path (process-wide, read when a call
+ * is planned).  Not for production use.
+ *   TP_DEBUG_TIMEOUT_MS: limit of every device-side wait, in ms; 0 restores
+ *     the default (TP_DEVICE_TIMEOUT_MS from the environment, else 2000).
+ *   TP_DEBUG_DROP_LOAD: n >= 0 makes CTA 0 of every following launch skip
+ *     arming its n-th k-block load, so the MMA issuer's wait on it runs out:
+ *     the kernel latches TP_ERR_DEVICE_TIMEOUT, stops its other roles, waits
+ *     (bounded) for its own copies and MMAs in flight, frees its tensor
+ *     memory and returns; -1 turns the hook off.  No fault or trap is used.
+ * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
+typedef enum { TP_DEBUG_TIMEOUT_MS = 0, TP_DEBUG_DROP_LOAD = 1 } tp_debug_key;
+tp_status tp_debug_set(tp_debug_key key, int64_t value);
+
 /* Static description of a status code. */
 const char* tp_status_string(tp_status s);
 
