@@ -56,12 +56,14 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--sweep", action="store_true",
                     help="chunk_m sweep of the GPT-3-scale FC pair: fused time vs the timeline model")
     ap.add_argument("--configs", action="store_true",
                     help="one JSON line per workload (all five), TFLOP/s and roofline fraction")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="0: planner chooses 128x256 or CTA-pair 256x256 tiles; 1: 128x256 only; 2: pairs")
     ap.add_argument("--profile-case", action="store_true",
                     help="run each GEMM variant of the step twice at the step's shapes (for ncu)")
     return ap.parse_args()
@@ -240,12 +242,12 @@ class MLPStep:
 
 # which kernel variant each call launches (one launch per call at these sizes)
 CALL_KERNEL = {
-    "col_fwd_gelu": "tp_gemm_kernel<K-major A, MN-major B, 128x256> (X.W)",
-    "row_fwd_allreduce": "tp_gemm_kernel<K-major A, MN-major B, 128x256> (X.W)",
-    "row_bwd_dx_dgelu": "tp_gemm_kernel<K-major A, K-major B, 128x256> (dY.W^T)",
-    "col_bwd_dx": "tp_gemm_kernel<K-major A, K-major B, 128x256> (dY.W^T)",
-    "row_bwd_dw": "tp_gemm_kernel<MN-major A, MN-major B, 128x256> (X^T.dY)",
-    "col_bwd_dw": "tp_gemm_kernel<MN-major A, MN-major B, 128x256> (X^T.dY)",
+    "col_fwd_gelu": "tp_gemm_pair_kernel<K-major A, MN-major B> (X.W, 256x256 on a CTA pair)",
+    "row_fwd_allreduce": "tp_gemm_pair_kernel<K-major A, MN-major B> (X.W, 256x256 on a CTA pair)",
+    "row_bwd_dx_dgelu": "tp_gemm_pair_kernel<K-major A, K-major B> (dY.W^T, 256x256 on a CTA pair)",
+    "col_bwd_dx": "tp_gemm_pair_kernel<K-major A, K-major B> (dY.W^T, 256x256 on a CTA pair)",
+    "row_bwd_dw": "tp_gemm_pair_kernel<MN-major A, MN-major B> (X^T.dY, 256x256 on a CTA pair)",
+    "col_bwd_dw": "tp_gemm_pair_kernel<MN-major A, MN-major B> (X^T.dY, 256x256 on a CTA pair)",
 }
 
 
@@ -395,28 +397,55 @@ def run_ours(args):
                 "per_call_ms": {n: per_call[n] / K for n in per_call},
                 "value_frac_of_peak": value / world / peak}
 
-    # end to end through the ABI with host buffers
+    # End to end through the ABI with host buffers: every step uploads its
+    # inputs from pinned host memory and downloads its outputs.  Two device
+    # buffer sets alternate, so step i+1's upload (copy stream) and step
+    # i-1's download (second copy stream) overlap step i's kernels.
     E = max(1, args.e2e_steps)
+    steps = [step, MLPStep(tp, torch, host)]
     houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.outputs()]
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in houts)
-    torch.cuda.synchronize()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+
+    def e2e_run(n):
+        done_up = [torch.cuda.Event() for _ in range(n)]
+        done_comp = [torch.cuda.Event() for _ in range(n)]
+        done_down = [torch.cuda.Event() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(up)
+        for i in range(n):
+            st = steps[i % 2]
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(done_comp[i - 2])     # this buffer set's previous step is done
+                st.upload(host)
+                done_up[i].record(up)
+            comp.wait_event(done_up[i])
+            if i >= 2:
+                comp.wait_event(done_down[i - 2])       # its outputs have left the device
+            for _, fn in st.calls():
+                fn()
+            done_comp[i].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done_comp[i])
+                for h, d in zip(houts, st.outputs()):
+                    h.copy_(d, non_blocking=True)
+                done_down[i].record(down)
+        t1.record(down)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    e2e_run(2)
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        step.upload(host)
-        for _, fn in calls:
-            fn()
-        for h, d in zip(houts, step.outputs()):
-            h.copy_(d, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e2e_run(E), world)
     barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e = {"value": aggregate_value(STEP_FLOPS, E, world, e2e_ms), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+           "ms_per_step": e2e_ms / E,
+           "how": "pinned H2D of X, W1, W2, dY and D2H of Y, dX, dW1, dW2 every step, on two copy "
+                  "streams overlapping the kernels of the neighbouring steps (double-buffered)"}
 
     if rank != 0:
         return
@@ -658,6 +687,9 @@ def run_sweep(args):
 
 def main():
     args = parse()
+    if args.tile_mode and args.impl == "ours":
+        import gemm_reduce_fusion_gb300 as tp
+        tp.tp_debug_set(tp.TP_DEBUG_TILE_MODE, args.tile_mode)
     if args.profile_case:
         profile_case()
         return

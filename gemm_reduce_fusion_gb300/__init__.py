@@ -46,6 +46,7 @@ TP_OP_ROW_AR_UNFUSED = 6
 # tp_debug_key
 TP_DEBUG_TIMEOUT_MS = 0
 TP_DEBUG_DROP_LOAD = 1
+TP_DEBUG_TILE_MODE = 2
 
 
 class TPError(RuntimeError):

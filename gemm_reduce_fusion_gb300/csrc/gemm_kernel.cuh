@@ -219,6 +219,86 @@ __device__ __forceinline__ void epi_store1(const GemmParams& P, float v, void* o
   else reinterpret_cast<__nv_bfloat16*>(out)[off_out] = __float2bfloat16_rn(v);
 }
 
+// Epilogue of one accumulator for one epilogue warp: columns
+// [half*BN/2, (half+1)*BN/2) of TMEM row `t_row` (this thread's lane), i.e.
+// GEMM row `gi` of group `g`; raw fp32 partials when the launch splits K.
+template <int BN, bool OUT_T>
+__device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, int32_t sp, int32_t g,
+                                           int32_t gi, bool row_ok, uint32_t t_row, int half) {
+  constexpr int HALF = BN / 2;
+  constexpr int CW = HALF < 32 ? HALF : 32;
+#pragma unroll 1
+  for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += CW) {
+    uint32_t r[32];
+    if constexpr (CW == 32) {
+      tmem_ld_32x32b_x32(t_row + c0, r);
+    } else if constexpr (CW == 16) {
+      tmem_ld_32x32b_x16(t_row + c0, r);
+    } else {
+      tmem_ld_32x32b_x8(t_row + c0, r);
+    }
+    tmem_wait_ld();
+    if (!row_ok) continue;
+    const int32_t gj0 = u.nt * BN + c0;
+    if (P.n_split > 1) {
+      // raw fp32 partial, dense, in output orientation
+      float* part = P.partial + static_cast<int64_t>(sp * P.Gm * P.Gn + g) *
+                                    static_cast<int64_t>(P.rows_g) * P.cols_g;
+      if (OUT_T) {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          const int32_t gj = gj0 + i;
+          if (gj < P.cols_g) part[static_cast<int64_t>(gj) * P.rows_g + gi] = __uint_as_float(r[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < CW; i += 4) {
+          const int32_t gj = gj0 + i;
+          if (gj < P.cols_g)
+            *reinterpret_cast<float4*>(part + static_cast<int64_t>(gi) * P.cols_g + gj) =
+                make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                            __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+        }
+      }
+      continue;
+    }
+    if (OUT_T) {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        const int32_t gj = gj0 + i;
+        if (gj < P.cols_g) {
+          const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
+          const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
+          for (int rep = 0; rep < P.n_rep; ++rep)
+            epi_store1(P, __uint_as_float(r[i]), P.out[g + rep], P.aux[g], off_o, off_a);
+        }
+      }
+    } else {
+      const size_t esz = P.out_f32 ? 4 : 2;
+#pragma unroll
+      for (int i = 0; i < CW; i += 8) {
+        const int32_t gj = gj0 + i;
+        if (gj >= P.cols_g) continue;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[i + e]);
+        void* auxp = nullptr;
+        if (P.epi != EPI_NONE && P.aux[g] != nullptr) {
+          const size_t aesz = (P.epi == EPI_DGELU) ? 2 : esz;
+          auxp = static_cast<uint8_t*>(P.aux[g]) +
+                 (static_cast<int64_t>(gi) * P.ld_aux + gj) * static_cast<int64_t>(aesz);
+        }
+        epi8(P, v, auxp);
+        for (int rep = 0; rep < P.n_rep; ++rep) {
+          uint8_t* dst = static_cast<uint8_t*>(P.out[g + rep]) +
+                         (static_cast<int64_t>(gi) * P.ld_out + gj) * static_cast<int64_t>(esz);
+          store8(dst, P.out_f32 != 0, v);
+        }
+      }
+    }
+  }
+}
+
 template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
@@ -405,76 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int32_t sp = t % P.n_split;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int c0 = half * Cfg::HALF; c0 < (half + 1) * Cfg::HALF; c0 += Cfg::CW) {
-        uint32_t r[32];
-        if constexpr (Cfg::CW == 32) {
-          tmem_ld_32x32b_x32(t_row + c0, r);
-        } else if constexpr (Cfg::CW == 16) {
-          tmem_ld_32x32b_x16(t_row + c0, r);
-        } else {
-          tmem_ld_32x32b_x8(t_row + c0, r);
-        }
-        tmem_wait_ld();
-        if (!row_ok) continue;
-        const int32_t gj0 = u.nt * BN + c0;
-        if (P.n_split > 1) {
-          // raw fp32 partial, dense, in output orientation
-          float* part = P.partial + static_cast<int64_t>(sp * P.Gm * P.Gn + g) *
-                                        static_cast<int64_t>(P.rows_g) * P.cols_g;
-          if (OUT_T) {
-#pragma unroll
-            for (int i = 0; i < Cfg::CW; ++i) {
-              const int32_t gj = gj0 + i;
-              if (gj < P.cols_g) part[static_cast<int64_t>(gj) * P.rows_g + gi] = __uint_as_float(r[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < Cfg::CW; i += 4) {
-              const int32_t gj = gj0 + i;
-              if (gj < P.cols_g)
-                *reinterpret_cast<float4*>(part + static_cast<int64_t>(gi) * P.cols_g + gj) =
-                    make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-            }
-          }
-          continue;
-        }
-        if (OUT_T) {
-#pragma unroll
-          for (int i = 0; i < Cfg::CW; ++i) {
-            const int32_t gj = gj0 + i;
-            if (gj < P.cols_g) {
-              const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
-              const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
-              for (int rep = 0; rep < P.n_rep; ++rep)
-                epi_store1(P, __uint_as_float(r[i]), P.out[g + rep], P.aux[g], off_o, off_a);
-            }
-          }
-        } else {
-          const size_t esz = P.out_f32 ? 4 : 2;
-#pragma unroll
-          for (int i = 0; i < Cfg::CW; i += 8) {
-            const int32_t gj = gj0 + i;
-            if (gj >= P.cols_g) continue;
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[i + e]);
-            void* auxp = nullptr;
-            if (P.epi != EPI_NONE && P.aux[g] != nullptr) {
-              const size_t aesz = (P.epi == EPI_DGELU) ? 2 : esz;
-              auxp = static_cast<uint8_t*>(P.aux[g]) +
-                     (static_cast<int64_t>(gi) * P.ld_aux + gj) * static_cast<int64_t>(aesz);
-            }
-            epi8(P, v, auxp);
-            for (int rep = 0; rep < P.n_rep; ++rep) {
-              uint8_t* dst = static_cast<uint8_t*>(P.out[g + rep]) +
-                             (static_cast<int64_t>(gi) * P.ld_out + gj) * static_cast<int64_t>(esz);
-              store8(dst, P.out_f32 != 0, v);
-            }
-          }
-        }
-      }
+      drain_tile<BN, OUT_T>(P, u, sp, g, gi, row_ok, t_row, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -491,6 +502,242 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------- CTA-pair kernel
+//
+// The same tile space with 256 x 256 tiles, each computed by a cluster of
+// two CTAs on two SMs: tcgen05.mma.cta_group::2 (M = 256, N = 256) reads CTA
+// r's 128 rows of A and 128 columns of B from CTA r's shared memory and
+// writes CTA r's 128 rows of the accumulator into CTA r's tensor memory, so
+// each SM stages 32 KiB per k-block instead of the 48 KiB of a 128 x 256
+// tile.  Protocol:
+//   - both producers wait on their own empty barrier, then load their
+//     halves; every load counts its bytes on the full barrier of CTA 0,
+//     whose producer arms it for both halves;
+//   - one thread of CTA 0 issues the pair MMAs and commits to the empty
+//     and accumulator-full barriers of both CTAs (multicast);
+//   - each CTA's epilogue warps drain its own tensor memory and release the
+//     accumulator on CTA 0's accumulator-empty barrier;
+//   - both CTAs meet at a cluster barrier before tensor memory is freed.
+
+constexpr int PAIR_STAGES = 6;
+
+template <bool A_MN, bool B_MN>
+struct PairCfg {
+  static constexpr int BN = 256;                       // pair tile N
+  static constexpr int BNH = 128;                      // B columns held by each CTA
+  static constexpr uint32_t A_BYTES = BM * BK * 2;     // 16 KiB
+  static constexpr uint32_t B_BYTES = BNH * BK * 2;    // 16 KiB
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t NUM_BARS = 2 * PAIR_STAGES + 5;
+  static constexpr uint32_t SMEM_BYTES = 1024 + PAIR_STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tp_gemm_pair_kernel(const __grid_constant__ GemmParams P) {
+  using Cfg = PairCfg<A_MN, B_MN>;
+  constexpr int STAGES = PAIR_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + STAGES * Cfg::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * Cfg::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  const int32_t first = static_cast<int32_t>(blockIdx.x >> 1);
+  const int32_t stride = static_cast<int32_t>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * NUM_EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producers (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      int32_t n_issued = 0;
+      bool ok = true;
+      for (int32_t t = first; t < P.num_units && ok; t += stride) {
+        const Unit u = decode_unit(P, t);
+        const int32_t arow = P.a_row_gm * u.gm + u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM;
+        const int32_t bcol = P.b_col_gn * u.gn + u.nt * Cfg::BN + static_cast<int32_t>(crank) * Cfg::BNH;
+        for (int32_t q = u.q0; q < u.q1; ++q) {
+          const int32_t s = q / P.kb_per_seg;
+          const int32_t kc = (q % P.kb_per_seg) * BK;
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
+            ok = false;
+            break;
+          }
+          if (blockIdx.x == 0 && n_issued++ == P.debug_drop_q) {
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          const CUtensorMap* am = &P.tmA[P.a_idx_gm * u.gm + P.a_idx_gn * u.gn + P.a_idx_s * s];
+          const CUtensorMap* bm = &P.tmB[P.b_idx_gm * u.gm + P.b_idx_gn * u.gn + P.b_idx_s * s];
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+          const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
+          const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
+          if (A_MN) {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d_pair(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kc);
+          } else {
+            tma_load_2d_pair(sa, am, fb, kc, arow);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < Cfg::BNH / 64; ++j)
+              tma_load_2d_pair(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kc);
+          } else {
+            tma_load_2d_pair(sb, bm, fb, kc, bcol);
+          }
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // CTA 0's full barriers count both CTAs' bytes: once its armed stages
+      // complete, every load of the pair for them has landed.
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) drain_wait(full_bar(s), (armed_parity >> s) & 1u, P.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ pair MMA issuer (CTA 0)
+      constexpr uint32_t idesc = make_idesc_bf16(2 * BM, Cfg::BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int32_t t = first; t < P.num_units && ok; t += stride) {
+        const Unit u = decode_unit(P, t);
+        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, P, abort_flag, 2u)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
+        for (int32_t q = u.q0; q < u.q1; ++q) {
+          if (!wait_bar(full_bar(stage), phase, P, abort_flag, 3u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
+          const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t ad = A_MN ? make_sw128_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                     : make_sw128_desc(sa + kk * (UMMA_K * 2), 16, 1024);
+            const uint64_t bd = B_MN ? make_sw128_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                     : make_sw128_desc(sb + kk * (UMMA_K * 2), 16, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (q > u.q0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit_pair(empty_bar(stage), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(tfull_bar(acc), 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit_pair(drain_bar, 0x1);
+      drain_wait(drain_bar, 0, P.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - 2) / 4;
+    const int row_in_tile = 32 * q + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int32_t t = first; t < P.num_units; t += stride) {
+      const Unit u = decode_unit(P, t);
+      bool ok = wait_bar(tfull_bar(acc), acc_phase, P, abort_flag, 4u);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int32_t g = u.gm * P.Gn + u.gn;
+      const int32_t gi = u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM + row_in_tile;
+      const bool row_ok = gi < P.rows_g;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::BN);
+      drain_tile<Cfg::BN, false>(P, u, 0, g, gi, row_ok, t_row, half);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  if (*abort_flag) {
+    // after a timeout, give the peer's copies into this CTA time to land
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) {
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();  // no CTA frees tensor memory or exits while its peer may use it
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

@@ -38,6 +38,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // else 2 s; tp_debug_set(TP_DEBUG_TIMEOUT_MS, ...) overrides it.
 std::atomic<uint64_t> g_timeout_override_ns{0};
 std::atomic<int64_t> g_debug_drop_q{-1};
+std::atomic<int64_t> g_debug_tile_mode{0};  // 0 auto, 1 single-CTA tiles only, 2 CTA pairs whenever possible
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -113,7 +114,47 @@ enum Variant : int {
   V_SW_KK16,   // swapped: A = W (K-major), B = tokens (K-major)
   V_SW_KK32,
   V_SW_KK64,
+  V_KN2,       // CTA pairs, 256x256 tiles: X . W
+  V_KK2,       //                           dY . W^T
+  V_MM2,       //                           X^T . dY
 };
+
+template <bool A_MN, bool B_MN>
+cudaError_t launch_pair(const GemmParams& P, int clusters, cudaStream_t s) {
+  using Cfg = PairCfg<A_MN, B_MN>;
+  auto k = tp_gemm_pair_kernel<A_MN, B_MN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // no more clusters than can be resident at once (persistent tiles)
+  static int max_active[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    if (max_active[dev] == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0) max_active[dev] = n;
+    }
+    if (max_active[dev] > 0 && clusters > max_active[dev]) {
+      clusters = max_active[dev];
+      cfg.gridDim = dim3(2 * clusters, 1, 1);
+    }
+  }
+  e = cudaLaunchKernelEx(&cfg, k, P);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
 cudaError_t launch_t(const GemmParams& P, int grid, cudaStream_t s) {
@@ -130,6 +171,9 @@ constexpr int stages_for(int bn) { return std::min(12, (220 * 1024) / (128 * 128
 
 cudaError_t launch_variant(int v, const GemmParams& P, int grid, cudaStream_t s) {
   switch (v) {
+    case V_KN2: return launch_pair<false, true>(P, grid, s);
+    case V_KK2: return launch_pair<false, false>(P, grid, s);
+    case V_MM2: return launch_pair<true, true>(P, grid, s);
     case V_KN: return launch_t<false, true, 256, false, kStagesWide>(P, grid, s);
     case V_KK: return launch_t<false, false, 256, false, kStagesWide>(P, grid, s);
     case V_MM: return launch_t<true, true, 256, false, kStagesWide>(P, grid, s);
@@ -149,6 +193,7 @@ cudaError_t launch_variant(int v, const GemmParams& P, int grid, cudaStream_t s)
 // need, computed from sizes alone (no pointers).
 struct Shape {
   bool swap = false;     // operand-swapped: tokens are the GEMM N axis
+  bool pair = false;     // 256x256 tiles on CTA pairs
   int bn = 256;          // tile N (token tile when swapped)
   int Gm = 1, Gn = 1, S = 1;
   int64_t rows_g = 0, cols_g = 0, kseg = 0;
@@ -169,7 +214,23 @@ void finish_shape(Shape* s) {
   s->kb_total = s->S * cdiv(s->kseg, BK);
   s->n_split = 1;
   s->kb_per_split = s->kb_total;
+  s->pair = false;
   if (s->units0 == 0 || s->kb_total == 0) return;
+  // 256x256 tiles on CTA pairs when a group has at least 256 rows and the
+  // pair tiles still fill the clusters; otherwise 128x256 tiles (with split-K
+  // when there are too few of them).
+  const int64_t mode = g_debug_tile_mode.load();
+  if (!s->swap && mode != 1) {
+    const int64_t pm = cdiv(s->rows_g, 2 * BM);
+    const int64_t pu = static_cast<int64_t>(s->Gm) * s->Gn * pm * s->n_tiles;
+    if (mode == 2 || (s->rows_g >= 2 * BM && pu >= kPlanSMs / 2)) {
+      s->pair = true;
+      s->m_tiles = pm;
+      s->units0 = pu;
+      s->chunk_tiles = cdiv(s->chunk_tiles, 2);
+      return;
+    }
+  }
   if (s->units0 < kPlanSMs) {
     // Deterministic split-K: choose the split that fills the SMs best, with
     // at least 4 k-blocks per split and at most 16 splits.
@@ -326,6 +387,7 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
                             const DevInfo& di, int phases) {
   const Shape& s = L.shape;
   if (s.empty()) return TP_OK;
+  if (s.pair) L.variant = L.variant == V_KN ? V_KN2 : L.variant == V_KK ? V_KK2 : V_MM2;
   GemmParams& P = L.P;
   P.status = static_cast<uint32_t*>(ws);
   P.out_f32 = out_dtype == TP_FP32 ? 1 : 0;
@@ -350,7 +412,8 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     return TP_OK;
   }
   if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  const int grid = static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
+  const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
+                         : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
   if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
   if (s.n_split > 1 && (phases & 2)) {
     ReduceParams R;
@@ -477,6 +540,10 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_DROP_LOAD:
       if (value < -1 || value > INT32_MAX) return TP_ERR_INVALID_ARG;
       g_debug_drop_q.store(value);
+      return TP_OK;
+    case TP_DEBUG_TILE_MODE:
+      if (value < 0 || value > 2) return TP_ERR_INVALID_ARG;
+      g_debug_tile_mode.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;
@@ -819,7 +886,7 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM) || !encode_map(&P.tmB[k], w[k], N, K, N, 256))
+          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM) || !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256))
             return TP_ERR_CUDA;
         } else {
           if (!encode_map(&P.tmA[k], w[k], N, K, N, BM) || !encode_map(&P.tmB[k], dy[k], N, M, N, s.bn))
@@ -878,7 +945,7 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmB[k], w[k], N, K, N, 256)) return TP_ERR_CUDA;
+          if (!encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256)) return TP_ERR_CUDA;
         } else {
           if (!encode_map(&P.tmA[k], w[k], N, K, N, BM)) return TP_ERR_CUDA;
         }

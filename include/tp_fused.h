@@ -231,8 +231,12 @@ tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* 
  *     the kernel latches TP_ERR_DEVICE_TIMEOUT, stops its other roles, waits
  *     (bounded) for its own copies and MMAs in flight, frees its tensor
  *     memory and returns; -1 turns the hook off.  No fault or trap is used.
+ *   TP_DEBUG_TILE_MODE: 0 (default) lets the planner choose 128x256 tiles on
+ *     one CTA or 256x256 tiles on a CTA pair; 1 forces single-CTA tiles; 2
+ *     uses CTA pairs for every non-swapped launch (parity testing of both
+ *     tile paths at small, ragged sizes).
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
-typedef enum { TP_DEBUG_TIMEOUT_MS = 0, TP_DEBUG_DROP_LOAD = 1 } tp_debug_key;
+typedef enum { TP_DEBUG_TIMEOUT_MS = 0, TP_DEBUG_DROP_LOAD = 1, TP_DEBUG_TILE_MODE = 2 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 
 /* Static description of a status code. */

@@ -369,3 +369,91 @@ def test_unfused_baseline_exact(tp, p, M, N, K, chunk):
         else:
             tp.tp_row_linear_fwd_unfused(dx, dw, y[0].t, wsp, chunk, phases=3)
         check_exact(y[0], ref, True)
+
+
+# ------------------------------------------------------------------ both tile paths
+
+@pytest.fixture
+def tile_mode(tp, request):
+    """Force 128x256 single-CTA tiles (1) or 256x256 CTA-pair tiles (2)."""
+    assert tp.tp_debug_set(tp.TP_DEBUG_TILE_MODE, request.param) == tp.TP_OK
+    yield request.param
+    tp.tp_debug_set(tp.TP_DEBUG_TILE_MODE, 0)
+
+
+@pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
+@pytest.mark.parametrize("p,M,N,K", [(1, 256, 256, 64), (2, 300, 520, 200), (3, 513, 264, 136), (4, 1300, 776, 72)])
+def test_tile_paths_row_ops_exact(tp, tile_mode, p, M, N, K):
+    xs = [ints((M, K), 500 + r) for r in range(p)]
+    ws = [ints((K, N), 510 + r) for r in range(p)]
+    y = outs([(M, N)], True)
+    tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(b) for b in ws], [y[0].t],
+                                   ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0), 0)
+    check_exact(y[0], oracle.row_fwd_allreduce(xs, ws), True)
+    Mr = M - M % p
+    xr = [a[:Mr] for a in xs]
+    ys = outs([(Mr // p, N)] * p, False)
+    tp.tp_row_linear_fwd_reducescatter([dev(a) for a in xr], [dev(b) for b in ws], [g.t for g in ys],
+                                       ws_for(tp, tp.TP_OP_ROW_RS, p, Mr, N, K, 0), 0)
+    for g, r in zip(ys, oracle.row_fwd_reducescatter(xr, ws)):
+        check_exact(g, r, False)
+    dy = ints((M, N), 520)
+    dx = outs([(M, K)] * p, True)
+    dw = outs([(K, N)] * p, True)
+    tp.tp_row_linear_bwd([dev(a) for a in xs], [dev(b) for b in ws], dev(dy), [g.t for g in dx],
+                         [g.t for g in dw], ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0))
+    for g, r in zip(dx, oracle.row_bwd_dx(ws, dy)):
+        check_exact(g, r, True)
+    for g, r in zip(dw, oracle.row_bwd_dw(xs, dy)):
+        check_exact(g, r, True)
+
+
+@pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
+@pytest.mark.parametrize("p,M,N,K", [(1, 256, 256, 64), (3, 300, 264, 136), (2, 777, 520, 200)])
+def test_tile_paths_col_ops_exact(tp, tile_mode, p, M, N, K):
+    x = ints((M, K), 530)
+    ws = [ints((K, N), 540 + k) for k in range(p)]
+    y = outs([(M, N)] * p, False)
+    tp.tp_col_linear_fwd(dev(x), [dev(b) for b in ws], [g.t for g in y], ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, 0))
+    refs, _ = oracle.col_fwd(x, ws)
+    for g, r in zip(y, refs):
+        check_exact(g, r, False)
+    dys = [ints((M, N), 550 + k) for k in range(p)]
+    dx = outs([(M, K)], True)
+    dw = outs([(K, N)] * p, True)
+    tp.tp_col_linear_bwd(dev(x), [dev(b) for b in ws], [dev(d) for d in dys], dx[0].t, [g.t for g in dw],
+                         ws_for(tp, tp.TP_OP_COL_BWD, p, M, N, K, 0))
+    check_exact(dx[0], oracle.col_bwd_dx(ws, dys), True)
+    for g, r in zip(dw, oracle.col_bwd_dw(x, dys)):
+        check_exact(g, r, True)
+    Mg = M - M % p
+    xs = [x[s * (Mg // p):(s + 1) * (Mg // p)] for s in range(p)]
+    ya = outs([(Mg, N)] * p, True)
+    tp.tp_ag_matmul([dev(a) for a in xs], [dev(b) for b in ws], [g.t for g in ya],
+                    ws_for(tp, tp.TP_OP_AG_MM, p, Mg, N, K, 0))
+    refa, _, _ = oracle.ag_matmul(xs, ws)
+    for g, r in zip(ya, refa):
+        check_exact(g, r, True)
+
+
+@pytest.mark.parametrize("tile_mode", [2], indirect=True)
+def test_pair_path_gelu_epilogues(tp, tile_mode):
+    p, M, N, K = 2, 520, 264, 136
+    x = synth.normal_bf16((M, K), 560, sigma=1.0 / np.sqrt(K))
+    ws = [synth.normal_bf16((K, N), 561 + k) for k in range(p)]
+    y = outs([(M, N)] * p, False)
+    h = outs([(M, N)] * p, False)
+    tp.tp_col_linear_fwd(dev(x), [dev(b) for b in ws], [g.t for g in y], ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, 0),
+                         epi=tp.TP_EPI_GELU, preact=[g.t for g in h])
+    refs, hs = oracle.col_fwd(x, ws, apply_gelu=True)
+    for k in range(p):
+        assert_close(host_f64(y[k].t), refs[k], False, "pair gelu")
+        assert_close(host_f64(h[k].t), hs[k], False, "pair preact")
+    w2 = [synth.normal_bf16((K, N), 570 + k, sigma=1.0 / np.sqrt(N)) for k in range(p)]
+    dy = synth.normal_bf16((M, N), 580)
+    hk = [synth.normal_bf16((M, K), 590 + k) for k in range(p)]
+    dx = outs([(M, K)] * p, False)
+    tp.tp_row_linear_bwd(None, [dev(b) for b in w2], dev(dy), [g.t for g in dx], None,
+                         ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0), preact=[dev(a) for a in hk])
+    for g, r in zip(dx, oracle.row_bwd_dx(w2, dy, preacts=hk)):
+        assert_close(host_f64(g.t), r, False, "pair dgelu")
