@@ -58,6 +58,8 @@ struct GemmParams {
   int32_t chunk_tiles;       // tiles per chunk along the chunked axis
   int32_t chunk_on_n;        // chunks run along GEMM N (operand-swapped kernels)
   int32_t band;              // other-axis tiles per raster band inside a chunk
+  int32_t map3d;             // operand maps are 3-D (64-element chunks as the third axis):
+                             // one copy per operand per stage
   int32_t num_units;         // Gm*Gn*m_tiles*n_tiles*n_split
   int32_t S;                 // K segments (ranks reduced)
   int32_t kb_per_seg;        // k-blocks per segment
@@ -394,17 +396,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
           const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
           const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
-          if (A_MN) {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kc);
+          if (P.map3d) {
+            if (A_MN) tma_load_3d(sa, am, fb, 0, kc, arow / 64);
+            else tma_load_3d(sa, am, fb, 0, arow, kc / 64);
+            if (B_MN) tma_load_3d(sb, bm, fb, 0, kc, bcol / 64);
+            else tma_load_3d(sb, bm, fb, 0, bcol, kc / 64);
           } else {
-            tma_load_2d(sa, am, fb, kc, arow);
-          }
-          if (B_MN) {
+            if (A_MN) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kc);
-          } else {
-            tma_load_2d(sb, bm, fb, kc, bcol);
+              for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kc);
+            } else {
+              tma_load_2d(sa, am, fb, kc, arow);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kc);
+            } else {
+              tma_load_2d(sb, bm, fb, kc, bcol);
+            }
           }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -512,7 +521,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // r's 128 rows of A and 128 columns of B from CTA r's shared memory and
 // writes CTA r's 128 rows of the accumulator into CTA r's tensor memory, so
 // each SM stages 32 KiB per k-block instead of the 48 KiB of a 128 x 256
-// tile.  Protocol:
+// tile; k-blocks are PAIR_BK = 128 deep (3 stages of 64 KiB per CTA), which
+// halves the barrier round trips and copies per byte.  Protocol:
 //   - both producers wait on their own empty barrier, then load their
 //     halves; every load counts its bytes on the full barrier of CTA 0,
 //     whose producer arms it for both halves;
@@ -522,25 +532,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //     accumulator on CTA 0's accumulator-empty barrier;
 //   - both CTAs meet at a cluster barrier before tensor memory is freed.
 
-constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_BK = 128;  // k-block depth of the pair kernel: 64 KiB stages, fewer round trips
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int BKP>
 struct PairCfg {
   static constexpr int BN = 256;                       // pair tile N
   static constexpr int BNH = 128;                      // B columns held by each CTA
-  static constexpr uint32_t A_BYTES = BM * BK * 2;     // 16 KiB
-  static constexpr uint32_t B_BYTES = BNH * BK * 2;    // 16 KiB
+  static constexpr uint32_t A_BYTES = BM * BKP * 2;    // 32 KiB at BKP = 128
+  static constexpr uint32_t B_BYTES = BNH * BKP * 2;   // 32 KiB
+  static constexpr int STAGES = (192 * 1024) / (A_BYTES + B_BYTES);
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t NUM_BARS = 2 * PAIR_STAGES + 5;
-  static constexpr uint32_t SMEM_BYTES = 1024 + PAIR_STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
 };
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int BKP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tp_gemm_pair_kernel(const __grid_constant__ GemmParams P) {
-  using Cfg = PairCfg<A_MN, B_MN>;
-  constexpr int STAGES = PAIR_STAGES;
+  using Cfg = PairCfg<A_MN, B_MN, BKP>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int KC = BKP / 64;  // 64-wide K chunks per k-block
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -602,7 +614,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int32_t bcol = P.b_col_gn * u.gn + u.nt * Cfg::BN + static_cast<int32_t>(crank) * Cfg::BNH;
         for (int32_t q = u.q0; q < u.q1; ++q) {
           const int32_t s = q / P.kb_per_seg;
-          const int32_t kc = (q % P.kb_per_seg) * BK;
+          const int32_t kc = (q % P.kb_per_seg) * BKP;
           if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
             ok = false;
             break;
@@ -620,19 +632,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
           const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
           const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
-          if (A_MN) {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d_pair(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kc);
+          // Shared-memory tiles: K-major operands as KC consecutive [rows][64]
+          // sub-tiles (one per 64-wide K chunk), MN-major operands as
+          // consecutive [BKP K-rows][64] sub-tiles (one per 64-wide MN block).
+          if (P.map3d) {
+            if (A_MN) tma_load_3d_pair(sa, am, fb, 0, kc, arow / 64);
+            else tma_load_3d_pair(sa, am, fb, 0, arow, kc / 64);
+            if (B_MN) tma_load_3d_pair(sb, bm, fb, 0, kc, bcol / 64);
+            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kc / 64);
           } else {
-            tma_load_2d_pair(sa, am, fb, kc, arow);
-          }
-          if (B_MN) {
+            if (A_MN) {
 #pragma unroll
-            for (int j = 0; j < Cfg::BNH / 64; ++j)
-              tma_load_2d_pair(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kc);
-          } else {
-            tma_load_2d_pair(sb, bm, fb, kc, bcol);
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d_pair(sa + j * (64 * BKP * 2), am, fb, arow + 64 * j, kc);
+            } else {
+#pragma unroll
+              for (int h = 0; h < KC; ++h) tma_load_2d_pair(sa + h * (BM * 128), am, fb, kc + 64 * h, arow);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < Cfg::BNH / 64; ++j)
+                tma_load_2d_pair(sb + j * (64 * BKP * 2), bm, fb, bcol + 64 * j, kc);
+            } else {
+#pragma unroll
+              for (int h = 0; h < KC; ++h)
+                tma_load_2d_pair(sb + h * (Cfg::BNH * 128), bm, fb, kc + 64 * h, bcol);
+            }
           }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -671,11 +696,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
           const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t ad = A_MN ? make_sw128_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
-                                     : make_sw128_desc(sa + kk * (UMMA_K * 2), 16, 1024);
-            const uint64_t bd = B_MN ? make_sw128_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
-                                     : make_sw128_desc(sb + kk * (UMMA_K * 2), 16, 1024);
+          for (int kk = 0; kk < BKP / UMMA_K; ++kk) {
+            // K-major: chunk kk/4, 32-byte step (kk%4) inside the swizzled row;
+            // MN-major: 16 K-rows of 128 bytes per step.
+            const uint32_t ka = (kk / 4) * (BM * 128) + (kk % 4) * (UMMA_K * 2);
+            const uint32_t kb = (kk / 4) * (Cfg::BNH * 128) + (kk % 4) * (UMMA_K * 2);
+            const uint64_t ad = A_MN ? make_sw128_desc(sa + kk * (UMMA_K * 128), 64 * BKP * 2, 1024)
+                                     : make_sw128_desc(sa + ka, 16, 1024);
+            const uint64_t bd = B_MN ? make_sw128_desc(sb + kk * (UMMA_K * 128), 64 * BKP * 2, 1024)
+                                     : make_sw128_desc(sb + kb, 16, 1024);
             umma_bf16_pair(d_tmem, ad, bd, idesc, (q > u.q0 || kk > 0) ? 1u : 0u);
           }
           umma_commit_pair(empty_bar(stage), 0x3);
@@ -712,7 +741,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = gi < P.rows_g;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * Cfg::BN);
-      drain_tile<Cfg::BN, false>(P, u, 0, g, gi, row_ok, t_row, half);
+      drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));

@@ -87,20 +87,41 @@ tp_status device_info(DevInfo* out) {
   return TP_OK;
 }
 
-// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per
-// row, `outer` rows, row pitch `ld` elements; box = 64 x box_outer.
+// bf16 tensor map with 128-byte swizzle over a row-major matrix with
+// `inner` contiguous elements per row, `outer` rows and a row pitch of `ld`
+// elements.
+//   chunks == 0: 2-D map, box = 64 x box_outer;
+//   chunks >= 1: 3-D map (64-element chunk, row, chunk index) with the chunk
+//     index stepping 128 bytes along the row; box = 64 x box_outer x chunks,
+//     which lands in shared memory as `chunks` consecutive 64-wide swizzled
+//     sub-tiles -- one copy instead of `chunks`.  Needs inner % 64 == 0.
 bool encode_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
-                int box_outer) {
+                int box_outer, int chunks) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_outer)};
-  cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  if (chunks == 0) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_outer)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  if (inner % 64 != 0) return false;
+  cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(outer), static_cast<cuuint64_t>(inner / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, 128u};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_outer), static_cast<cuuint32_t>(chunks)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// 3-D maps are used for a launch when every operand's contiguous extent is
+// a multiple of 64 (K and N here); otherwise 2-D maps with one copy per
+// 64-wide sub-tile.
+inline bool use_3d(int64_t N, int64_t K) { return N % 64 == 0 && K % 64 == 0; }
 
 // ------------------------------------------------------------------ kernel variants
 
@@ -121,8 +142,8 @@ enum Variant : int {
 
 template <bool A_MN, bool B_MN>
 cudaError_t launch_pair(const GemmParams& P, int clusters, cudaStream_t s) {
-  using Cfg = PairCfg<A_MN, B_MN>;
-  auto k = tp_gemm_pair_kernel<A_MN, B_MN>;
+  using Cfg = PairCfg<A_MN, B_MN, PAIR_BK>;
+  auto k = tp_gemm_pair_kernel<A_MN, B_MN, PAIR_BK>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::SMEM_BYTES));
   if (e != cudaSuccess) return e;
@@ -194,6 +215,7 @@ cudaError_t launch_variant(int v, const GemmParams& P, int grid, cudaStream_t s)
 struct Shape {
   bool swap = false;     // operand-swapped: tokens are the GEMM N axis
   bool pair = false;     // 256x256 tiles on CTA pairs
+  bool no_pair = false;  // the launch needs split-K (e.g. the unfused baseline)
   int bn = 256;          // tile N (token tile when swapped)
   int Gm = 1, Gn = 1, S = 1;
   int64_t rows_g = 0, cols_g = 0, kseg = 0;
@@ -220,7 +242,7 @@ void finish_shape(Shape* s) {
   // pair tiles still fill the clusters; otherwise 128x256 tiles (with split-K
   // when there are too few of them).
   const int64_t mode = g_debug_tile_mode.load();
-  if (!s->swap && mode != 1) {
+  if (!s->swap && !s->no_pair && mode != 1) {
     const int64_t pm = cdiv(s->rows_g, 2 * BM);
     const int64_t pu = static_cast<int64_t>(s->Gm) * s->Gn * pm * s->n_tiles;
     if (mode == 2 || (s->rows_g >= 2 * BM && pu >= kPlanSMs / 2)) {
@@ -290,6 +312,7 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
       s.S = p; s.kseg = K; tok(M, N, 1, 1); break;
     case TP_OP_ROW_AR_UNFUSED:
       s.S = p; s.kseg = K; tok(M, N, 1, 1);
+      s.no_pair = true;
       finish_shape(&s);
       if (s.units0 > 0 && s.kb_total > 0) {  // one split per rank: fp32 partial per rank
         s.n_split = p;
@@ -360,9 +383,9 @@ void fill_common(GemmParams* P, const Shape& s) {
   const int64_t TO = s.swap ? s.Gm * s.m_tiles : s.Gn * s.n_tiles;
   P->band = static_cast<int32_t>(std::max<int64_t>(1, s.swap ? TO : std::min<int64_t>(8, TO)));
   P->S = s.S;
-  P->kb_per_seg = static_cast<int32_t>(cdiv(s.kseg, BK));
+  P->kb_per_seg = static_cast<int32_t>(cdiv(s.kseg, s.pair ? PAIR_BK : BK));
   P->n_split = s.n_split;
-  P->kb_per_split = static_cast<int32_t>(s.kb_per_split);
+  P->kb_per_split = static_cast<int32_t>(s.pair ? s.S * P->kb_per_seg : s.kb_per_split);
   P->num_units = static_cast<int32_t>(s.units0 * s.n_split);
   P->rows_g = static_cast<int32_t>(s.rows_g);
   P->cols_g = static_cast<int32_t>(s.cols_g);
@@ -664,13 +687,17 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   fill_common(&L.P, L.shape);
   GemmParams& P = L.P;
   const Shape& s = L.shape;
+  const bool m3 = use_3d(N, K);
+  P.map3d = m3 ? 1 : 0;
   if (K > 0) {
     for (int r = 0; r < p; ++r) {
       if (!s.swap) {
-        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM) || !encode_map(&P.tmB[r], w[r], N, K, N, 64))
+        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+            !encode_map(&P.tmB[r], w[r], N, K, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
           return TP_ERR_CUDA;
       } else {
-        if (!encode_map(&P.tmA[r], w[r], N, K, N, 64) || !encode_map(&P.tmB[r], x[r], K, M, K, s.bn))
+        if (!encode_map(&P.tmA[r], w[r], N, K, N, 64, m3 ? 2 : 0) ||
+            !encode_map(&P.tmB[r], x[r], K, M, K, s.bn, m3 ? 1 : 0))
           return TP_ERR_CUDA;
       }
     }
@@ -752,21 +779,24 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
   fill_common(&L.P, L.shape);
   GemmParams& P = L.P;
   const Shape& s = L.shape;
+  const bool m3 = use_3d(N, K);
+  P.map3d = m3 ? 1 : 0;
   const size_t es = esize(dt);
   if (K > 0) {
     for (int k = 0; k < p; ++k) {
       // weights: MN-major in both orientations ([K, N] row-major)
       CUtensorMap* wm = s.swap ? &P.tmA[k] : &P.tmB[k];
-      if (!encode_map(wm, w[k], N, K, N, 64)) return TP_ERR_CUDA;
+      if (!encode_map(wm, w[k], N, K, N, s.pair ? PAIR_BK : 64, m3 ? (s.swap ? 2 : s.pair ? 2 : 4) : 0))
+        return TP_ERR_CUDA;
     }
     const int tok_box = s.swap ? s.bn : BM;
     if (!ag) {
       CUtensorMap* xm = s.swap ? &P.tmB[0] : &P.tmA[0];
-      if (!encode_map(xm, x1, K, M, K, tok_box)) return TP_ERR_CUDA;
+      if (!encode_map(xm, x1, K, M, K, tok_box, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
     } else {
       for (int t = 0; t < p; ++t) {
         CUtensorMap* xm = s.swap ? &P.tmB[t] : &P.tmA[t];
-        if (!encode_map(xm, xs[t], K, Mp, K, tok_box)) return TP_ERR_CUDA;
+        if (!encode_map(xm, xs[t], K, Mp, K, tok_box, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
       }
     }
   }
@@ -828,11 +858,14 @@ static tp_status weight_grad(const Shape& s, const void* const* xk, const void* 
   init_params(&L.P);
   fill_common(&L.P, s);
   GemmParams& P = L.P;
+  const bool m3 = use_3d(N, K);
+  P.map3d = m3 ? 1 : 0;
   if (M > 0) {
     for (int k = 0; k < (xk ? p : 1); ++k)
-      if (!encode_map(&P.tmA[k], xk ? xk[k] : x1, K, M, K, 64)) return TP_ERR_CUDA;
+      if (!encode_map(&P.tmA[k], xk ? xk[k] : x1, K, M, K, s.pair ? PAIR_BK : 64, m3 ? 2 : 0)) return TP_ERR_CUDA;
     for (int k = 0; k < (dyk ? p : 1); ++k)
-      if (!encode_map(&P.tmB[k], dyk ? dyk[k] : dy1, N, M, N, 64)) return TP_ERR_CUDA;
+      if (!encode_map(&P.tmB[k], dyk ? dyk[k] : dy1, N, M, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
+        return TP_ERR_CUDA;
   }
   // the p problems are the groups (along N for the column case, along M for the row case)
   if (s.Gn == p && s.Gm == 1) {
@@ -883,13 +916,17 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
     fill_common(&L.P, L.shape);
     GemmParams& P = L.P;
     const Shape& s = L.shape;
+    const bool m3 = use_3d(N, K);
+    P.map3d = m3 ? 1 : 0;
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM) || !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256))
+          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+              !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0))
             return TP_ERR_CUDA;
         } else {
-          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM) || !encode_map(&P.tmB[k], dy[k], N, M, N, s.bn))
+          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM, m3 ? 1 : 0) ||
+              !encode_map(&P.tmB[k], dy[k], N, M, N, s.bn, m3 ? 1 : 0))
             return TP_ERR_CUDA;
         }
       }
@@ -942,18 +979,20 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
     fill_common(&L.P, L.shape);
     GemmParams& P = L.P;
     const Shape& s = L.shape;
+    const bool m3 = use_3d(N, K);
+    P.map3d = m3 ? 1 : 0;
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256)) return TP_ERR_CUDA;
+          if (!encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
         } else {
-          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM)) return TP_ERR_CUDA;
+          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM, m3 ? 1 : 0)) return TP_ERR_CUDA;
         }
       }
       if (!s.swap) {
-        if (!encode_map(&P.tmA[0], dy, N, M, N, BM)) return TP_ERR_CUDA;
+        if (!encode_map(&P.tmA[0], dy, N, M, N, BM, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
       } else {
-        if (!encode_map(&P.tmB[0], dy, N, M, N, s.bn)) return TP_ERR_CUDA;
+        if (!encode_map(&P.tmB[0], dy, N, M, N, s.bn, m3 ? 1 : 0)) return TP_ERR_CUDA;
       }
     }
     if (!s.swap) P.b_idx_gn = 1;
@@ -1004,13 +1043,17 @@ extern "C" tp_status tp_row_linear_fwd_unfused(const void* const* x, const void*
   fill_common(&L.P, L.shape);
   GemmParams& P = L.P;
   const Shape& s = L.shape;
+  const bool m3 = use_3d(N, K);
+  P.map3d = m3 ? 1 : 0;
   if (K > 0) {
     for (int r = 0; r < p; ++r) {
       if (!s.swap) {
-        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM) || !encode_map(&P.tmB[r], w[r], N, K, N, 64))
+        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+            !encode_map(&P.tmB[r], w[r], N, K, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
           return TP_ERR_CUDA;
       } else {
-        if (!encode_map(&P.tmA[r], w[r], N, K, N, 64) || !encode_map(&P.tmB[r], x[r], K, M, K, s.bn))
+        if (!encode_map(&P.tmA[r], w[r], N, K, N, 64, m3 ? 2 : 0) ||
+            !encode_map(&P.tmB[r], x[r], K, M, K, s.bn, m3 ? 1 : 0))
           return TP_ERR_CUDA;
       }
     }

@@ -382,7 +382,8 @@ def tile_mode(tp, request):
 
 
 @pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
-@pytest.mark.parametrize("p,M,N,K", [(1, 256, 256, 64), (2, 300, 520, 200), (3, 513, 264, 136), (4, 1300, 776, 72)])
+@pytest.mark.parametrize("p,M,N,K", [(1, 256, 256, 64), (2, 300, 520, 200), (3, 513, 264, 136), (4, 1300, 776, 72),
+                                     (2, 300, 256, 192), (3, 130, 512, 320), (2, 640, 320, 448)])
 def test_tile_paths_row_ops_exact(tp, tile_mode, p, M, N, K):
     xs = [ints((M, K), 500 + r) for r in range(p)]
     ws = [ints((K, N), 510 + r) for r in range(p)]
@@ -409,7 +410,8 @@ def test_tile_paths_row_ops_exact(tp, tile_mode, p, M, N, K):
 
 
 @pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
-@pytest.mark.parametrize("p,M,N,K", [(1, 256, 256, 64), (3, 300, 264, 136), (2, 777, 520, 200)])
+@pytest.mark.parametrize("p,M,N,K", [(1, 256, 256, 64), (3, 300, 264, 136), (2, 777, 520, 200), (2, 300, 320, 192),
+                                     (4, 520, 256, 320)])
 def test_tile_paths_col_ops_exact(tp, tile_mode, p, M, N, K):
     x = ints((M, K), 530)
     ws = [ints((K, N), 540 + k) for k in range(p)]
