@@ -43,6 +43,8 @@ TP_OP_COL_BWD = 3
 TP_OP_ROW_BWD = 4
 TP_OP_AG_MM = 5
 TP_OP_ROW_AR_UNFUSED = 6
+TP_OP_AG_MM_BWD = 7
+TP_OP_ROW_RS_BWD = 8
 # tp_debug_key
 TP_DEBUG_TIMEOUT_MS = 0
 TP_DEBUG_DROP_LOAD = 1
@@ -75,6 +77,8 @@ def _load() -> ctypes.CDLL:
         "tp_row_linear_bwd": (I, [PP, PP, P, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_ag_matmul": (I, [PP, PP, PP, P, I, PP, I, L, L, L, L, I, P, S, P]),
         "tp_row_linear_fwd_unfused": (I, [PP, PP, P, I, L, L, L, L, I, I, P, S, P]),
+        "tp_ag_matmul_bwd": (I, [PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_bwd_reducescatter": (I, [PP, PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_pipeline_time": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, L]),
         "tp_num_chunks": (L, [L, L]),
         "tp_choose_chunk_m": (L, [I, I, L, L, L]),
@@ -126,6 +130,15 @@ def _dtype_code(t) -> int:
     if t.dtype == torch.float32:
         return TP_FP32
     raise ValueError(f"unsupported output dtype {t.dtype}")
+
+
+def _out_dtype(*groups) -> int:
+    """The single output dtype of a call: every output tensor must share it."""
+    codes = {_dtype_code(t) for g in groups if g is not None
+             for t in (g if isinstance(g, (list, tuple)) else [g])}
+    if len(codes) != 1:
+        raise ValueError("all outputs of one call must have the same dtype (bfloat16 or float32)")
+    return codes.pop()
 
 
 def _ws(ws):
@@ -210,7 +223,7 @@ def tp_col_linear_fwd(x, w: Sequence, y: Sequence, ws, epi: int = TP_EPI_NONE, p
     N = w[0].shape[1]
     wp, wb = _ws(ws)
     _check(_lib.tp_col_linear_fwd(_ptr(x), _arr(w), _arr(y), _arr(preact), epi, p, M, N, K, chunk_m,
-                                  _dtype_code(y[0]), wp, wb, _stream(stream)), "tp_col_linear_fwd")
+                                  _out_dtype(y, preact), wp, wb, _stream(stream)), "tp_col_linear_fwd")
 
 
 def tp_col_linear_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0,
@@ -219,10 +232,9 @@ def tp_col_linear_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0]
-    out = dx if dx is not None else dw[0]
     wp, wb = _ws(ws)
     _check(_lib.tp_col_linear_bwd(_ptr(x), _arr(w), _arr(dy), _ptr(dx), _arr(dw), p, M, N, K, chunk_m,
-                                  _dtype_code(out), wp, wb, _stream(stream)), "tp_col_linear_bwd")
+                                  _out_dtype(dx, dw), wp, wb, _stream(stream)), "tp_col_linear_bwd")
 
 
 def tp_row_linear_bwd(x, w: Sequence, dy, dx, dw, ws, preact=None, chunk_m: int = 0,
@@ -231,10 +243,9 @@ def tp_row_linear_bwd(x, w: Sequence, dy, dx, dw, ws, preact=None, chunk_m: int 
     p = len(w)
     K, N = w[0].shape
     M = dy.shape[0]
-    out = dx[0] if dx is not None else dw[0]
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_bwd(_arr(x), _arr(w), _ptr(dy), _arr(dx), _arr(dw), _arr(preact), p,
-                                  M, N, K, chunk_m, _dtype_code(out), wp, wb, _stream(stream)),
+                                  M, N, K, chunk_m, _out_dtype(dx, dw), wp, wb, _stream(stream)),
            "tp_row_linear_bwd")
 
 
@@ -246,8 +257,30 @@ def tp_ag_matmul(x: Sequence, w: Sequence, y: Sequence, ws, x_gathered=None,
     N = w[0].shape[1]
     wp, wb = _ws(ws)
     _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
-                             Mp * p, N, K, chunk_m, _dtype_code(y[0]), wp, wb, _stream(stream)),
+                             Mp * p, N, K, chunk_m, _out_dtype(y, preact), wp, wb, _stream(stream)),
            "tp_ag_matmul")
+
+
+def tp_ag_matmul_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0, stream=None) -> None:
+    """dx[s] = rows of sum_k dY_k A_k^T (ReduceScatter); dw[k] = [X_0;...]^T dY_k."""
+    p = len(w)
+    K, N = w[0].shape
+    M = dy[0].shape[0]
+    wp, wb = _ws(ws)
+    _check(_lib.tp_ag_matmul_bwd(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), p, M, N, K, chunk_m,
+                                 _out_dtype(dx, dw), wp, wb, _stream(stream)), "tp_ag_matmul_bwd")
+
+
+def tp_row_linear_bwd_reducescatter(x, w: Sequence, dy: Sequence, dx, dw, ws, preact=None, chunk_m: int = 0,
+                                    stream=None) -> None:
+    """dx[r] = [dY_0;...] A_r^T (* GeLU'(preact[r])) (AllGather); dw[r] = X_r^T [dY_0;...]."""
+    p = len(w)
+    K, N = w[0].shape
+    M = dy[0].shape[0] * p
+    wp, wb = _ws(ws)
+    _check(_lib.tp_row_linear_bwd_reducescatter(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), _arr(preact), p,
+                                                M, N, K, chunk_m, _out_dtype(dx, dw), wp, wb, _stream(stream)),
+           "tp_row_linear_bwd_reducescatter")
 
 
 def tp_row_linear_fwd_unfused(x: Sequence, w: Sequence, y, ws, chunk_m: int = 0, phases: int = 3,

@@ -69,6 +69,8 @@ struct GemmParams {
   int32_t b_idx_gm, b_idx_gn, b_idx_s;
   int32_t a_row_gm;          // GEMM-M coordinate offset of group gm in its A map
   int32_t b_col_gn;          // GEMM-N coordinate offset of group gn in its B map
+  int32_t a_koff_s, b_koff_s;  // K coordinate offset of segment s in the A / B map (a
+                               // contraction over tokens that walks the p row shards)
   int32_t rows_g, cols_g;    // valid GEMM rows / cols of one group
   int64_t ld_out, ld_aux;    // row pitch (elements) of out / aux
   int32_t out_f32;           // output is fp32 (else bf16)
@@ -378,6 +380,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int32_t q = u.q0; q < u.q1; ++q) {
           const int32_t s = q / P.kb_per_seg;
           const int32_t kc = (q % P.kb_per_seg) * BK;
+          const int32_t kca = kc + s * P.a_koff_s;
+          const int32_t kcb = kc + s * P.b_koff_s;
           if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
             ok = false;
             break;
@@ -397,22 +401,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
           const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
           if (P.map3d) {
-            if (A_MN) tma_load_3d(sa, am, fb, 0, kc, arow / 64);
-            else tma_load_3d(sa, am, fb, 0, arow, kc / 64);
-            if (B_MN) tma_load_3d(sb, bm, fb, 0, kc, bcol / 64);
-            else tma_load_3d(sb, bm, fb, 0, bcol, kc / 64);
+            if (A_MN) tma_load_3d(sa, am, fb, 0, kca, arow / 64);
+            else tma_load_3d(sa, am, fb, 0, arow, kca / 64);
+            if (B_MN) tma_load_3d(sb, bm, fb, 0, kcb, bcol / 64);
+            else tma_load_3d(sb, bm, fb, 0, bcol, kcb / 64);
           } else {
             if (A_MN) {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kc);
+              for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (64 * BK * 2), am, fb, arow + 64 * j, kca);
             } else {
-              tma_load_2d(sa, am, fb, kc, arow);
+              tma_load_2d(sa, am, fb, kca, arow);
             }
             if (B_MN) {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kc);
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (64 * BK * 2), bm, fb, bcol + 64 * j, kcb);
             } else {
-              tma_load_2d(sb, bm, fb, kc, bcol);
+              tma_load_2d(sb, bm, fb, kcb, bcol);
             }
           }
           armed |= 1u << stage;
@@ -615,6 +619,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int32_t q = u.q0; q < u.q1; ++q) {
           const int32_t s = q / P.kb_per_seg;
           const int32_t kc = (q % P.kb_per_seg) * BKP;
+          const int32_t kca = kc + s * P.a_koff_s;
+          const int32_t kcb = kc + s * P.b_koff_s;
           if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
             ok = false;
             break;
@@ -636,27 +642,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // sub-tiles (one per 64-wide K chunk), MN-major operands as
           // consecutive [BKP K-rows][64] sub-tiles (one per 64-wide MN block).
           if (P.map3d) {
-            if (A_MN) tma_load_3d_pair(sa, am, fb, 0, kc, arow / 64);
-            else tma_load_3d_pair(sa, am, fb, 0, arow, kc / 64);
-            if (B_MN) tma_load_3d_pair(sb, bm, fb, 0, kc, bcol / 64);
-            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kc / 64);
+            if (A_MN) tma_load_3d_pair(sa, am, fb, 0, kca, arow / 64);
+            else tma_load_3d_pair(sa, am, fb, 0, arow, kca / 64);
+            if (B_MN) tma_load_3d_pair(sb, bm, fb, 0, kcb, bcol / 64);
+            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kcb / 64);
           } else {
             if (A_MN) {
 #pragma unroll
               for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d_pair(sa + j * (64 * BKP * 2), am, fb, arow + 64 * j, kc);
+                tma_load_2d_pair(sa + j * (64 * BKP * 2), am, fb, arow + 64 * j, kca);
             } else {
 #pragma unroll
-              for (int h = 0; h < KC; ++h) tma_load_2d_pair(sa + h * (BM * 128), am, fb, kc + 64 * h, arow);
+              for (int h = 0; h < KC; ++h) tma_load_2d_pair(sa + h * (BM * 128), am, fb, kca + 64 * h, arow);
             }
             if (B_MN) {
 #pragma unroll
               for (int j = 0; j < Cfg::BNH / 64; ++j)
-                tma_load_2d_pair(sb + j * (64 * BKP * 2), bm, fb, bcol + 64 * j, kc);
+                tma_load_2d_pair(sb + j * (64 * BKP * 2), bm, fb, bcol + 64 * j, kcb);
             } else {
 #pragma unroll
               for (int h = 0; h < KC; ++h)
-                tma_load_2d_pair(sb + h * (Cfg::BNH * 128), bm, fb, kc + 64 * h, bcol);
+                tma_load_2d_pair(sb + h * (Cfg::BNH * 128), bm, fb, kcb + 64 * h, bcol);
             }
           }
           armed |= 1u << stage;

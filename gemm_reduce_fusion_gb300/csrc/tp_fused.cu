@@ -337,6 +337,28 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
       v.push_back(w);
       return v;
     }
+    case TP_OP_AG_MM_BWD: {
+      s.S = p; s.kseg = N; tok(Mp, K, p, 1);   // dX: ReduceScatter rows of sum_k dY_k A_k^T
+      finish_shape(&s);
+      v.push_back(s);
+      Shape w;  // dA_k = [X_0; ...; X_{p-1}]^T dY_k: segments walk the p token shards
+      w.S = p; w.kseg = Mp; w.rows_g = K; w.cols_g = N; w.Gm = 1; w.Gn = p;
+      w.chunk_tiles = cdiv(K, BM);
+      finish_shape(&w);
+      v.push_back(w);
+      return v;
+    }
+    case TP_OP_ROW_RS_BWD: {
+      s.S = 1; s.kseg = N; tok(Mp, K, p, p);   // dX_r: AllGather of dY, group = (source shard, r)
+      finish_shape(&s);
+      v.push_back(s);
+      Shape w;  // dA_r = X_r^T [dY_0; ...; dY_{p-1}]
+      w.S = p; w.kseg = Mp; w.rows_g = K; w.cols_g = N; w.Gm = p; w.Gn = 1;
+      w.chunk_tiles = cdiv(K, BM);
+      finish_shape(&w);
+      v.push_back(w);
+      return v;
+    }
     case TP_OP_ROW_BWD: {
       s.S = 1; s.kseg = N; tok(M, K, 1, p);
       finish_shape(&s);
@@ -1012,6 +1034,203 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
 }
 
 }  // extern "C"
+
+
+// ---------------------------------------------------------------- sequence-parallel backward
+
+extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w, const void* const* dy,
+                                      void* const* dx, void* const* dw, int p, int64_t M, int64_t N,
+                                      int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
+                                      size_t ws_bytes, cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
+  if (M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
+  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  const int64_t Mp = M / p;
+  const bool dx_work = dx != nullptr && M > 0 && K > 0;
+  const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dx), p, dx_work));
+  TP_TRY(check_ptrs(w, p, dx_work && N > 0));
+  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptrs(x, p, dw_work && M > 0));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
+  std::vector<Shape> shapes = op_shapes(TP_OP_AG_MM_BWD, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  {
+    std::vector<Range> ins, outs;
+    add_ranges(&ins, x, p, Mp * K * 2);
+    add_ranges(&ins, w, p, K * N * 2);
+    add_ranges(&ins, dy, p, M * N * 2);
+    if (dx) add_ranges(&outs, const_cast<const void* const*>(dx), p, Mp * K * esize(out_dtype));
+    if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  if (!dx_work && !dw_work) return TP_OK;
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  if (dx_work) {
+    Launch L;
+    L.shape = shapes[0];
+    init_params(&L.P);
+    fill_common(&L.P, L.shape);
+    GemmParams& P = L.P;
+    const Shape& s = L.shape;
+    const bool m3 = use_3d(N, K);
+    P.map3d = m3 ? 1 : 0;
+    if (N > 0) {
+      for (int k = 0; k < p; ++k) {
+        if (!s.swap) {
+          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+              !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0))
+            return TP_ERR_CUDA;
+        } else {
+          if (!encode_map(&P.tmA[k], w[k], N, K, N, BM, m3 ? 1 : 0) ||
+              !encode_map(&P.tmB[k], dy[k], N, M, N, s.bn, m3 ? 1 : 0))
+            return TP_ERR_CUDA;
+        }
+      }
+    }
+    P.a_idx_s = 1;
+    P.b_idx_s = 1;
+    if (!s.swap) P.a_row_gm = static_cast<int32_t>(Mp);  // groups along M pick their rows of dY_k
+    else P.b_col_gn = static_cast<int32_t>(Mp);
+    for (int j = 0; j < p; ++j) P.out[j] = dx[j];
+    P.ld_out = K;
+    P.epi = EPI_NONE;
+    L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
+    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
+  }
+  if (dw_work) {
+    Launch L;
+    L.shape = shapes[1];
+    init_params(&L.P);
+    fill_common(&L.P, L.shape);
+    GemmParams& P = L.P;
+    const Shape& s = L.shape;
+    const bool m3 = use_3d(N, K);
+    P.map3d = m3 ? 1 : 0;
+    if (M > 0) {
+      for (int t = 0; t < p; ++t) {
+        if (!encode_map(&P.tmA[t], x[t], K, Mp, K, s.pair ? PAIR_BK : 64, m3 ? 2 : 0) ||
+            !encode_map(&P.tmB[t], dy[t], N, M, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
+          return TP_ERR_CUDA;
+      }
+    }
+    P.a_idx_s = 1;                                 // segment s reads token shard X_s from row 0
+    P.b_idx_gn = 1;                                // group k reads dY_k ...
+    P.b_koff_s = static_cast<int32_t>(Mp);         // ... at rows s*M/p of segment s
+    for (int k = 0; k < p; ++k) P.out[k] = dw[k];
+    P.ld_out = N;
+    P.epi = EPI_NONE;
+    L.variant = V_MM;
+    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
+  }
+  return TP_OK;
+}
+
+extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const void* const* w,
+                                                     const void* const* dy, void* const* dx,
+                                                     void* const* dw, const void* const* preact, int p,
+                                                     int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                                     tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                                                     cudaStream_t stream) {
+  TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
+  if (M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
+  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  const int64_t Mp = M / p;
+  const bool dx_work = dx != nullptr && M > 0 && K > 0;
+  const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dx), p, dx_work));
+  TP_TRY(check_ptrs(w, p, dx_work && N > 0));
+  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptrs(x, p, dw_work && M > 0));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
+  TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
+  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_RS_BWD, p, M, N, K, chunk_m);
+  TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
+  {
+    std::vector<Range> ins, outs;
+    add_ranges(&ins, x, p, M * K * 2);
+    add_ranges(&ins, w, p, K * N * 2);
+    add_ranges(&ins, dy, p, Mp * N * 2);
+    add_ranges(&ins, preact, p, M * K * 2);
+    if (dx) add_ranges(&outs, const_cast<const void* const*>(dx), p, M * K * esize(out_dtype));
+    if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
+  }
+  if (!dx_work && !dw_work) return TP_OK;
+  DevInfo di;
+  TP_TRY(device_info(&di));
+  const size_t es = esize(out_dtype);
+  if (dx_work) {
+    Launch L;
+    L.shape = shapes[0];
+    init_params(&L.P);
+    fill_common(&L.P, L.shape);
+    GemmParams& P = L.P;
+    const Shape& s = L.shape;
+    const bool m3 = use_3d(N, K);
+    P.map3d = m3 ? 1 : 0;
+    if (N > 0) {
+      for (int t = 0; t < p; ++t) {
+        // shard t of dY (source rows) and weight A_t (output r = t)
+        if (!s.swap) {
+          if (!encode_map(&P.tmA[t], dy[t], N, Mp, N, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+              !encode_map(&P.tmB[t], w[t], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0))
+            return TP_ERR_CUDA;
+        } else {
+          if (!encode_map(&P.tmA[t], w[t], N, K, N, BM, m3 ? 1 : 0) ||
+              !encode_map(&P.tmB[t], dy[t], N, Mp, N, s.bn, m3 ? 1 : 0))
+            return TP_ERR_CUDA;
+        }
+      }
+    }
+    // standard: gm = source shard of dY, gn = output r; swapped: gm = r, gn = source shard
+    P.a_idx_gm = 1;
+    P.b_idx_gn = 1;
+    for (int gm = 0; gm < p; ++gm) {
+      for (int gn = 0; gn < p; ++gn) {
+        const int r = s.swap ? gm : gn;
+        const int src = s.swap ? gn : gm;
+        const int64_t off_o = static_cast<int64_t>(src) * Mp * K * es;
+        const int64_t off_a = static_cast<int64_t>(src) * Mp * K * 2;
+        P.out[gm * p + gn] = static_cast<uint8_t*>(dx[r]) + off_o;
+        P.aux[gm * p + gn] = preact ? static_cast<uint8_t*>(const_cast<void*>(preact[r])) + off_a : nullptr;
+      }
+    }
+    P.ld_out = K;
+    P.ld_aux = K;
+    P.epi = preact ? EPI_DGELU : EPI_NONE;
+    L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
+    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
+  }
+  if (dw_work) {
+    Launch L;
+    L.shape = shapes[1];
+    init_params(&L.P);
+    fill_common(&L.P, L.shape);
+    GemmParams& P = L.P;
+    const Shape& s = L.shape;
+    const bool m3 = use_3d(N, K);
+    P.map3d = m3 ? 1 : 0;
+    if (M > 0) {
+      for (int t = 0; t < p; ++t) {
+        if (!encode_map(&P.tmA[t], x[t], K, M, K, s.pair ? PAIR_BK : 64, m3 ? 2 : 0) ||
+            !encode_map(&P.tmB[t], dy[t], N, Mp, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
+          return TP_ERR_CUDA;
+      }
+    }
+    if (s.Gm == p) P.a_idx_gm = 1;              // group r reads X_r ...
+    else P.a_idx_gn = 1;
+    P.a_koff_s = static_cast<int32_t>(Mp);      // ... at token rows s*M/p in segment s
+    P.b_idx_s = 1;                              // segment s reads dY shard s from row 0
+    for (int r = 0; r < p; ++r) P.out[r] = dw[r];
+    P.ld_out = N;
+    P.epi = EPI_NONE;
+    L.variant = V_MM;
+    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
+  }
+  return TP_OK;
+}
 
 // ====================================================================== unfused baseline
 

@@ -83,7 +83,9 @@ typedef enum {
   TP_OP_COL_BWD = 3, /* tp_col_linear_bwd */
   TP_OP_ROW_BWD = 4, /* tp_row_linear_bwd */
   TP_OP_AG_MM = 5,   /* tp_ag_matmul */
-  TP_OP_ROW_AR_UNFUSED = 6  /* tp_row_linear_fwd_unfused */
+  TP_OP_ROW_AR_UNFUSED = 6, /* tp_row_linear_fwd_unfused */
+  TP_OP_AG_MM_BWD = 7,      /* tp_ag_matmul_bwd */
+  TP_OP_ROW_RS_BWD = 8      /* tp_row_linear_bwd_reducescatter */
 } tp_op;
 
 /* Bytes of device workspace the call (op, p, M, N, K, chunk_m) needs, with
@@ -157,6 +159,36 @@ tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* 
                        int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                        tp_dtype out_dtype, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
+
+/* Sequence-parallel backward of AllGather+MatMul (the dual collectives of
+ * tp_ag_matmul).  [TP §2.6-2.7, §11.3]
+ *   dX_s = rows [s*M/p, (s+1)*M/p) of sum_k dY_k . A_k^T   (ReduceScatter of
+ *          the input gradient; the sum runs k = 0..p-1 in one accumulator)
+ *          -> dx[s] [M/p, K] if dx != NULL
+ *   dA_k = [X_0; ...; X_{p-1}]^T . dY_k  (contraction over all M tokens; the
+ *          row shards X_s are read in place, in shard order)
+ *          -> dw[k] [K, N] if dw != NULL
+ *   x[s]: X_s [M/p, K] (read when dw != NULL); w[k]: A_k [K, N];
+ *   dy[k]: dY_k [M, N].  Requires M % p == 0.                              */
+tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w, const void* const* dy,
+                           void* const* dx, void* const* dw, int p, int64_t M, int64_t N, int64_t K,
+                           int64_t chunk_m, tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Sequence-parallel backward of MatMul+ReduceScatter (the dual collectives
+ * of tp_row_linear_fwd_reducescatter).  [TP §2.6-2.7, §11.3]
+ *   dX_r = [dY_0; ...; dY_{p-1}] . A_r^T, times GeLU'(H_r) when preact is
+ *          given (AllGather of the output gradient; the M-tiles of shard s
+ *          read dY_s in place) -> dx[r] [M, K] if dx != NULL
+ *   dA_r = X_r^T . [dY_0; ...; dY_{p-1}] -> dw[r] [K, N] if dw != NULL
+ *   x[r]: X_r [M, K] (read when dw != NULL); w[r]: A_r [K, N];
+ *   dy[s]: dY_s [M/p, N]; preact[r]: H_r [M, K] bf16 or NULL.
+ *   Requires M % p == 0.                                                    */
+tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const void* const* w,
+                                          const void* const* dy, void* const* dx, void* const* dw,
+                                          const void* const* preact, int p, int64_t M, int64_t N,
+                                          int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
+                                          size_t ws_bytes, cudaStream_t stream);
 
 /* Unfused baseline of the row-parallel MatMul+AllReduce, for measurement.
  * [M027 §04: time the MatMul and the collective separately]

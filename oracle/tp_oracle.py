@@ -224,3 +224,38 @@ def allreduce_bytes(p: int, msg_bytes: float) -> float:
 def allgather_bytes(p: int, msg_bytes: float) -> float:
     """AllGather (and ReduceScatter) volume per rank, (p-1)/p * msg.  [TP §2.6-2.7]"""
     return (p - 1) / p * msg_bytes
+
+
+# ---------------------------------------------------------------- sequence-parallel backward
+
+def ag_matmul_bwd_dx(ws, dys) -> list[np.ndarray]:
+    """Backward of AllGather+MatMul, input gradient: the column backward's
+    dX = sum_k dY_k . A_k^T (k in order), then ReduceScatter of its rows:
+    shard s keeps rows [s*M/p, (s+1)*M/p).  [TP §2.6-2.7: the AllGather's
+    backward is a ReduceScatter; §11.3]"""
+    dx = col_bwd_dx(ws, dys)
+    p = len(ws)
+    m = dx.shape[0]
+    assert m % p == 0
+    mp = m // p
+    return [dx[s * mp:(s + 1) * mp] for s in range(p)]
+
+
+def ag_matmul_bwd_dw(xs, dys) -> list[np.ndarray]:
+    """Backward of AllGather+MatMul, weight gradient: dA_k = X^T . dY_k with
+    X = [X_0; ...; X_{p-1}] the gathered input.  [TP §三, §11.3]"""
+    return col_bwd_dw(np.vstack([np.asarray(x, dtype=np.uint16) for x in xs]), dys)
+
+
+def row_rs_bwd_dx(ws, dys, preacts=None) -> list[np.ndarray]:
+    """Backward of MatMul+ReduceScatter, input gradient: the output gradient
+    is gathered, dY = [dY_0; ...; dY_{p-1}], then dX_r = dY . A_r^T
+    (times GeLU'(H_r) with preacts).  [TP §2.6-2.7: the ReduceScatter's
+    backward is an AllGather; §四; §11.3]"""
+    return row_bwd_dx(ws, np.vstack([np.asarray(d, dtype=np.uint16) for d in dys]), preacts)
+
+
+def row_rs_bwd_dw(xs, dys) -> list[np.ndarray]:
+    """Backward of MatMul+ReduceScatter, weight gradient: dA_r = X_r^T . dY
+    with dY the gathered output gradient.  [TP §四, §11.3]"""
+    return row_bwd_dw(xs, np.vstack([np.asarray(d, dtype=np.uint16) for d in dys]))

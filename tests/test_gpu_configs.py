@@ -198,6 +198,53 @@ def test_config4_sequence_parallel_pair(tp):
     assert_close(y_gpu, yr, False, "MatMul+ReduceScatter")
 
 
+def test_config4_sequence_parallel_pair_backward(tp):
+    """The dual of the SP pair: FC2's MatMul+ReduceScatter backward gathers dY
+    (with GeLU'), FC1's AllGather+MatMul backward reduce-scatters dX."""
+    inp = synth.config4_inputs()
+    p, Mp, h, nk = 8, 1024, 8192, 3584
+    M = p * Mp
+    dys = [synth.normal_bf16((Mp, h), synth.seed_for(43, s)) for s in range(p)]
+    XS, W1, W2 = [dev(a) for a in inp["x"]], [dev(a) for a in inp["w1"]], [dev(a) for a in inp["w2"]]
+    DYS = [dev(d) for d in dys]
+    Z = [bf((M, nk)) for _ in range(p)]
+    H = [bf((M, nk)) for _ in range(p)]
+    DZ = [bf((M, nk)) for _ in range(p)]
+    DW2 = [bf((nk, h)) for _ in range(p)]
+    DXS = [bf((Mp, h)) for _ in range(p)]
+    DW1 = [bf((h, nk)) for _ in range(p)]
+    ws = ws_max(tp, [(tp.TP_OP_AG_MM, p, M, nk, h, 0), (tp.TP_OP_ROW_RS_BWD, p, M, h, nk, 0),
+                     (tp.TP_OP_AG_MM_BWD, p, M, nk, h, 0)])
+    tp.tp_ag_matmul(XS, W1, Z, ws, epi=tp.TP_EPI_GELU, preact=H)
+    tp.tp_row_linear_bwd_reducescatter(Z, W2, DYS, DZ, DW2, ws, preact=H)
+    tp.tp_ag_matmul_bwd(XS, W1, DZ, DXS, DW1, ws)
+    assert tp.tp_get_device_status(ws) == tp.TP_OK
+    rows = sample_idx(M, extra=[s * Mp + d for s in range(p) for d in (0, Mp - 1)])
+    h_b = [host_bits(t) for t in H]
+    z_b = [host_bits(t) for t in Z]
+    dz_b = [host_bits(t) for t in DZ]
+    dy_full = np.vstack(dys)
+    dzr = oracle.row_bwd_dx(inp["w2"], dy_full[rows], preacts=[a[rows] for a in h_b])
+    for k in range(p):
+        assert_close(rows_of(DZ[k], rows), dzr[k], False, f"SP bwd dZ {k}")
+    cols = sample_idx(h, seed=11)
+    dw2r = oracle.row_rs_bwd_dw(z_b, [d[:, cols] for d in dys])
+    for k in range(p):
+        assert_close(host_f64(DW2[k])[:, cols], dw2r[k], False, f"SP bwd dW2 {k}")
+    dxr = oracle.col_bwd_dx(inp["w1"], [d[rows] for d in dz_b])
+    dx_gpu = host_f64(torch_cat(DXS))[rows]
+    assert_close(dx_gpu, dxr, False, "SP bwd dX (ReduceScatter)")
+    c1 = sample_idx(nk, seed=12)
+    dw1r = oracle.ag_matmul_bwd_dw(inp["x"], [d[:, c1] for d in dz_b])
+    for k in range(p):
+        assert_close(host_f64(DW1[k])[:, c1], dw1r[k], False, f"SP bwd dW1 {k}")
+
+
+def torch_cat(ts):
+    import torch
+    return torch.cat(ts, 0)
+
+
 # ------------------------------------------------------------------ 5: GPT-3-scale MLP, chunk sweep
 
 @pytest.mark.parametrize("M,chunks", [(2048, (0, 16, 64, 256, 1024, 2048)), (16, (0, 16))])

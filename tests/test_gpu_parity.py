@@ -459,3 +459,61 @@ def test_pair_path_gelu_epilogues(tp, tile_mode):
                          ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0), preact=[dev(a) for a in hk])
     for g, r in zip(dx, oracle.row_bwd_dx(w2, dy, preacts=hk)):
         assert_close(host_f64(g.t), r, False, "pair dgelu")
+
+
+# ------------------------------------------------------------------ sequence-parallel backward
+
+SP_BWD_CASES = [  # p, M, N, K, chunk_m
+    (2, 256, 256, 128, 0), (4, 600, 264, 136, 0), (3, 300, 320, 192, 128), (2, 128, 136, 72, 32),
+    (4, 192, 256, 64, 16), (8, 1024, 512, 256, 0)]
+
+
+@pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
+@pytest.mark.parametrize("p,M,N,K,chunk", SP_BWD_CASES)
+def test_ag_matmul_bwd_exact(tp, tile_mode, p, M, N, K, chunk):
+    Mp = M // p
+    xs = [ints((Mp, K), 600 + s) for s in range(p)]
+    ws = [ints((K, N), 610 + k) for k in range(p)]
+    dys = [ints((M, N), 620 + k) for k in range(p)]
+    dx = outs([(Mp, K)] * p, True)
+    dw = outs([(K, N)] * p, True)
+    tp.tp_ag_matmul_bwd([dev(a) for a in xs], [dev(b) for b in ws], [dev(d) for d in dys], [g.t for g in dx],
+                        [g.t for g in dw], ws_for(tp, tp.TP_OP_AG_MM_BWD, p, M, N, K, chunk), chunk)
+    for g, r in zip(dx, oracle.ag_matmul_bwd_dx(ws, dys)):
+        check_exact(g, r, True)
+    for g, r in zip(dw, oracle.ag_matmul_bwd_dw(xs, dys)):
+        check_exact(g, r, True)
+
+
+@pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
+@pytest.mark.parametrize("p,M,N,K,chunk", SP_BWD_CASES)
+def test_row_bwd_reducescatter_exact(tp, tile_mode, p, M, N, K, chunk):
+    Mp = M // p
+    xs = [ints((M, K), 630 + r) for r in range(p)]
+    ws = [ints((K, N), 640 + r) for r in range(p)]
+    dys = [ints((Mp, N), 650 + s) for s in range(p)]
+    for f32 in (False, True):   # one output dtype per call
+        dx = outs([(M, K)] * p, f32)
+        dw = outs([(K, N)] * p, f32)
+        tp.tp_row_linear_bwd_reducescatter([dev(a) for a in xs], [dev(b) for b in ws], [dev(d) for d in dys],
+                                           [g.t for g in dx], [g.t for g in dw],
+                                           ws_for(tp, tp.TP_OP_ROW_RS_BWD, p, M, N, K, chunk), chunk_m=chunk)
+        for g, r in zip(dx, oracle.row_rs_bwd_dx(ws, dys)):
+            check_exact(g, r, f32)
+        for g, r in zip(dw, oracle.row_rs_bwd_dw(xs, dys)):
+            check_exact(g, r, f32)
+
+
+@pytest.mark.parametrize("p,M,N,K,chunk", [(4, 512, 256, 192, 0), (2, 128, 136, 64, 32)])
+def test_row_bwd_reducescatter_dgelu(tp, p, M, N, K, chunk):
+    Mp = M // p
+    ws = [synth.normal_bf16((K, N), 660 + r, sigma=1.0 / np.sqrt(N)) for r in range(p)]
+    dys = [synth.normal_bf16((Mp, N), 670 + s) for s in range(p)]
+    hs = [synth.normal_bf16((M, K), 680 + r) for r in range(p)]
+    dx = outs([(M, K)] * p, False)
+    tp.tp_row_linear_bwd_reducescatter(None, [dev(b) for b in ws], [dev(d) for d in dys], [g.t for g in dx], None,
+                                       ws_for(tp, tp.TP_OP_ROW_RS_BWD, p, M, N, K, chunk),
+                                       preact=[dev(h) for h in hs], chunk_m=chunk)
+    for g, r in zip(dx, oracle.row_rs_bwd_dx(ws, dys, preacts=hs)):
+        g.check_bands()
+        assert_close(host_f64(g.t), r, False, "SP bwd dgelu")

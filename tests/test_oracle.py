@@ -392,3 +392,62 @@ def test_planted_mistakes_are_caught():
     assert not check_ag(_ag_wrong_order, p, m, k, n, 3)
     bad_gelu = lambda h: 0.5 * h * (1.0 + np.tanh(h))  # noqa: E731 (wrong activation)
     assert abs(bad_gelu(1.0) - 0.8413447460685429) > 1e-3
+
+
+# --------------------------------------------------------------- sequence-parallel backward
+
+def check_ag_bwd(dx_fn, dw_fn, p, m, k, n, seed):
+    """AllGather+MatMul backward against the unsharded layer Y = X A (A = [A_0 | ...]):
+    dX = dY A^T scattered by rows, dA = X^T dY split by columns."""
+    x = _ints((m, k), seed)
+    a = _ints((k, n * p), seed + 1)
+    dy = _ints((m, n * p), seed + 2)
+    xs, ws, dys = _shard_rows(x, p), _shard_cols(a, p), _shard_cols(dy, p)
+    want_dx = _as_int(dy) @ _as_int(a).T
+    want_dw = _as_int(x).T @ _as_int(dy)
+    got_dx = dx_fn(ws, dys)
+    got_dw = dw_fn(xs, dys)
+    return (len(got_dx) == p and np.array_equal(np.vstack(got_dx), want_dx.astype(np.float64)) and
+            np.array_equal(np.hstack(got_dw), want_dw.astype(np.float64)))
+
+
+def check_rs_bwd(dx_fn, dw_fn, p, m, k, n, seed):
+    """MatMul+ReduceScatter backward against the unsharded layer Y = X A
+    (X = [X_0 | ...], A = [A_0; ...]): dY gathered by rows, dX = dY A^T split by
+    columns, dA = X^T dY split by rows."""
+    x = _ints((m, k * p), seed)
+    a = _ints((k * p, n), seed + 1)
+    dy = _ints((m, n), seed + 2)
+    xs, ws, dys = _shard_cols(x, p), _shard_rows(a, p), _shard_rows(dy, p)
+    want_dx = _as_int(dy) @ _as_int(a).T
+    want_dw = _as_int(x).T @ _as_int(dy)
+    return (np.array_equal(np.hstack(dx_fn(ws, dys)), want_dx.astype(np.float64)) and
+            np.array_equal(np.vstack(dw_fn(xs, dys)), want_dw.astype(np.float64)))
+
+
+@pytest.mark.parametrize("p,m,k,n", [(1, 8, 5, 7), (2, 6, 4, 6), (4, 8, 16, 8), (8, 16, 8, 3)])
+def test_sequence_parallel_backward_exact(p, m, k, n):
+    assert check_ag_bwd(oracle.ag_matmul_bwd_dx, oracle.ag_matmul_bwd_dw, p, m, k, n, 2000 + p)
+    assert check_rs_bwd(oracle.row_rs_bwd_dx, oracle.row_rs_bwd_dw, p, m, k, n, 2100 + p)
+
+
+def test_sequence_parallel_backward_duality():
+    """RS of the column-backward dX equals the column backward's row blocks, and
+    the gathered-gradient row backward equals the row backward on the stacked dY."""
+    p, m, k, n = 4, 8, 6, 5
+    ws = [_ints((k, n), 2200 + i) for i in range(p)]
+    dys = [_ints((m, n), 2210 + i) for i in range(p)]
+    assert np.array_equal(np.vstack(oracle.ag_matmul_bwd_dx(ws, dys)), oracle.col_bwd_dx(ws, dys))
+    shards = [_ints((m // p, n), 2220 + i) for i in range(p)]
+    assert all(np.array_equal(a, b) for a, b in
+               zip(oracle.row_rs_bwd_dx(ws, shards), oracle.row_bwd_dx(ws, np.vstack(shards))))
+
+
+def test_sequence_parallel_backward_planted_mistakes():
+    p, m, k, n = 2, 8, 6, 5
+    wrong_order_dx = lambda ws, dys: oracle.ag_matmul_bwd_dx(ws, dys)[::-1]          # noqa: E731
+    assert not check_ag_bwd(wrong_order_dx, oracle.ag_matmul_bwd_dw, p, m, k, n, 5)
+    wrong_gather_dw = lambda xs, dys: oracle.ag_matmul_bwd_dw(xs[::-1], dys)          # noqa: E731
+    assert not check_ag_bwd(oracle.ag_matmul_bwd_dx, wrong_gather_dw, p, m, k, n, 5)
+    wrong_gather_dx = lambda ws, dys: oracle.row_rs_bwd_dx(ws, dys[::-1])             # noqa: E731
+    assert not check_rs_bwd(wrong_gather_dx, oracle.row_rs_bwd_dw, p, m, k, n, 6)
