@@ -499,6 +499,222 @@ def profile_case():
     print("profile case done")
 
 
+# ------------------------------------------------------------------ all workloads / chunk sweep
+
+def _dev_all(torch, tree):
+    import numpy as np
+    conv = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    return {k: ([conv(a) for a in v] if isinstance(v, list) else conv(v)) for k, v in tree.items()}
+
+
+def _ws_for(torch, tp, calls):
+    n = max(tp.tp_workspace_size(*c) for c in calls)
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def workloads(torch, tp):
+    """(name, setup) pairs; setup() -> dict(calls=[(name, fn)], flops=..., bytes=..., bound=...)."""
+    import synth
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+
+    def w1():
+        d = _dev_all(torch, synth.config1_inputs())
+        p, M, K, N = 2, 128, 1024, 2048
+        y = torch.empty((M, N), **bf)
+        ys = [torch.empty((M // p, N), **bf) for _ in range(p)]
+        ws = _ws_for(torch, tp, [(tp.TP_OP_ROW_AR, p, M, N, K, 32), (tp.TP_OP_ROW_RS, p, M, N, K, 32)])
+        return dict(calls=[("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(d["x"], d["w"], [y], ws, 32)),
+                           ("row_fwd_reducescatter",
+                            lambda: tp.tp_row_linear_fwd_reducescatter(d["x"], d["w"], ys, ws, 32))],
+                    flops=2 * 2.0 * M * N * K * p, bytes=2 * (2 * (p * M * K + p * K * N) + 2 * M * N),
+                    bound="hbm", flush=True,
+                    desc="row-parallel p=2, X_r[128,1024], W_r[1024,2048], AllReduce + ReduceScatter, chunk_m=32")
+
+    def w2():
+        d = _dev_all(torch, synth.config2_inputs())
+        p, M, h, nk = 4, 4096, 4096, 4096
+        Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+        Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
+        Y = torch.empty((M, h), **bf)
+        DZ = [torch.empty((M, nk), **bf) for _ in range(p)]
+        DW2 = [torch.empty((nk, h), **bf) for _ in range(p)]
+        DX = torch.empty((M, h), **bf)
+        DW1 = [torch.empty((h, nk), **bf) for _ in range(p)]
+        ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_BWD, p, M, h, nk, 0)])
+        return dict(calls=[
+            ("col_fwd_gelu", lambda: tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
+            ("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(Z, d["w2"], [Y], ws)),
+            ("row_bwd_dx_dgelu", lambda: tp.tp_row_linear_bwd(None, d["w2"], d["dy"], DZ, None, ws, preact=Hh)),
+            ("row_bwd_dw", lambda: tp.tp_row_linear_bwd(Z, d["w2"], d["dy"], None, DW2, ws)),
+            ("col_bwd_dx", lambda: tp.tp_col_linear_bwd(None, d["w1"], DZ, DX, None, ws)),
+            ("col_bwd_dw", lambda: tp.tp_col_linear_bwd(d["x"], d["w1"], DZ, None, DW1, ws))],
+            flops=6 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
+            desc="Megatron MLP block fwd+bwd p=4, 4096 tokens, h=4096, ffn=16384")
+
+    def w3():
+        d = _dev_all(torch, synth.config3_inputs())
+        p, M, h, nq, no = 4, 4096, 4096, 3072, 1024
+        QKV = [torch.empty((M, nq), **bf) for _ in range(p)]
+        Y = torch.empty((M, h), **bf)
+        DO = [torch.empty((M, no), **bf) for _ in range(p)]
+        DWO = [torch.empty((no, h), **bf) for _ in range(p)]
+        DX = torch.empty((M, h), **bf)
+        DWQ = [torch.empty((h, nq), **bf) for _ in range(p)]
+        ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, p, M, nq, h, 0), (tp.TP_OP_ROW_AR, p, M, h, no, 0),
+                                 (tp.TP_OP_ROW_BWD, p, M, h, no, 0), (tp.TP_OP_COL_BWD, p, M, nq, h, 0)])
+        return dict(calls=[
+            ("qkv_col_fwd", lambda: tp.tp_col_linear_fwd(d["x"], d["wqkv"], QKV, ws)),
+            ("wo_row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(d["o"], d["wo"], [Y], ws)),
+            ("wo_row_bwd", lambda: tp.tp_row_linear_bwd(d["o"], d["wo"], d["dy"], DO, DWO, ws)),
+            ("qkv_col_bwd", lambda: tp.tp_col_linear_bwd(d["x"], d["wqkv"], d["dqkv"], DX, DWQ, ws))],
+            flops=3 * (2.0 * M * h * nq * p + 2.0 * M * no * h * p), bytes=None, bound="tensor", flush=False,
+            desc="MHA projections fwd+bwd p=4, 4096 tokens, h=4096, QKV [4096,3072]/shard, W_O [1024,4096]/shard")
+
+    def w4():
+        d = _dev_all(torch, synth.config4_inputs())
+        p, Mp, h, nk = 8, 1024, 8192, 3584
+        M = p * Mp
+        Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+        Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
+        YS = [torch.empty((Mp, h), **bf) for _ in range(p)]
+        ws = _ws_for(torch, tp, [(tp.TP_OP_AG_MM, p, M, nk, h, 0), (tp.TP_OP_ROW_RS, p, M, h, nk, 0)])
+        return dict(calls=[
+            ("ag_matmul_gelu", lambda: tp.tp_ag_matmul(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
+            ("row_fwd_reducescatter", lambda: tp.tp_row_linear_fwd_reducescatter(Z, d["w2"], YS, ws))],
+            flops=2 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
+            desc="sequence-parallel pair fwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672")
+
+    def w4b():
+        d = _dev_all(torch, synth.config4_inputs())
+        p, Mp, h, nk = 8, 1024, 8192, 3584
+        M = p * Mp
+        dys = _dev_all(torch, {"dy": [synth.normal_bf16((Mp, h), synth.seed_for(43, s)) for s in range(p)]})["dy"]
+        Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+        Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
+        YS = [torch.empty((Mp, h), **bf) for _ in range(p)]
+        DZ = [torch.empty((M, nk), **bf) for _ in range(p)]
+        DW2 = [torch.empty((nk, h), **bf) for _ in range(p)]
+        DXS = [torch.empty((Mp, h), **bf) for _ in range(p)]
+        DW1 = [torch.empty((h, nk), **bf) for _ in range(p)]
+        ws = _ws_for(torch, tp, [(tp.TP_OP_AG_MM, p, M, nk, h, 0), (tp.TP_OP_ROW_RS, p, M, h, nk, 0),
+                                 (tp.TP_OP_ROW_RS_BWD, p, M, h, nk, 0), (tp.TP_OP_AG_MM_BWD, p, M, nk, h, 0)])
+        return dict(calls=[
+            ("ag_matmul_gelu", lambda: tp.tp_ag_matmul(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
+            ("row_fwd_reducescatter", lambda: tp.tp_row_linear_fwd_reducescatter(Z, d["w2"], YS, ws)),
+            ("row_bwd_allgather", lambda: tp.tp_row_linear_bwd_reducescatter(Z, d["w2"], dys, DZ, DW2, ws,
+                                                                             preact=Hh)),
+            ("ag_matmul_bwd", lambda: tp.tp_ag_matmul_bwd(d["x"], d["w1"], DZ, DXS, DW1, ws))],
+            flops=6 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
+            desc="sequence-parallel pair fwd+bwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672")
+
+    def w5(M):
+        def setup():
+            d = _dev_all(torch, synth.config5_inputs(M))
+            p, h, nk = 8, 12288, 6144
+            Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+            Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
+            Y = torch.empty((M, h), **bf)
+            ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_AR, p, M, h, nk, 0)])
+            wbytes = 2 * 2.0 * h * nk * p
+            return dict(calls=[
+                ("col_fwd_gelu", lambda: tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
+                ("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(Z, d["w2"], [Y], ws))],
+                flops=2 * 2.0 * M * h * nk * p,
+                bytes=wbytes + 4.0 * M * h + 6.0 * M * nk * p,
+                bound="hbm" if M <= 64 else "tensor", flush=M <= 64,
+                desc=f"GPT-3-scale MLP fwd p=8, h=12288, ffn=49152, M={M}")
+        return setup
+
+    return [("config1", w1), ("config2", w2), ("config3", w3), ("config4", w4), ("config4_fwd_bwd", w4b),
+            ("config5_m2048", w5(2048)), ("config5_m16", w5(16))]
+
+
+def _time_calls(torch, calls, steps, warmup, flush_buf=None):
+    """Median per-step ms of the calls (L2 flushed before each step when asked)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    times, per = [], {n: [] for n, _ in calls}
+    for _ in range(steps):
+        if flush_buf is not None:
+            flush_buf.fill_(1.0)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record(stream)
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        times.append(ev[0].elapsed_time(ev[-1]))
+        for i, (n, _) in enumerate(calls):
+            per[n].append(ev[i].elapsed_time(ev[i + 1]))
+    med = lambda v: sorted(v)[len(v) // 2]
+    return med(times), {n: med(v) for n, v in per.items()}, min(times), sorted(times)[int(0.9 * (len(times) - 1))]
+
+
+def run_configs(args):
+    import torch
+    torch.cuda.set_device(0)
+    import gemm_reduce_fusion_gb300 as tp
+    pk, src = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.float32, device="cuda")   # 1 GiB > 2 x L2
+    for name, setup in workloads(torch, tp):
+        w = setup()
+        ms, per, mn, p90 = _time_calls(torch, w["calls"], max(10, args.steps), max(3, args.warmup),
+                                       flush if w["flush"] else None)
+        tflops = w["flops"] / (ms / 1e3) / 1e12
+        line = {"workload": name, "desc": w["desc"], "ms_per_step": ms, "ms_min": mn, "ms_p90": p90,
+                "tflops": tflops, "frac_of_bf16_sustained": tflops / pk["bf16_tflops_sustained"],
+                "per_call_ms": per, "l2": "flushed before each step" if w["flush"] else "inputs larger than L2",
+                "peak_source": src}
+        if w["bytes"]:
+            gbs = w["bytes"] / (ms / 1e3) / 1e9
+            line.update({"hbm_gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"], "bytes_per_step": w["bytes"]})
+        print(json.dumps(line), flush=True)
+        del w
+        torch.cuda.empty_cache()
+
+
+def run_sweep(args):
+    """chunk_m sweep of the GPT-3-scale FC pair at M = 2048 ([M027] §03-§04):
+    fused time per chunk_m beside the two-engine timeline T = c + (n-1) max(c, m) + m
+    with c = one chunk's per-rank GEMMs and m = its reduce, both measured on
+    the unfused baseline."""
+    import torch
+    torch.cuda.set_device(0)
+    import gemm_reduce_fusion_gb300 as tp
+    import synth
+    M, p, h, nk = 2048, 8, 12288, 6144
+    d = _dev_all(torch, synth.config5_inputs(M))
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+    Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
+    Y = torch.empty((M, h), **bf)
+    chunks = [16, 64, 256, 1024, 2048]
+    ws = _ws_for(torch, tp, [(op, p, M, n, k, c) for c in chunks for op, n, k in
+                             [(tp.TP_OP_COL_FWD, nk, h), (tp.TP_OP_ROW_AR, h, nk), (tp.TP_OP_ROW_AR_UNFUSED, h, nk)]])
+    tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)
+    for c in chunks:
+        n = tp.tp_num_chunks(M, c)
+        fc1, _, _, _ = _time_calls(torch, [("f", lambda: tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU,
+                                                                               preact=Hh, chunk_m=c))], 5, 2)
+        fc2, _, _, _ = _time_calls(torch, [("f", lambda: tp.tp_row_linear_fwd_allreduce(Z, d["w2"], [Y], ws, chunk_m=c))], 5, 2)
+        zc = [z[:min(c, M)] for z in Z]
+        yc = Y[:min(c, M)]
+        cm, _, _, _ = _time_calls(torch, [("c", lambda: tp.tp_row_linear_fwd_unfused(zc, d["w2"], yc, ws, c, phases=1))], 5, 2)
+        mm, _, _, _ = _time_calls(torch, [("m", lambda: tp.tp_row_linear_fwd_unfused(zc, d["w2"], yc, ws, c, phases=2))], 5, 2)
+        full_unfused, _, _, _ = _time_calls(torch, [("u", lambda: tp.tp_row_linear_fwd_unfused(Z, d["w2"], Y, ws, c, phases=3))], 3, 1)
+        flops_fc = 2.0 * M * h * nk * p
+        print(json.dumps({"sweep": "GPT-3-scale FC pair, p=8, M=2048", "chunk_m": c, "n_chunks": n,
+                          "fc1_fused_ms": fc1, "fc2_fused_ms": fc2,
+                          "fc1_tflops": flops_fc / fc1 / 1e9, "fc2_tflops": flops_fc / fc2 / 1e9,
+                          "fc2_c_ms": cm, "fc2_m_ms": mm,
+                          "fc2_model_pipelined_ms": tp.tp_pipeline_time(cm, mm, n),
+                          "fc2_model_serial_ms": n * (cm + mm),
+                          "fc2_unfused_whole_ms": full_unfused}), flush=True)
+
+
 def main():
     args = parse()
     if args.tile_mode and args.impl == "ours":

@@ -72,3 +72,16 @@ def test_reference_arm_rank0_line():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "TFLOP/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_bench_modes_present():
+    """Every bench mode the design notes cite exists and is wired to its flag."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in ("run_ours", "run_reference", "run_configs", "run_sweep", "profile_case", "workloads",
+                 "cpu_baseline", "aggregate_value"):
+        assert callable(getattr(bench, name)), name
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True,
+                         text=True, timeout=120)
+    for flag in ("--configs", "--sweep", "--profile-case", "--tile-mode", "--impl", "--gpus", "--steps", "--warmup"):
+        assert flag in out.stdout, flag
