@@ -49,6 +49,8 @@ TP_OP_ROW_RS_BWD = 8
 TP_DEBUG_TIMEOUT_MS = 0
 TP_DEBUG_DROP_LOAD = 1
 TP_DEBUG_TILE_MODE = 2
+# tp_row_linear_fwd_unfused flags
+TP_UNFUSED_BF16_COLLECTIVE = 1
 
 
 class TPError(RuntimeError):
@@ -69,14 +71,14 @@ def _load() -> ctypes.CDLL:
     L = ctypes.c_int64
     S = ctypes.c_size_t
     sig = {
-        "tp_workspace_size": (S, [I, I, L, L, L, L]),
+        "tp_workspace_size": (S, [I, I, L, L, L, L, I]),
         "tp_row_linear_fwd_allreduce": (I, [PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
         "tp_row_linear_fwd_reducescatter": (I, [PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_col_linear_fwd": (I, [P, PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
         "tp_col_linear_bwd": (I, [P, PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
         "tp_row_linear_bwd": (I, [PP, PP, P, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_ag_matmul": (I, [PP, PP, PP, P, I, PP, I, L, L, L, L, I, P, S, P]),
-        "tp_row_linear_fwd_unfused": (I, [PP, PP, P, I, L, L, L, L, I, I, P, S, P]),
+        "tp_row_linear_fwd_unfused": (I, [PP, PP, P, I, L, L, L, L, I, I, I, P, S, P]),
         "tp_ag_matmul_bwd": (I, [PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_row_linear_bwd_reducescatter": (I, [PP, PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
         "tp_pipeline_time": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, L]),
@@ -156,8 +158,9 @@ def tp_status_string(status: int) -> str:
     return _lib.tp_status_string(int(status)).decode()
 
 
-def tp_workspace_size(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0) -> int:
-    return int(_lib.tp_workspace_size(op, p, M, N, K, chunk_m))
+def tp_workspace_size(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0,
+                      out_dtype: int = TP_BF16) -> int:
+    return int(_lib.tp_workspace_size(op, p, M, N, K, chunk_m, out_dtype))
 
 
 def tp_pipeline_time(c: float, m: float, n_chunks: int) -> float:
@@ -172,10 +175,11 @@ def tp_choose_chunk_m(op: int, p: int, M: int, N: int, K: int) -> int:
     return int(_lib.tp_choose_chunk_m(op, p, M, N, K))
 
 
-def workspace(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0, device="cuda"):
+def workspace(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0, device="cuda",
+              out_dtype: int = TP_BF16):
     """A zero-filled device workspace of tp_workspace_size(...) bytes (torch-allocated)."""
     import torch
-    n = tp_workspace_size(op, p, M, N, K, chunk_m)
+    n = tp_workspace_size(op, p, M, N, K, chunk_m, out_dtype)
     return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
 
 
@@ -284,14 +288,15 @@ def tp_row_linear_bwd_reducescatter(x, w: Sequence, dy: Sequence, dx, dw, ws, pr
 
 
 def tp_row_linear_fwd_unfused(x: Sequence, w: Sequence, y, ws, chunk_m: int = 0, phases: int = 3,
-                              stream=None) -> None:
-    """Unfused baseline: per-rank fp32 partials (phase 1), rank-order reduce into y (phase 2)."""
+                              flags: int = 0, stream=None) -> None:
+    """Unfused baseline: per-rank fp32 partials (phase 1), rank-order reduce into y (phase 2);
+    flags=TP_UNFUSED_BF16_COLLECTIVE sums bf16-rounded partials with a bf16 running sum."""
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_fwd_unfused(_arr(x), _arr(w), _ptr(y), p, M, N, K, chunk_m, _dtype_code(y),
-                                          phases, wp, wb, _stream(stream)), "tp_row_linear_fwd_unfused")
+                                          phases, flags, wp, wb, _stream(stream)), "tp_row_linear_fwd_unfused")
 
 
 def tp_row_linear_fwd_allreduce_noalloc(x: Sequence, w: Sequence, y: Sequence, chunk_m: int = 0,

@@ -786,10 +786,17 @@ struct ReduceParams {
   int32_t A, B;       // output-orientation extents of one group (B contiguous)
   int64_t ld_out, ld_aux;
   int32_t out_f32, epi, n_split, n_rep;
+  int32_t bf16_chain;  // 1: round every partial and every running sum to bf16
 };
 
+__device__ __forceinline__ float bf16_round_f(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 // out[g][a, b] = epilogue( sum_{s=0}^{n_split-1} partial[s][g][a][b] ), the
-// partials summed in split order; 4 consecutive b per thread.
+// partials summed in split order; 4 consecutive b per thread.  With
+// bf16_chain the sum is the one a bf16 collective forms from bf16 partials:
+// acc = bf16(P_0), then acc = bf16(acc + bf16(P_s)) for s = 1, 2, ...
 __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) {
   const int64_t per_group = static_cast<int64_t>(R.A) * R.B;
   const int64_t total4 = static_cast<int64_t>(R.G) * per_group / 4;
@@ -798,12 +805,24 @@ __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) 
        i4 += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t e = i4 * 4;
     float4 acc = *reinterpret_cast<const float4*>(R.partial + e);
-    for (int s = 1; s < R.n_split; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(R.partial + s * split_stride + e);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    if (R.bf16_chain) {
+      acc = make_float4(bf16_round_f(acc.x), bf16_round_f(acc.y), bf16_round_f(acc.z),
+                        bf16_round_f(acc.w));
+      for (int s = 1; s < R.n_split; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(R.partial + s * split_stride + e);
+        acc.x = bf16_round_f(acc.x + bf16_round_f(v.x));
+        acc.y = bf16_round_f(acc.y + bf16_round_f(v.y));
+        acc.z = bf16_round_f(acc.z + bf16_round_f(v.z));
+        acc.w = bf16_round_f(acc.w + bf16_round_f(v.w));
+      }
+    } else {
+      for (int s = 1; s < R.n_split; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(R.partial + s * split_stride + e);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
     }
     const int32_t g = static_cast<int32_t>(e / per_group);
     const int64_t rem = e % per_group;

@@ -27,6 +27,12 @@ constexpr int kPlanSMs = 152;            // SM count the split-K plan assumes (G
 constexpr size_t kStatusBytes = 256;     // workspace head: status word, padded
 constexpr int kStagesWide = 4;           // 128x256 tiles: 48 KiB per stage
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// fp32-output mode: at most this many 64-deep k-blocks (K = 2048) are
+// accumulated in one tensor-core accumulator; longer contractions are split
+// (deterministic split-K) and the fp32 partials summed in split order.  The
+// accumulator's own rounding grows with the number of k-steps it takes, and
+// over K = 16384 it alone passes 1e-5 of max|Y|.
+constexpr int64_t kPreciseKb = 32;
 
 // ------------------------------------------------------------------ small helpers
 
@@ -216,6 +222,7 @@ struct Shape {
   bool swap = false;     // operand-swapped: tokens are the GEMM N axis
   bool pair = false;     // 256x256 tiles on CTA pairs
   bool no_pair = false;  // the launch needs split-K (e.g. the unfused baseline)
+  bool precise = false;  // fp32 outputs: cap the k-blocks per accumulator at kPreciseKb
   int bn = 256;          // tile N (token tile when swapped)
   int Gm = 1, Gn = 1, S = 1;
   int64_t rows_g = 0, cols_g = 0, kseg = 0;
@@ -242,7 +249,8 @@ void finish_shape(Shape* s) {
   // pair tiles still fill the clusters; otherwise 128x256 tiles (with split-K
   // when there are too few of them).
   const int64_t mode = g_debug_tile_mode.load();
-  if (!s->swap && !s->no_pair && mode != 1) {
+  const bool must_split = s->precise && s->kb_total > kPreciseKb;
+  if (!s->swap && !s->no_pair && !must_split && mode != 1) {
     const int64_t pm = cdiv(s->rows_g, 2 * BM);
     const int64_t pu = static_cast<int64_t>(s->Gm) * s->Gn * pm * s->n_tiles;
     if (mode == 2 || (s->rows_g >= 2 * BM && pu >= kPlanSMs / 2)) {
@@ -272,6 +280,10 @@ void finish_shape(Shape* s) {
       s->n_split = static_cast<int>(cdiv(s->kb_total, s->kb_per_split));
     }
   }
+  if (must_split && s->kb_per_split > kPreciseKb) {
+    s->kb_per_split = kPreciseKb;
+    s->n_split = static_cast<int>(cdiv(s->kb_total, kPreciseKb));
+  }
 }
 
 // Chunk used by a call: 0 -> scheduler; clamp to M.
@@ -293,11 +305,14 @@ void apply_chunk(Shape* s, int64_t chunk) {
 }
 
 // Shapes of the launches an op makes, in launch order.
-std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m) {
+std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                             tp_dtype dt) {
   std::vector<Shape> v;
   const int64_t chunk = resolve_chunk(op, p, M, N, K, chunk_m);
   const int64_t Mp = (p > 0) ? M / p : 0;
+  const bool precise = dt == TP_FP32;
   Shape s;
+  s.precise = precise;
   auto tok = [&](int64_t rows_tok, int64_t other, int gtok, int goth) {
     // tokens along GEMM M (standard) or GEMM N (swapped)
     apply_chunk(&s, chunk);
@@ -313,6 +328,7 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
     case TP_OP_ROW_AR_UNFUSED:
       s.S = p; s.kseg = K; tok(M, N, 1, 1);
       s.no_pair = true;
+      s.precise = false;  // one split per rank, as the per-rank GEMMs it stands for
       finish_shape(&s);
       if (s.units0 > 0 && s.kb_total > 0) {  // one split per rank: fp32 partial per rank
         s.n_split = p;
@@ -331,6 +347,7 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
       finish_shape(&s);
       v.push_back(s);
       Shape w;  // dA_k = X^T . dY_k : [K, N] per k, contraction over M
+      w.precise = precise;
       w.S = 1; w.kseg = M; w.rows_g = K; w.cols_g = N; w.Gm = 1; w.Gn = p;
       w.chunk_tiles = cdiv(K, BM);
       finish_shape(&w);
@@ -342,6 +359,7 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
       finish_shape(&s);
       v.push_back(s);
       Shape w;  // dA_k = [X_0; ...; X_{p-1}]^T dY_k: segments walk the p token shards
+      w.precise = precise;
       w.S = p; w.kseg = Mp; w.rows_g = K; w.cols_g = N; w.Gm = 1; w.Gn = p;
       w.chunk_tiles = cdiv(K, BM);
       finish_shape(&w);
@@ -353,6 +371,7 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
       finish_shape(&s);
       v.push_back(s);
       Shape w;  // dA_r = X_r^T [dY_0; ...; dY_{p-1}]
+      w.precise = precise;
       w.S = p; w.kseg = Mp; w.rows_g = K; w.cols_g = N; w.Gm = p; w.Gn = 1;
       w.chunk_tiles = cdiv(K, BM);
       finish_shape(&w);
@@ -364,6 +383,7 @@ std::vector<Shape> op_shapes(tp_op op, int p, int64_t M, int64_t N, int64_t K, i
       finish_shape(&s);
       v.push_back(s);
       Shape w;  // dA_k = X_k^T . dY : [K, N] per k
+      w.precise = precise;
       w.S = 1; w.kseg = M; w.rows_g = K; w.cols_g = N; w.Gm = p; w.Gn = 1;
       w.chunk_tiles = cdiv(K, BM);
       finish_shape(&w);
@@ -388,6 +408,7 @@ struct Launch {
   Shape shape;
   GemmParams P;
   int variant = V_KN;
+  bool bf16_chain = false;  // split-K second stage sums as a bf16 collective would
 };
 
 void init_params(GemmParams* P) { std::memset(P, 0, sizeof(*P)); }
@@ -477,6 +498,7 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     R.epi = P.epi;
     R.n_split = s.n_split;
     R.n_rep = P.n_rep;
+    R.bf16_chain = L.bf16_chain ? 1 : 0;
     const int64_t total4 = static_cast<int64_t>(R.G) * R.A * R.B / 4;
     const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(total4, 256), di.sms * 8)));
     tp_splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(R);
@@ -655,10 +677,11 @@ int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K) {
   return std::min(best, M);
 }
 
-size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m) {
+size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                         tp_dtype out_dtype) {
   if (p < 1 || p > kMaxP || M < 0 || N < 0 || K < 0 || chunk_m < 0) return kStatusBytes;
   if ((op == TP_OP_ROW_RS || op == TP_OP_AG_MM) && M % p != 0) return kStatusBytes;
-  return workspace_for(op_shapes(op, p, M, N, K, chunk_m));
+  return workspace_for(op_shapes(op, p, M, N, K, chunk_m, out_dtype));
 }
 
 tp_status tp_get_device_status(void* ws, cudaStream_t stream) {
@@ -690,7 +713,7 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   TP_TRY(check_ptrs(w, p, work && K > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(y), n_out, work));
   const tp_op op = rs ? TP_OP_ROW_RS : TP_OP_ROW_AR;
-  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m, dt);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   if (!work) return TP_OK;
   const int64_t Mp = M / p;
@@ -772,7 +795,7 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
   TP_TRY(check_ptrs(const_cast<const void* const*>(preact), p, work && want_h));
   TP_TRY(check_ptr(x_gathered, x_gathered != nullptr));
   const tp_op op = ag ? TP_OP_AG_MM : TP_OP_COL_FWD;
-  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m, dt);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   const int64_t Mp = M / p;
   {
@@ -917,7 +940,7 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
   TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
   TP_TRY(check_ptr(x, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
-  std::vector<Shape> shapes = op_shapes(TP_OP_COL_BWD, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(TP_OP_COL_BWD, p, M, N, K, chunk_m, out_dtype);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -979,7 +1002,7 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
-  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_BWD, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_BWD, p, M, N, K, chunk_m, out_dtype);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1053,7 +1076,7 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
   TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
-  std::vector<Shape> shapes = op_shapes(TP_OP_AG_MM_BWD, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(TP_OP_AG_MM_BWD, p, M, N, K, chunk_m, out_dtype);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1145,7 +1168,7 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
-  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_RS_BWD, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_RS_BWD, p, M, N, K, chunk_m, out_dtype);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1237,14 +1260,16 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
 extern "C" tp_status tp_row_linear_fwd_unfused(const void* const* x, const void* const* w, void* y,
                                                int p, int64_t M, int64_t N, int64_t K,
                                                int64_t chunk_m, tp_dtype out_dtype, int phases,
-                                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+                                               int flags, void* ws, size_t ws_bytes,
+                                               cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
   if (phases < 1 || phases > 3) return TP_ERR_INVALID_ARG;
+  if ((flags & ~TP_UNFUSED_BF16_COLLECTIVE) != 0) return TP_ERR_INVALID_ARG;
   const bool work = M > 0 && N > 0;
   TP_TRY(check_ptrs(x, p, work && K > 0));
   TP_TRY(check_ptrs(w, p, work && K > 0));
   TP_TRY(check_ptr(y, work));
-  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk_m);
+  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk_m, out_dtype);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   if (!work) return TP_OK;
   {
@@ -1283,6 +1308,7 @@ extern "C" tp_status tp_row_linear_fwd_unfused(const void* const* x, const void*
   P.epi = EPI_NONE;
   P.out[0] = y;
   L.variant = s.swap ? sw_variant_mk(s.bn) : V_KN;
+  L.bf16_chain = (flags & TP_UNFUSED_BF16_COLLECTIVE) != 0;
   return run_launch_phases(L, out_dtype, ws, stream, di, phases);
 }
 
@@ -1325,7 +1351,7 @@ extern "C" tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, c
                                                          int64_t chunk_m, tp_dtype out_dtype,
                                                          cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
-  if (workspace_for(op_shapes(TP_OP_ROW_AR, p, M, N, K, chunk_m)) > TP_NOALLOC_SCRATCH_BYTES)
+  if (workspace_for(op_shapes(TP_OP_ROW_AR, p, M, N, K, chunk_m, out_dtype)) > TP_NOALLOC_SCRATCH_BYTES)
     return TP_ERR_WORKSPACE_TOO_SMALL;
   if (M == 0 || N == 0) return TP_OK;
   void* scratch = nullptr;

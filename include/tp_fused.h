@@ -88,9 +88,15 @@ typedef enum {
   TP_OP_ROW_RS_BWD = 8      /* tp_row_linear_bwd_reducescatter */
 } tp_op;
 
-/* Bytes of device workspace the call (op, p, M, N, K, chunk_m) needs, with
- * M, N, K meant as in that call.  Always >= 256 (the status word). */
-size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m);
+/* Bytes of device workspace the call (op, p, M, N, K, chunk_m, out_dtype)
+ * needs, with M, N, K meant as in that call.  Always >= 256 (the status
+ * word).  out_dtype matters: with TP_FP32 outputs no tensor-core
+ * accumulator takes more than 2048 of the contraction (all ranks' K laid
+ * end to end), so a longer contraction is split and its fp32 partials,
+ * ceil(sum K / 2048) copies of the outputs, live in the workspace.  This
+ * keeps fp32 outputs within 1e-5 of max|Y| of the exact sum at any K. */
+size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                         tp_dtype out_dtype);
 
 /* Row-parallel forward, MatMul+AllReduce layout.  [M027 §01; TP §2.4, §四]
  *   Y = sum_{r=0}^{p-1} X_r . W_r, accumulated in rank order, written once.
@@ -190,19 +196,29 @@ tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const void* cons
                                           int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
                                           size_t ws_bytes, cudaStream_t stream);
 
-/* Unfused baseline of the row-parallel MatMul+AllReduce, for measurement.
- * [M027 §04: time the MatMul and the collective separately]
+/* Unfused baseline of the row-parallel MatMul+AllReduce, for measurement
+ * and for the output-error comparison against it.
+ * [M027 §04: time the MatMul and the collective separately, compare the
+ *  whole layer's output error; §06: record the separate baseline and the
+ *  output error]
  *   phase bit 0: every rank's partial P_r = X_r . W_r into its own fp32
  *                buffer in the workspace (one launch over all ranks);
  *   phase bit 1: Y = P_0 + P_1 + ... + P_{p-1} in rank order, cast, -> y.
  *   phases = 3 runs both.  Arguments as in tp_row_linear_fwd_allreduce with
  *   n_out = 1; the workspace holds p fp32 copies of Y
  *   (tp_workspace_size(TP_OP_ROW_AR_UNFUSED, ...)).  Phase 1 without a
- *   later phase 2 leaves y untouched.                                    */
+ *   later phase 2 leaves y untouched.
+ *   flags: 0, or TP_UNFUSED_BF16_COLLECTIVE to make phase 2 sum the way an
+ *   unfused AllReduce of bf16 tensors does: each rank's partial is first
+ *   rounded to bf16 (the tensor it would hand to the collective), and the
+ *   running sum is rounded to bf16 after every addition, in rank order:
+ *   acc = bf16(P_0); acc = bf16(acc + bf16(P_r)) for r = 1..p-1.  Any
+ *   other bit is TP_ERR_INVALID_ARG.                                     */
+#define TP_UNFUSED_BF16_COLLECTIVE 1
 tp_status tp_row_linear_fwd_unfused(const void* const* x, const void* const* w, void* y, int p,
                                     int64_t M, int64_t N, int64_t K, int64_t chunk_m,
-                                    tp_dtype out_dtype, int phases, void* ws, size_t ws_bytes,
-                                    cudaStream_t stream);
+                                    tp_dtype out_dtype, int phases, int flags, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream);
 
 /* Two-engine chunk timeline: c + (n-1) * max(c, m) + m for n >= 1, 0 for
  * n <= 0; c = per-chunk compute time, m = per-chunk reduce time.  [M027 §03] */
@@ -236,7 +252,8 @@ tp_status tp_get_device_status(void* ws, cudaStream_t stream);
  * TP_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library holds
  * until the process exits.
  *
- *  - A call whose scratch need (tp_workspace_size(TP_OP_ROW_AR, ...))
+ *  - A call whose scratch need (tp_workspace_size(TP_OP_ROW_AR, ...,
+ *    out_dtype))
  *    exceeds TP_NOALLOC_SCRATCH_BYTES is rejected with
  *    TP_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *  - The first call on each device looks up the array's device address

@@ -101,6 +101,26 @@ def row_fwd_allreduce(xs, ws) -> np.ndarray:
     return y
 
 
+def row_fwd_allreduce_bf16_collective(xs, ws) -> np.ndarray:
+    """The row-parallel output an unfused bf16 AllReduce would produce.
+
+    Each rank's partial P_r = X_r . W_r is handed to the collective as a
+    bfloat16 tensor, and the collective adds those tensors in rank order
+    r = 0, 1, ..., p-1, storing its running sum as bfloat16 after every
+    addition:  acc = bf16(P_0);  acc = bf16(acc + bf16(P_r)).
+    This is the separate baseline whose whole-layer output error the fused
+    path (one rounding, after all p partials) is compared with.
+    [M027 §04: compare the whole layer's output error against the baseline;
+    §06: record the separate baseline and the output error.  The rounding
+    points are the reading of "an AllReduce of bf16 partials" in rank order.]
+    """
+    parts = row_partials(xs, ws)
+    acc = widen(round_bf16(parts[0]))
+    for p_r in parts[1:]:
+        acc = widen(round_bf16(acc + widen(round_bf16(p_r))))
+    return acc
+
+
 def row_fwd_reducescatter(xs, ws) -> list[np.ndarray]:
     """MatMul+ReduceScatter: rank j holds rows [j*M/p, (j+1)*M/p) of Y.
 

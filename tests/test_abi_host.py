@@ -82,6 +82,21 @@ def test_workspace_size(tp):
     assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 0, 16, 16, 16, 0) == 256
 
 
+def test_fp32_workspace_holds_the_precise_splits(tp):
+    """fp32 outputs: no accumulator takes more than 2048 of the contraction.
+    p = 4 ranks of K = 4096 (16384 in all) need 8 fp32 copies of Y; a
+    contraction of 2048 or less needs none."""
+    bf = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0, tp.TP_BF16)
+    f32 = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0, tp.TP_FP32)
+    assert bf == 256
+    assert f32 == 256 + 8 * 4096 * 4096 * 4
+    assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 512, 0, tp.TP_FP32) == 256
+    # column backward with enough tiles to need no split for occupancy: dX
+    # contracts over p * N = 8192 (4 splits), dW over M = 4096 (2 splits)
+    cb = tp.tp_workspace_size(tp.TP_OP_COL_BWD, 4, 4096, 2048, 2048, 0, tp.TP_FP32)
+    assert cb == 256 + max(4 * 4096 * 2048 * 4, 2 * 4 * 2048 * 2048 * 4)
+
+
 # ---------------------------------------------------------------- host argument checks
 
 A = 1 << 20          # fake, 16-byte aligned "device" addresses: never dereferenced

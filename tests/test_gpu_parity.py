@@ -66,7 +66,10 @@ def check_exact(g, ref, f32):
 
 
 def ws_for(tp, op, p, M, N, K, chunk):
-    return tp.workspace(op, p, M, N, K, chunk)
+    """A workspace that serves the call with bf16 or fp32 outputs."""
+    import torch
+    n = max(tp.tp_workspace_size(op, p, M, N, K, chunk, dt) for dt in (tp.TP_BF16, tp.TP_FP32))
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
 ROW_CASES = [  # p, M, N, K, chunk_m
@@ -369,6 +372,114 @@ def test_unfused_baseline_exact(tp, p, M, N, K, chunk):
         else:
             tp.tp_row_linear_fwd_unfused(dx, dw, y[0].t, wsp, chunk, phases=3)
         check_exact(y[0], ref, True)
+
+
+# ------------------------------------------------------------------ bf16-collective emulation
+
+@pytest.mark.parametrize("p,M,N,K,chunk", [(2, 300, 520, 200, 0), (4, 130, 136, 72, 32), (8, 64, 264, 64, 16)])
+def test_unfused_bf16_collective_exact(tp, p, M, N, K, chunk):
+    """Integer inputs: every fp32 partial is an exact integer, many above 256
+    where bf16 has to round, so each rounding of the emulated bf16 collective
+    is decided the same way on both sides and the GPU equals the oracle bit
+    for bit, with bf16 and with fp32 output buffers."""
+    xs = [ints((M, K), 195 + r) for r in range(p)]
+    ws = [ints((K, N), 295 + r) for r in range(p)]
+    ref = oracle.row_fwd_allreduce_bf16_collective(xs, ws)
+    assert not np.array_equal(ref, oracle.row_fwd_allreduce(xs, ws))  # rounding is exercised
+    dx, dw = [dev(a) for a in xs], [dev(b) for b in ws]
+    for f32 in (False, True):
+        y = outs([(M, N)], f32)
+        wsp = ws_for(tp, tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk)
+        tp.tp_row_linear_fwd_unfused(dx, dw, y[0].t, wsp, chunk, flags=tp.TP_UNFUSED_BF16_COLLECTIVE)
+        check_exact(y[0], ref, f32)
+
+
+def test_unfused_bf16_collective_normal_inputs(tp):
+    """Normal inputs at p = 8: the emulation matches the oracle's bf16
+    collective within the bf16 tolerance, and its error against the exact
+    sum is at least that of the fused path (which rounds once)."""
+    import torch
+    from gpu_util import rel_err
+    p, M, N, K = 8, 256, 512, 1024
+    xs = [synth.normal_bf16((M, K), synth.seed_for(50, r)) for r in range(p)]
+    ws = [synth.normal_bf16((K, N), synth.seed_for(50, 8 + r), 0.02) for r in range(p)]
+    dx, dw = [dev(a) for a in xs], [dev(b) for b in ws]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tp.tp_row_linear_fwd_unfused(dx, dw, y, ws_for(tp, tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, 0), 0,
+                                 flags=tp.TP_UNFUSED_BF16_COLLECTIVE)
+    got = host_f64(y)
+    assert_close(got, oracle.row_fwd_allreduce_bf16_collective(xs, ws), False, "bf16 collective")
+    fused = torch.empty_like(y)
+    tp.tp_row_linear_fwd_allreduce(dx, dw, [fused], ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0))
+    exact = oracle.row_fwd_allreduce(xs, ws)
+    assert rel_err(got, exact) >= rel_err(host_f64(fused), exact)
+
+
+def test_unfused_rejects_unknown_flags(tp):
+    import torch
+    p, M, N, K = 2, 16, 8, 8
+    x = [torch.zeros((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    w = [torch.zeros((K, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_row_linear_fwd_unfused(x, w, y, ws_for(tp, tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, 0), flags=2)
+    assert e.value.status == tp.TP_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ fp32 outputs at long contractions
+
+def test_fp32_mode_within_1e5_at_large_k(tp):
+    """p = 4 ranks of K = 4096 (16384 in all): fp32 outputs stay within 1e-5
+    of max|Y| of the exact sum, for the AllReduce (both chunk paths) and the
+    ReduceScatter."""
+    import torch
+    p, M, N, K = 4, 256, 512, 4096
+    xs = [synth.normal_bf16((M, K), synth.seed_for(51, r)) for r in range(p)]
+    ws = [synth.normal_bf16((K, N), synth.seed_for(51, 8 + r)) for r in range(p)]
+    dx, dw = [dev(a) for a in xs], [dev(b) for b in ws]
+    ref = oracle.row_fwd_allreduce(xs, ws)
+    for chunk in (0, 32):
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        wsp = tp.workspace(tp.TP_OP_ROW_AR, p, M, N, K, chunk, out_dtype=tp.TP_FP32)
+        tp.tp_row_linear_fwd_allreduce(dx, dw, [y], wsp, chunk)
+        assert_close(host_f64(y), ref, True, f"AllReduce chunk {chunk}")
+    ys = [torch.empty((M // p, N), dtype=torch.float32, device="cuda") for _ in range(p)]
+    tp.tp_row_linear_fwd_reducescatter(dx, dw, ys, tp.workspace(tp.TP_OP_ROW_RS, p, M, N, K, 0,
+                                                                out_dtype=tp.TP_FP32))
+    for j in range(p):
+        assert_close(host_f64(ys[j]), ref[j * (M // p):(j + 1) * (M // p)], True, f"ReduceScatter {j}")
+
+
+def test_fp32_mode_column_long_contractions(tp):
+    """Column forward with GeLU over K = 16384, and the column backward whose
+    dX contracts over p * N = 8192 and whose dW contracts over M = 8192."""
+    import torch
+    p, M, N, K = 2, 256, 256, 16384
+    x = synth.normal_bf16((M, K), synth.seed_for(52, 0))
+    ws = [synth.normal_bf16((K, N), synth.seed_for(52, 1 + k), 0.02) for k in range(p)]
+    y = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(p)]
+    h = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(p)]
+    tp.tp_col_linear_fwd(dev(x), [dev(b) for b in ws], y,
+                         tp.workspace(tp.TP_OP_COL_FWD, p, M, N, K, 0, out_dtype=tp.TP_FP32),
+                         epi=tp.TP_EPI_GELU, preact=h)
+    zr, hr = oracle.col_fwd(x, ws, apply_gelu=True)
+    for k in range(p):
+        assert_close(host_f64(h[k]), hr[k], True, f"H {k}")
+        assert_close(host_f64(y[k]), zr[k], True, f"GeLU(H) {k}")
+    p, M, N, K = 2, 8192, 4096, 256
+    xb = synth.normal_bf16((M, K), synth.seed_for(53, 0))
+    wb = [synth.normal_bf16((K, N), synth.seed_for(53, 1 + k), 0.02) for k in range(p)]
+    dyb = [synth.normal_bf16((M, N), synth.seed_for(53, 4 + k)) for k in range(p)]
+    dxo = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    dwo = [torch.empty((K, N), dtype=torch.float32, device="cuda") for _ in range(p)]
+    tp.tp_col_linear_bwd(dev(xb), [dev(b) for b in wb], [dev(d) for d in dyb], dxo, dwo,
+                         tp.workspace(tp.TP_OP_COL_BWD, p, M, N, K, 0, out_dtype=tp.TP_FP32))
+    rows = np.arange(0, M, 61)
+    assert_close(host_f64(dxo)[rows], oracle.col_bwd_dx(wb, [d[rows] for d in dyb]), True, "dX")
+    cols = np.arange(0, N, 37)
+    dwr = oracle.col_bwd_dw(xb, [d[:, cols] for d in dyb])
+    for k in range(p):
+        assert_close(host_f64(dwo[k])[:, cols], dwr[k], True, f"dW {k}")
 
 
 # ------------------------------------------------------------------ both tile paths

@@ -451,3 +451,86 @@ def test_sequence_parallel_backward_planted_mistakes():
     assert not check_ag_bwd(oracle.ag_matmul_bwd_dx, wrong_gather_dw, p, m, k, n, 5)
     wrong_gather_dx = lambda ws, dys: oracle.row_rs_bwd_dx(ws, dys[::-1])             # noqa: E731
     assert not check_rs_bwd(wrong_gather_dx, oracle.row_rs_bwd_dw, p, m, k, n, 6)
+
+
+# --------------------------------------------------------------- bf16-collective emulation
+
+def _scalar_ranks(vals):
+    """Rank r contributes the 1x1 partial vals[r] (X_r = [[v]], W_r = [[1]])."""
+    one = synth.f32_to_bf16_bits(np.array([[1.0]], np.float32))
+    xs = [synth.f32_to_bf16_bits(np.array([[v]], np.float32)) for v in vals]
+    return xs, [one] * len(vals)
+
+
+def test_bf16_collective_hand_values():
+    """bf16 keeps 8 significant bits: between 256 and 512 its step is 2, and a
+    tie goes to the even significand (256, not 258)."""
+    coll = oracle.row_fwd_allreduce_bf16_collective
+    # running sum rounded: 256 + 1 = 257 -> 256 (exact sum 257)
+    assert coll(*_scalar_ranks([256.0, 1.0]))[0, 0] == 256.0
+    assert oracle.row_fwd_allreduce(*_scalar_ranks([256.0, 1.0]))[0, 0] == 257.0
+    assert coll(*_scalar_ranks([255.0, 2.0]))[0, 0] == 256.0
+    # rank order: (1 + 1) + 256 = 258 exactly, (256 + 1) + 1 = 256
+    assert coll(*_scalar_ranks([1.0, 1.0, 256.0]))[0, 0] == 258.0
+    assert coll(*_scalar_ranks([256.0, 1.0, 1.0]))[0, 0] == 256.0
+    # each partial is rounded before it enters the sum: p = 1, P_0 = 256 + 1
+    x = synth.f32_to_bf16_bits(np.array([[1.0, 1.0]], np.float32))
+    w = synth.f32_to_bf16_bits(np.array([[256.0], [1.0]], np.float32))
+    assert coll([x], [w])[0, 0] == 256.0
+    assert oracle.row_fwd_allreduce([x], [w])[0, 0] == 257.0
+
+
+def test_bf16_collective_small_integers_are_exact():
+    """Partials and running sums within [-256, 256] are bf16 integers: no
+    rounding happens and the emulation equals the exact sum."""
+    p = 4
+    xs = [_ints((6, 4), 3000 + r, 2) for r in range(p)]
+    ws = [_ints((4, 5), 3010 + r, 2) for r in range(p)]
+    assert np.array_equal(oracle.row_fwd_allreduce_bf16_collective(xs, ws), oracle.row_fwd_allreduce(xs, ws))
+
+
+def test_bf16_collective_error_bound_and_representable():
+    """Every output is a bf16 value, and it differs from the exact sum by at
+    most the p partial roundings plus the p - 1 sum roundings, each at most
+    half a bf16 step (2^-8 relative) of the value it rounds."""
+    p, m, k, n = 8, 16, 64, 12
+    xs = [synth.normal_bf16((m, k), synth.seed_for(60, r)) for r in range(p)]
+    ws = [synth.normal_bf16((k, n), synth.seed_for(60, 8 + r)) for r in range(p)]
+    got = oracle.row_fwd_allreduce_bf16_collective(xs, ws)
+    assert np.array_equal(oracle.widen(oracle.round_bf16(got)), got)
+    parts = oracle.row_partials(xs, ws)
+    exact = oracle.row_fwd_allreduce(xs, ws)
+    u = 2.0 ** -8
+    bound = sum(np.abs(pr) for pr in parts) * u * (1 + u) ** (2 * p)
+    for r in range(1, p):
+        bound = bound + np.abs(sum(parts[:r + 1])) * u * (1 + u) ** (2 * p)
+    bound = bound + sum(np.abs(pr) for pr in parts) * (2 * p * u) ** 2 * 4
+    assert np.all(np.abs(got - exact) <= bound)
+    assert not np.array_equal(got, exact)
+
+
+def test_bf16_collective_planted_mistakes():
+    """Dropping the partial rounding, the running-sum rounding or the rank
+    order each changes a hand value above."""
+    def no_partial_rounding(xs, ws):
+        parts = oracle.row_partials(xs, ws)
+        acc = parts[0]
+        for pr in parts[1:]:
+            acc = oracle.widen(oracle.round_bf16(acc + pr))
+        return oracle.widen(oracle.round_bf16(acc))
+
+    def no_sum_rounding(xs, ws):
+        parts = oracle.row_partials(xs, ws)
+        return sum(oracle.widen(oracle.round_bf16(pr)) for pr in parts)
+
+    def reversed_order(xs, ws):
+        return oracle.row_fwd_allreduce_bf16_collective(xs[::-1], ws[::-1])
+
+    x = synth.f32_to_bf16_bits(np.array([[1.0, 1.0]], np.float32))
+    w = synth.f32_to_bf16_bits(np.array([[256.0], [1.0]], np.float32))
+    # P_0 = 257 and P_1 = 1: rounded first, 256 + 1 -> 256; unrounded, 258
+    one = synth.f32_to_bf16_bits(np.array([[1.0]], np.float32))
+    assert oracle.row_fwd_allreduce_bf16_collective([x, one], [w, one])[0, 0] == 256.0
+    assert no_partial_rounding([x, one], [w, one])[0, 0] == 258.0
+    assert no_sum_rounding(*_scalar_ranks([256.0, 1.0]))[0, 0] == 257.0
+    assert reversed_order(*_scalar_ranks([256.0, 1.0, 1.0]))[0, 0] == 258.0
