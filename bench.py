@@ -66,6 +66,8 @@ def parse():
                     help="0: planner chooses 128x256 or CTA-pair 256x256 tiles; 1: 128x256 only; 2: pairs")
     ap.add_argument("--profile-case", action="store_true",
                     help="run each GEMM variant of the step twice at the step's shapes (for ncu)")
+    ap.add_argument("--precision-report", action="store_true",
+                    help="output error of the fused path vs the unfused baseline with fp32 or bf16 collectives")
     return ap.parse_args()
 
 
@@ -715,6 +717,121 @@ def run_sweep(args):
                           "fc2_unfused_whole_ms": full_unfused}), flush=True)
 
 
+def _err_stats(torch, got, ref):
+    """Error of a bf16 result against an fp32 reference: max|d|/max|ref|,
+    rms(d)/rms(ref), and the share of elements that differ from bf16(ref)."""
+    g = got.float()
+    d = (g - ref).abs()
+    return {"max_rel": float(d.max() / ref.abs().max()),
+            "rms_rel": float(d.pow(2).mean().sqrt() / ref.pow(2).mean().sqrt()),
+            "frac_not_rounded_ref": float((got != ref.to(torch.bfloat16)).float().mean())}
+
+
+def run_precision_report(args):
+    """Whole-layer output (and gradient) error of the fused path against the
+    separate baseline ([M027] §04: compare the layer's output error, and for
+    training its backward and parameter gradients; §06: record the output and
+    gradient error and the workspace peak).  For each row-parallel layer of
+    the workloads, bf16 outputs of
+      fused        -- all p partials in one fp32 accumulator, rounded once;
+      unfused_fp32 -- per-rank fp32 partials, then an fp32 rank-order sum;
+      unfused_bf16 -- per-rank partials rounded to bf16, summed as a bf16
+                      collective would (bf16 running sum, rank order);
+    are compared with the library's own fp32-output result, which the parity
+    tests hold within 1e-5 of max|Y| of the exact fp64 sum (far below the
+    bf16 errors measured here).  Every element of the layer is compared."""
+    import torch
+    torch.cuda.set_device(0)
+    import gemm_reduce_fusion_gb300 as tp
+    import synth
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+
+    def ws(calls):
+        return _ws_for(torch, tp, calls)
+
+    def row_layer(name, xs, wsh, extra=None):
+        p = len(xs)
+        M, K = xs[0].shape
+        N = wsh[0].shape[1]
+        calls = [(tp.TP_OP_ROW_AR, p, M, N, K, 0, tp.TP_FP32), (tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, 0)]
+        w_ = ws(calls)
+        ref = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        tp.tp_row_linear_fwd_allreduce(xs, wsh, [ref], w_)
+        out = {}
+        y = torch.empty((M, N), **bf)
+        tp.tp_row_linear_fwd_allreduce(xs, wsh, [y], w_)
+        out["fused"] = _err_stats(torch, y, ref)
+        tp.tp_row_linear_fwd_unfused(xs, wsh, y, w_)
+        out["unfused_fp32"] = _err_stats(torch, y, ref)
+        tp.tp_row_linear_fwd_unfused(xs, wsh, y, w_, flags=tp.TP_UNFUSED_BF16_COLLECTIVE)
+        out["unfused_bf16"] = _err_stats(torch, y, ref)
+        line = {"precision_report": name, "p": p, "M": M, "N": N, "K_per_rank": K, "errors_vs_fp32": out,
+                "workspace_bytes": {"fused_bf16_out": tp.tp_workspace_size(tp.TP_OP_ROW_AR, p, M, N, K, 0),
+                                    "unfused": tp.tp_workspace_size(tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, 0)}}
+        if extra:
+            line.update(extra)
+        print(json.dumps(line), flush=True)
+        del ref, y, w_
+        torch.cuda.empty_cache()
+
+    # worked example: p = 2
+    d = _dev_all(torch, synth.config1_inputs())
+    row_layer("row-parallel worked example (p=2, X_r[128,1024], W_r[1024,2048])", d["x"], d["w"])
+    # MLP block: FC2 forward on the GPU's own GeLU output, then the backward's gradients
+    d = _dev_all(torch, synth.config2_inputs())
+    p, M, h, nk = 4, 4096, 4096, 4096
+    Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+    Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
+    w0 = ws([(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_BWD, p, M, h, nk, 0, tp.TP_FP32),
+             (tp.TP_OP_COL_BWD, p, M, nk, h, 0, tp.TP_FP32)])
+    tp.tp_col_linear_fwd(d["x"], d["w1"], Z, w0, epi=tp.TP_EPI_GELU, preact=Hh)
+    row_layer("MLP FC2 forward (p=4, 4096 tokens, h=4096, ffn=16384)", Z, d["w2"])
+    # gradients: bf16 results of the fused backward vs its fp32-output results
+    grads = {}
+    DZ = [torch.empty((M, nk), **bf) for _ in range(p)]
+    DZf = [torch.empty((M, nk), dtype=torch.float32, device="cuda") for _ in range(p)]
+    tp.tp_row_linear_bwd(None, d["w2"], d["dy"], DZ, None, w0, preact=Hh)
+    tp.tp_row_linear_bwd(None, d["w2"], d["dy"], DZf, None, w0, preact=Hh)
+    grads["dZ_k (FC2 dX * GeLU')"] = _err_stats(torch, torch.cat(DZ, 1), torch.cat(DZf, 1))
+    del DZf
+    DW2 = [torch.empty((nk, h), **bf) for _ in range(p)]
+    DW2f = [torch.empty((nk, h), dtype=torch.float32, device="cuda") for _ in range(p)]
+    tp.tp_row_linear_bwd(Z, d["w2"], d["dy"], None, DW2, w0)
+    tp.tp_row_linear_bwd(Z, d["w2"], d["dy"], None, DW2f, w0)
+    grads["dW2_k"] = _err_stats(torch, torch.cat(DW2, 1), torch.cat(DW2f, 1))
+    del DW2, DW2f
+    DX = torch.empty((M, h), **bf)
+    DXf = torch.empty((M, h), dtype=torch.float32, device="cuda")
+    tp.tp_col_linear_bwd(None, d["w1"], DZ, DX, None, w0)
+    tp.tp_col_linear_bwd(None, d["w1"], DZ, DXf, None, w0)
+    grads["dX (fused reduce over k)"] = _err_stats(torch, DX, DXf)
+    DW1 = [torch.empty((h, nk), **bf) for _ in range(p)]
+    DW1f = [torch.empty((h, nk), dtype=torch.float32, device="cuda") for _ in range(p)]
+    tp.tp_col_linear_bwd(d["x"], d["w1"], DZ, None, DW1, w0)
+    tp.tp_col_linear_bwd(d["x"], d["w1"], DZ, None, DW1f, w0)
+    grads["dW1_k"] = _err_stats(torch, torch.cat(DW1, 1), torch.cat(DW1f, 1))
+    del DW1, DW1f, DXf, w0
+    print(json.dumps({"precision_report": "MLP backward gradients, bf16 vs the fp32-output result",
+                      "errors_vs_fp32": grads}), flush=True)
+    # FC1's dX reduce as an unfused collective would do it: X_k = dZ_k, W_k = W1_k^T
+    w1t = [w.t().contiguous() for w in d["w1"]]
+    row_layer("MLP FC1 backward dX = sum_k dZ_k W1_k^T (p=4)", DZ, w1t)
+    del w1t, DZ, Z, Hh, d
+    torch.cuda.empty_cache()
+    # MHA output projection
+    d = _dev_all(torch, synth.config3_inputs())
+    row_layer("MHA W_O forward (p=4, 4096 tokens, K_r=1024, h=4096)", d["o"], d["wo"])
+    del d
+    torch.cuda.empty_cache()
+    # GPT-3-scale FC2, p = 8
+    d = _dev_all(torch, synth.config5_inputs(2048))
+    p, M, h, nk = 8, 2048, 12288, 6144
+    Z = [torch.empty((M, nk), **bf) for _ in range(p)]
+    w0 = ws([(tp.TP_OP_COL_FWD, p, M, nk, h, 0)])
+    tp.tp_col_linear_fwd(d["x"], d["w1"], Z, w0, epi=tp.TP_EPI_GELU)
+    row_layer("GPT-3-scale FC2 forward (p=8, M=2048, K_r=6144, N=12288)", Z, d["w2"])
+
+
 def main():
     args = parse()
     if args.tile_mode and args.impl == "ours":
@@ -731,6 +848,9 @@ def main():
         return
     if args.configs:
         run_configs(args)
+        return
+    if args.precision_report:
+        run_precision_report(args)
         return
     run_ours(args)
 

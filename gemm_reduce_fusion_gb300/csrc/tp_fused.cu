@@ -79,9 +79,22 @@ struct DevInfo {
   bool ok = false;
 };
 
+// The calling thread's current device, with that device's primary context
+// made current on the thread.  A thread that has not yet made a CUDA call of
+// its own (an autograd worker thread, a user's thread) may have no current
+// context, and tensor-map encoding and launches from it then fail;
+// cudaSetDevice binds the primary context.
+tp_status bind_device(int* dev) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return TP_ERR_CUDA;
+  if (cudaSetDevice(d) != cudaSuccess) return TP_ERR_CUDA;
+  *dev = d;
+  return TP_OK;
+}
+
 tp_status device_info(DevInfo* out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (bind_device(&dev) != TP_OK) return TP_ERR_CUDA;
   int major = 0, minor = 0, sms = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -686,6 +699,8 @@ size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64
 
 tp_status tp_get_device_status(void* ws, cudaStream_t stream) {
   if (ws == nullptr) return TP_ERR_INVALID_ARG;
+  int dev = 0;
+  if (bind_device(&dev) != TP_OK) return TP_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return TP_ERR_CUDA;
   uint32_t word = 0;
   if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TP_ERR_CUDA;
@@ -1331,7 +1346,7 @@ tp_status noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (bind_device(&dev) != TP_OK) return TP_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return TP_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   if (addr[dev] == nullptr) {

@@ -312,6 +312,43 @@ def test_deterministic_and_chunk_invariant(tp):
         assert_close(host_f64(y), ref, False, f"chunk {c}")
 
 
+# ------------------------------------------------------------------ calls from other threads
+
+def test_call_from_a_fresh_thread(tp):
+    """A thread that made no CUDA call before (as autograd's worker threads)
+    gets the same results as the main thread."""
+    import threading
+    import torch
+    p, M, N, K = 2, 300, 264, 136
+    x = ints((M, K), 560)
+    ws = [ints((K, N), 561 + k) for k in range(p)]
+    dys = [ints((M, N), 563 + k) for k in range(p)]
+    X, W, DY = dev(x), [dev(a) for a in ws], [dev(a) for a in dys]
+    wsp = ws_for(tp, tp.TP_OP_COL_BWD, p, M, N, K, 0)
+    res = {}
+
+    def run():
+        try:
+            dx = outs([(M, K)], True)
+            dw = outs([(K, N)] * p, True)
+            tp.tp_col_linear_bwd(X, W, DY, dx[0].t, [g.t for g in dw], wsp)
+            torch.cuda.synchronize()
+            res["out"] = (dx, dw)
+        except Exception as e:  # re-raised on the main thread
+            res["err"] = e
+
+    t = threading.Thread(target=run)
+    t.start()
+    t.join()
+    if "err" in res:
+        raise res["err"]
+    dx, dw = res["out"]
+    check_exact(dx[0], oracle.col_bwd_dx(ws, dys), True)
+    for g, r in zip(dw, oracle.col_bwd_dw(x, dys)):
+        check_exact(g, r, True)
+    assert tp.tp_get_device_status(wsp) == tp.TP_OK
+
+
 # ------------------------------------------------------------------ edge cases
 
 def test_edge_sizes(tp):
