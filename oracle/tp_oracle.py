@@ -88,16 +88,20 @@ def row_partials(xs: Sequence[np.ndarray], ws: Sequence[np.ndarray]) -> list[np.
     return [widen(x) @ widen(w) for x, w in zip(xs, ws)]
 
 
-def row_fwd_allreduce(xs, ws) -> np.ndarray:
+def row_fwd_allreduce(xs, ws, bias=None) -> np.ndarray:
     """MatMul+AllReduce: full Y = sum_r X_r . W_r, summed r = 0, 1, ..., p-1.
 
     [M027 §01: Y = Y0 + Y1; the AllReduce layout leaves the whole Y on
     every rank.  TP §2.4 / §四: Y = sum_k X_k @ A_k.]
+    With ``bias`` (b [N]) the bias is added once, after the reduction:
+    Y = sum_k X_k A_k + b.  [TP §四, row-parallel forward]
     """
     parts = row_partials(xs, ws)
     y = parts[0].copy()
     for p_r in parts[1:]:
         y = y + p_r
+    if bias is not None:
+        y = y + widen(bias)[None, :]
     return y
 
 
@@ -121,13 +125,14 @@ def row_fwd_allreduce_bf16_collective(xs, ws) -> np.ndarray:
     return acc
 
 
-def row_fwd_reducescatter(xs, ws) -> list[np.ndarray]:
-    """MatMul+ReduceScatter: rank j holds rows [j*M/p, (j+1)*M/p) of Y.
+def row_fwd_reducescatter(xs, ws, bias=None) -> list[np.ndarray]:
+    """MatMul+ReduceScatter: rank j holds rows [j*M/p, (j+1)*M/p) of Y
+    (Y with the bias added once, as in :func:`row_fwd_allreduce`).
 
     [M027 §01: ReduceScatter in the layout that matches what follows;
     TP §2.7: reduce, then each rank keeps one slice.]
     """
-    y = row_fwd_allreduce(xs, ws)
+    y = row_fwd_allreduce(xs, ws, bias)
     p = len(xs)
     m = y.shape[0]
     assert m % p == 0, "ReduceScatter needs M divisible by p"
@@ -160,14 +165,18 @@ def row_bwd_dw(xs, dy) -> list[np.ndarray]:
 
 # ---------------------------------------------------------------- column parallel
 
-def col_fwd(x, ws, apply_gelu: bool = False):
-    """Column-parallel forward: H_k = X . A_k for every shard k.  [TP §2.3, §三]
+def col_fwd(x, ws, apply_gelu: bool = False, biases=None):
+    """Column-parallel forward: H_k = X . A_k (+ b_k) for every shard k.  [TP §2.3, §三]
 
     Returns ``(ys, hs)``: with ``apply_gelu`` ys[k] = GeLU(H_k) (the MLP
     FC1, TP §7.1) and hs[k] = H_k; otherwise ys[k] = H_k and hs is None.
+    ``biases[k]`` (b_k [N_k], optional) is rank k's bias block, added before
+    the activation.  [TP §三, column-parallel forward Y_k = X A_k + b_k]
     """
     xf = widen(x)
     hs = [xf @ widen(w) for w in ws]
+    if biases is not None:
+        hs = [h + widen(b)[None, :] for h, b in zip(hs, biases)]
     if apply_gelu:
         return [gelu(h) for h in hs], hs
     return hs, None
@@ -197,13 +206,15 @@ def all_gather_rows(xs) -> np.ndarray:
     return np.vstack([widen(x) for x in xs])
 
 
-def ag_matmul(xs, ws, apply_gelu: bool = False):
-    """AllGather+MatMul: Y_k = [X_0; ...; X_{p-1}] . A_k.  [M027 §01-§02; TP §11.3]
+def ag_matmul(xs, ws, apply_gelu: bool = False, biases=None):
+    """AllGather+MatMul: Y_k = [X_0; ...; X_{p-1}] . A_k (+ b_k).  [M027 §01-§02; TP §11.3]
 
-    Returns ``(ys, hs, x_gathered)`` with ys/hs as in :func:`col_fwd`.
+    Returns ``(ys, hs, x_gathered)`` with ys/hs (and biases) as in :func:`col_fwd`.
     """
     xg = all_gather_rows(xs)
     hs = [xg @ widen(w) for w in ws]
+    if biases is not None:
+        hs = [h + widen(b)[None, :] for h, b in zip(hs, biases)]
     if apply_gelu:
         return [gelu(h) for h in hs], hs, xg
     return hs, None, xg
@@ -279,3 +290,21 @@ def row_rs_bwd_dw(xs, dys) -> list[np.ndarray]:
     """Backward of MatMul+ReduceScatter, weight gradient: dA_r = X_r^T . dY
     with dY the gathered output gradient.  [TP §四, §11.3]"""
     return row_bwd_dw(xs, np.vstack([np.asarray(d, dtype=np.uint16) for d in dys]))
+
+
+# ---------------------------------------------------------------- bias gradients
+
+def bias_grad(dys) -> np.ndarray:
+    """Gradient of a bias added to every row: db = sum over rows of dY.
+
+    ``dys`` is one output gradient [M, N] or a list of row blocks of one
+    (the token shards of a ReduceScatter output), summed over all their
+    rows.  For the column layer, rank k's db_k is bias_grad(dY_k); for the
+    row layer, db = bias_grad(dY).  [TP §三/§四: Y_k = X A_k + b_k and
+    Y = sum_k X_k A_k + b; b enters every row of Y with weight 1]
+    """
+    if isinstance(dys, (list, tuple)):
+        g = np.vstack([widen(d) for d in dys])
+    else:
+        g = widen(dys)
+    return g.sum(axis=0)

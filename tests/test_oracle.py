@@ -534,3 +534,67 @@ def test_bf16_collective_planted_mistakes():
     assert no_partial_rounding([x, one], [w, one])[0, 0] == 258.0
     assert no_sum_rounding(*_scalar_ranks([256.0, 1.0]))[0, 0] == 257.0
     assert reversed_order(*_scalar_ranks([256.0, 1.0, 1.0]))[0, 0] == 258.0
+
+
+# --------------------------------------------------------------- bias
+
+def test_bias_forward_matches_the_unsharded_layer():
+    """Y = X A + b of the unsharded layer, with b added once on the row
+    layer and b split into the column blocks b_k on the column layer."""
+    p, m, k, n = 4, 8, 6, 12
+    x = _ints((m, k * p), 4000)
+    a = _ints((k * p, n), 4001)
+    b = _ints((1, n), 4002)[0]
+    want = _as_int(x) @ _as_int(a) + _as_int(b)[None, :]
+    got = oracle.row_fwd_allreduce(_shard_cols(x, p), _shard_rows(a, p), bias=b)
+    assert np.array_equal(got, want.astype(np.float64))
+    rs = oracle.row_fwd_reducescatter(_shard_cols(x, p), _shard_rows(a, p), bias=b)
+    assert np.array_equal(np.vstack(rs), want.astype(np.float64))
+    xc = _ints((m, k), 4003)
+    ac = _ints((k, n * p), 4004)
+    bc = _ints((1, n * p), 4005)[0]
+    wantc = _as_int(xc) @ _as_int(ac) + _as_int(bc)[None, :]
+    bks = [bc[j * n:(j + 1) * n] for j in range(p)]
+    ys, _ = oracle.col_fwd(xc, _shard_cols(ac, p), biases=bks)
+    assert np.array_equal(np.hstack(ys), wantc.astype(np.float64))
+    yg, _, _ = oracle.ag_matmul(_shard_rows(xc, p), _shard_cols(ac, p), biases=bks)
+    assert np.array_equal(np.hstack(yg), wantc.astype(np.float64))
+    # GeLU sees the biased pre-activation
+    z, h = oracle.col_fwd(xc, _shard_cols(ac, p), apply_gelu=True, biases=bks)
+    assert np.array_equal(np.hstack(h), wantc.astype(np.float64))
+    assert np.allclose(np.hstack(z), oracle.gelu(wantc.astype(np.float64)))
+
+
+def test_bias_grad_is_the_forward_difference():
+    """For L = sum(G * Y), raising b_j by one raises L by exactly sum_i G[i, j]
+    (integer inputs: every value exact), which is what bias_grad returns; the
+    row-shard form sums the shards' rows."""
+    p, m, k, n = 2, 6, 4, 5
+    x = _ints((m, k * p), 4100)
+    a = _ints((k * p, n), 4101)
+    b = _ints((1, n), 4102)[0]
+    g = _ints((m, n), 4103)
+    xs, ws = _shard_cols(x, p), _shard_rows(a, p)
+    base = float(np.sum(oracle.widen(g) * oracle.row_fwd_allreduce(xs, ws, bias=b)))
+    db = oracle.bias_grad(g)
+    for j in range(n):
+        bj = oracle.widen(b).copy()
+        bj[j] += 1.0
+        up = float(np.sum(oracle.widen(g) * oracle.row_fwd_allreduce(xs, ws, bias=oracle.round_bf16(bj))))
+        assert up - base == db[j]
+    assert np.array_equal(oracle.bias_grad(_shard_rows(g, 3)), db)
+
+
+def test_bias_planted_mistakes():
+    p, m, k, n = 2, 4, 3, 4
+    x = _ints((m, k * p), 4200)
+    a = _ints((k * p, n), 4201)
+    b = _ints((1, n), 4202, 3)[0]
+    want = _as_int(x) @ _as_int(a) + _as_int(b)[None, :]
+    # a bias added by every rank (p times) is caught
+    twice = oracle.row_fwd_allreduce(_shard_cols(x, p), _shard_rows(a, p)) + p * oracle.widen(b)[None, :]
+    assert np.any(_as_int(b) != 0)
+    assert not np.array_equal(twice, want.astype(np.float64))
+    # a bias gradient over the wrong axis is caught
+    g = _ints((m, n), 4203)
+    assert not np.array_equal(oracle.widen(g).sum(axis=1)[:n], oracle.bias_grad(g))
