@@ -72,15 +72,15 @@ def _load() -> ctypes.CDLL:
     S = ctypes.c_size_t
     sig = {
         "tp_workspace_size": (S, [I, I, L, L, L, L, I]),
-        "tp_row_linear_fwd_allreduce": (I, [PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
-        "tp_row_linear_fwd_reducescatter": (I, [PP, PP, PP, I, L, L, L, L, I, P, S, P]),
-        "tp_col_linear_fwd": (I, [P, PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
-        "tp_col_linear_bwd": (I, [P, PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
-        "tp_row_linear_bwd": (I, [PP, PP, P, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
-        "tp_ag_matmul": (I, [PP, PP, PP, P, I, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_fwd_allreduce": (I, [PP, PP, P, PP, I, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_fwd_reducescatter": (I, [PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_col_linear_fwd": (I, [P, PP, PP, PP, PP, I, I, L, L, L, L, I, P, S, P]),
+        "tp_col_linear_bwd": (I, [P, PP, PP, P, PP, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_bwd": (I, [PP, PP, P, PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_ag_matmul": (I, [PP, PP, PP, PP, P, I, PP, I, L, L, L, L, I, P, S, P]),
         "tp_row_linear_fwd_unfused": (I, [PP, PP, P, I, L, L, L, L, I, I, I, P, S, P]),
-        "tp_ag_matmul_bwd": (I, [PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
-        "tp_row_linear_bwd_reducescatter": (I, [PP, PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_ag_matmul_bwd": (I, [PP, PP, PP, PP, PP, PP, I, L, L, L, L, I, P, S, P]),
+        "tp_row_linear_bwd_reducescatter": (I, [PP, PP, PP, PP, PP, P, PP, I, L, L, L, L, I, P, S, P]),
         "tp_pipeline_time": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, L]),
         "tp_num_chunks": (L, [L, L]),
         "tp_choose_chunk_m": (L, [I, I, L, L, L]),
@@ -196,95 +196,97 @@ def tp_get_device_status(ws, stream=None) -> int:
 # ------------------------------------------------------------------ the sharded Linear
 
 def tp_row_linear_fwd_allreduce(x: Sequence, w: Sequence, y: Sequence, ws, chunk_m: int = 0,
-                                stream=None) -> None:
-    """Y = sum_r X_r W_r written once (len(y) == 1) or as p replicas (len(y) == p)."""
+                                stream=None, bias=None) -> None:
+    """Y = sum_r X_r W_r (+ bias) written once (len(y) == 1) or as p replicas (len(y) == p)."""
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
     wp, wb = _ws(ws)
-    _check(_lib.tp_row_linear_fwd_allreduce(_arr(x), _arr(w), _arr(y), len(y), p, M, N, K, chunk_m,
+    _check(_lib.tp_row_linear_fwd_allreduce(_arr(x), _arr(w), _ptr(bias), _arr(y), len(y), p, M, N, K, chunk_m,
                                             _dtype_code(y[0]), wp, wb, _stream(stream)),
            "tp_row_linear_fwd_allreduce")
 
 
 def tp_row_linear_fwd_reducescatter(x: Sequence, w: Sequence, y: Sequence, ws, chunk_m: int = 0,
-                                    stream=None) -> None:
-    """Rank j's y[j] = rows [j M/p, (j+1) M/p) of sum_r X_r W_r."""
+                                    stream=None, bias=None) -> None:
+    """Rank j's y[j] = rows [j M/p, (j+1) M/p) of sum_r X_r W_r (+ bias)."""
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
     wp, wb = _ws(ws)
-    _check(_lib.tp_row_linear_fwd_reducescatter(_arr(x), _arr(w), _arr(y), p, M, N, K, chunk_m,
+    _check(_lib.tp_row_linear_fwd_reducescatter(_arr(x), _arr(w), _ptr(bias), _arr(y), p, M, N, K, chunk_m,
                                                 _dtype_code(y[0]), wp, wb, _stream(stream)),
            "tp_row_linear_fwd_reducescatter")
 
 
 def tp_col_linear_fwd(x, w: Sequence, y: Sequence, ws, epi: int = TP_EPI_NONE, preact=None,
-                      chunk_m: int = 0, stream=None) -> None:
-    """y[k] = X A_k (or GeLU(X A_k), with H_k into preact[k])."""
+                      chunk_m: int = 0, stream=None, bias=None) -> None:
+    """y[k] = X A_k + b_k (or GeLU of it, with H_k into preact[k]); bias[k] = b_k or bias None."""
     p = len(w)
     M, K = x.shape
     N = w[0].shape[1]
     wp, wb = _ws(ws)
-    _check(_lib.tp_col_linear_fwd(_ptr(x), _arr(w), _arr(y), _arr(preact), epi, p, M, N, K, chunk_m,
+    _check(_lib.tp_col_linear_fwd(_ptr(x), _arr(w), _arr(bias), _arr(y), _arr(preact), epi, p, M, N, K, chunk_m,
                                   _out_dtype(y, preact), wp, wb, _stream(stream)), "tp_col_linear_fwd")
 
 
 def tp_col_linear_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0,
-                      stream=None) -> None:
-    """dX = sum_k dY_k A_k^T; dw[k] = X^T dY_k (dw may be None)."""
+                      stream=None, db=None) -> None:
+    """dX = sum_k dY_k A_k^T; dw[k] = X^T dY_k; db[k] = row sum of dY_k (dx, dw, db may be None)."""
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0]
     wp, wb = _ws(ws)
-    _check(_lib.tp_col_linear_bwd(_ptr(x), _arr(w), _arr(dy), _ptr(dx), _arr(dw), p, M, N, K, chunk_m,
-                                  _out_dtype(dx, dw), wp, wb, _stream(stream)), "tp_col_linear_bwd")
+    _check(_lib.tp_col_linear_bwd(_ptr(x), _arr(w), _arr(dy), _ptr(dx), _arr(dw), _arr(db), p, M, N, K,
+                                  chunk_m, _out_dtype(dx, dw, db), wp, wb, _stream(stream)), "tp_col_linear_bwd")
 
 
 def tp_row_linear_bwd(x, w: Sequence, dy, dx, dw, ws, preact=None, chunk_m: int = 0,
-                      stream=None) -> None:
-    """dx[k] = dY A_k^T (times GeLU'(preact[k])); dw[k] = X_k^T dY."""
+                      stream=None, db=None) -> None:
+    """dx[k] = dY A_k^T (times GeLU'(preact[k])); dw[k] = X_k^T dY; db = row sum of dY."""
     p = len(w)
     K, N = w[0].shape
     M = dy.shape[0]
     wp, wb = _ws(ws)
-    _check(_lib.tp_row_linear_bwd(_arr(x), _arr(w), _ptr(dy), _arr(dx), _arr(dw), _arr(preact), p,
-                                  M, N, K, chunk_m, _out_dtype(dx, dw), wp, wb, _stream(stream)),
+    _check(_lib.tp_row_linear_bwd(_arr(x), _arr(w), _ptr(dy), _arr(dx), _arr(dw), _ptr(db), _arr(preact), p,
+                                  M, N, K, chunk_m, _out_dtype(dx, dw, db), wp, wb, _stream(stream)),
            "tp_row_linear_bwd")
 
 
 def tp_ag_matmul(x: Sequence, w: Sequence, y: Sequence, ws, x_gathered=None,
-                 epi: int = TP_EPI_NONE, preact=None, chunk_m: int = 0, stream=None) -> None:
-    """y[k] = [X_0; ...; X_{p-1}] A_k (optionally GeLU, H_k, gathered X)."""
+                 epi: int = TP_EPI_NONE, preact=None, chunk_m: int = 0, stream=None, bias=None) -> None:
+    """y[k] = [X_0; ...; X_{p-1}] A_k + b_k (optionally GeLU, H_k, gathered X)."""
     p = len(x)
     Mp, K = x[0].shape
     N = w[0].shape[1]
     wp, wb = _ws(ws)
-    _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
+    _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(bias), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
                              Mp * p, N, K, chunk_m, _out_dtype(y, preact), wp, wb, _stream(stream)),
            "tp_ag_matmul")
 
 
-def tp_ag_matmul_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0, stream=None) -> None:
-    """dx[s] = rows of sum_k dY_k A_k^T (ReduceScatter); dw[k] = [X_0;...]^T dY_k."""
+def tp_ag_matmul_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0, stream=None,
+                     db=None) -> None:
+    """dx[s] = rows of sum_k dY_k A_k^T (ReduceScatter); dw[k] = [X_0;...]^T dY_k; db[k] = row sum of dY_k."""
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0]
     wp, wb = _ws(ws)
-    _check(_lib.tp_ag_matmul_bwd(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), p, M, N, K, chunk_m,
-                                 _out_dtype(dx, dw), wp, wb, _stream(stream)), "tp_ag_matmul_bwd")
+    _check(_lib.tp_ag_matmul_bwd(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), _arr(db), p, M, N, K, chunk_m,
+                                 _out_dtype(dx, dw, db), wp, wb, _stream(stream)), "tp_ag_matmul_bwd")
 
 
 def tp_row_linear_bwd_reducescatter(x, w: Sequence, dy: Sequence, dx, dw, ws, preact=None, chunk_m: int = 0,
-                                    stream=None) -> None:
-    """dx[r] = [dY_0;...] A_r^T (* GeLU'(preact[r])) (AllGather); dw[r] = X_r^T [dY_0;...]."""
+                                    stream=None, db=None) -> None:
+    """dx[r] = [dY_0;...] A_r^T (* GeLU'(preact[r])) (AllGather); dw[r] = X_r^T [dY_0;...];
+    db = row sum of all the dY shards."""
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0] * p
     wp, wb = _ws(ws)
-    _check(_lib.tp_row_linear_bwd_reducescatter(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), _arr(preact), p,
-                                                M, N, K, chunk_m, _out_dtype(dx, dw), wp, wb, _stream(stream)),
-           "tp_row_linear_bwd_reducescatter")
+    _check(_lib.tp_row_linear_bwd_reducescatter(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), _ptr(db),
+                                                _arr(preact), p, M, N, K, chunk_m, _out_dtype(dx, dw, db), wp, wb,
+                                                _stream(stream)), "tp_row_linear_bwd_reducescatter")
 
 
 def tp_row_linear_fwd_unfused(x: Sequence, w: Sequence, y, ws, chunk_m: int = 0, phases: int = 3,

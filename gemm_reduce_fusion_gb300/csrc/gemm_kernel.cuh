@@ -53,6 +53,8 @@ struct GemmParams {
   CUtensorMap tmB[MAX_MAPS];
   void* out[MAX_GROUPS];  // per-group output base (group g = gm * Gn + gn)
   void* aux[MAX_GROUPS];  // GELU: H out (nullable); DGELU: H in (bf16)
+  const void* bias[MAX_GROUPS];  // per-group bias over the output's columns (bf16, nullable),
+                                 // added to the accumulator before the activation
   int32_t Gm, Gn;
   int32_t m_tiles, n_tiles;  // per group
   int32_t chunk_tiles;       // tiles per chunk along the chunked axis
@@ -167,6 +169,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// v[e] += b[e] for 8 consecutive bf16 bias values (16-byte aligned).
+__device__ __forceinline__ void add_bias8(float (&v)[8], const uint16_t* b) {
+  const uint4 q = *reinterpret_cast<const uint4*>(b);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] += bf16_bits_to_f(static_cast<uint16_t>(w[i] & 0xFFFFu));
+    v[2 * i + 1] += bf16_bits_to_f(static_cast<uint16_t>(w[i] >> 16));
+  }
+}
+
 // Epilogue transform of 8 consecutive values; `aux` points at the matching 8
 // elements of H (DGELU reads them, GELU writes them when non-null).
 __device__ __forceinline__ void epi8(const GemmParams& P, float (&v)[8], void* aux) {
@@ -267,6 +280,10 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
       continue;
     }
     if (OUT_T) {
+      // operand-swapped: GEMM row gi is the output column, so one bias value
+      const float bsc = P.bias[g] != nullptr
+                            ? bf16_bits_to_f(static_cast<const uint16_t*>(P.bias[g])[gi])
+                            : 0.0f;
 #pragma unroll
       for (int i = 0; i < CW; ++i) {
         const int32_t gj = gj0 + i;
@@ -274,7 +291,7 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
           const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
           const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
           for (int rep = 0; rep < P.n_rep; ++rep)
-            epi_store1(P, __uint_as_float(r[i]), P.out[g + rep], P.aux[g], off_o, off_a);
+            epi_store1(P, __uint_as_float(r[i]) + bsc, P.out[g + rep], P.aux[g], off_o, off_a);
         }
       }
     } else {
@@ -286,6 +303,7 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
         float v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[i + e]);
+        if (P.bias[g] != nullptr) add_bias8(v, static_cast<const uint16_t*>(P.bias[g]) + gj);
         void* auxp = nullptr;
         if (P.epi != EPI_NONE && P.aux[g] != nullptr) {
           const size_t aesz = (P.epi == EPI_DGELU) ? 2 : esz;
@@ -781,6 +799,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 struct ReduceParams {
   void* out[MAX_GROUPS];
   void* aux[MAX_GROUPS];
+  const void* bias[MAX_GROUPS];  // as GemmParams::bias, indexed by the output column b
   const float* partial;
   int32_t G;          // groups
   int32_t A, B;       // output-orientation extents of one group (B contiguous)
@@ -797,6 +816,7 @@ __device__ __forceinline__ float bf16_round_f(float x) {
 // partials summed in split order; 4 consecutive b per thread.  With
 // bf16_chain the sum is the one a bf16 collective forms from bf16 partials:
 // acc = bf16(P_0), then acc = bf16(acc + bf16(P_s)) for s = 1, 2, ...
+// n_split == 0 (a contraction of length zero) sums nothing: out = epilogue(bias).
 __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) {
   const int64_t per_group = static_cast<int64_t>(R.A) * R.B;
   const int64_t total4 = static_cast<int64_t>(R.G) * per_group / 4;
@@ -804,7 +824,8 @@ __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) 
   for (int64_t i4 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i4 < total4;
        i4 += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t e = i4 * 4;
-    float4 acc = *reinterpret_cast<const float4*>(R.partial + e);
+    float4 acc = R.n_split > 0 ? *reinterpret_cast<const float4*>(R.partial + e)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
     if (R.bf16_chain) {
       acc = make_float4(bf16_round_f(acc.x), bf16_round_f(acc.y), bf16_round_f(acc.z),
                         bf16_round_f(acc.w));
@@ -828,6 +849,13 @@ __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) 
     const int64_t rem = e % per_group;
     const int64_t a = rem / R.B;
     const int64_t b = rem % R.B;
+    if (R.bias[g] != nullptr) {
+      const uint2 q = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(R.bias[g]) + b);
+      acc.x += bf16_bits_to_f(static_cast<uint16_t>(q.x & 0xFFFFu));
+      acc.y += bf16_bits_to_f(static_cast<uint16_t>(q.x >> 16));
+      acc.z += bf16_bits_to_f(static_cast<uint16_t>(q.y & 0xFFFFu));
+      acc.w += bf16_bits_to_f(static_cast<uint16_t>(q.y >> 16));
+    }
     float v[4] = {acc.x, acc.y, acc.z, acc.w};
     if (R.epi == EPI_GELU) {
       if (R.aux[g] != nullptr) {
@@ -856,6 +884,62 @@ __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) 
         *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(R.out[g + rep]) + a * R.ld_out + b) =
             make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
       }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- bias gradient
+
+struct BiasGradParams {
+  const void* src[MAX_MAPS];  // bf16 [rows, N] row-major sources
+  void* out[MAX_MAPS];        // [N] outputs
+  int32_t src_per_out;        // output o sums sources o*src_per_out .. (o+1)*src_per_out-1, in order
+  int32_t N;
+  int64_t rows;               // rows of every source
+  int32_t out_f32;
+};
+
+constexpr int BG_COLS = 64;   // columns per CTA: 8 threads x 8 bf16 (one 16-byte load each)
+constexpr int BG_LANES = 32;  // row lanes per CTA
+
+// out[o][j] = sum over the sources of o, in order, and over their rows of
+// src[i, j].  CTA (blockIdx.x, blockIdx.y = o) owns 64 columns; thread
+// (lane, cg) sums rows lane, lane + 32, ... of 8 columns with 16-byte loads
+// (a warp reads four 128-byte row segments), then the 32 lanes are summed in
+// lane order through shared memory: the result does not depend on timing.
+__global__ void __launch_bounds__(BG_COLS / 8 * BG_LANES)
+    tp_bias_grad_kernel(const __grid_constant__ BiasGradParams B) {
+  __shared__ float red[BG_LANES][BG_COLS + 1];
+  const int cg = threadIdx.x % (BG_COLS / 8);
+  const int lane = threadIdx.x / (BG_COLS / 8);
+  const int o = blockIdx.y;
+  const int32_t c0 = blockIdx.x * BG_COLS + cg * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c0 < B.N && B.rows > 0) {
+    for (int s = 0; s < B.src_per_out; ++s) {
+      const uint16_t* src = static_cast<const uint16_t*>(B.src[o * B.src_per_out + s]) + c0;
+#pragma unroll 4
+      for (int64_t i = lane; i < B.rows; i += BG_LANES) {
+        const uint4 q = *reinterpret_cast<const uint4*>(src + i * B.N);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] += bf16_bits_to_f(static_cast<uint16_t>(w[k] & 0xFFFFu));
+          acc[2 * k + 1] += bf16_bits_to_f(static_cast<uint16_t>(w[k] >> 16));
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) red[lane][cg * 8 + k] = acc[k];
+  __syncthreads();
+  if (threadIdx.x < BG_COLS) {
+    const int32_t col = blockIdx.x * BG_COLS + threadIdx.x;
+    float sum = 0.f;
+    for (int l = 0; l < BG_LANES; ++l) sum += red[l][threadIdx.x];
+    if (col < B.N) {
+      if (B.out_f32) static_cast<float*>(B.out[o])[col] = sum;
+      else static_cast<__nv_bfloat16*>(B.out[o])[col] = __float2bfloat16_rn(sum);
     }
   }
 }

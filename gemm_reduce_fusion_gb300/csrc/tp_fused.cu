@@ -455,6 +455,54 @@ size_t esize(tp_dtype d) { return d == TP_FP32 ? 4 : 2; }
 tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
                             const DevInfo& di, int phases);
 
+// Second stage over the launch's groups: out = epilogue(bias + sum of the
+// n_split fp32 partials in split order); n_split == 0 sums nothing.
+tp_status launch_reduce(const Launch& L, const Shape& s, int n_split, cudaStream_t stream,
+                        const DevInfo& di) {
+  const GemmParams& P = L.P;
+  ReduceParams R;
+  std::memset(&R, 0, sizeof(R));
+  for (int g = 0; g < MAX_GROUPS; ++g) {
+    R.out[g] = P.out[g];
+    R.aux[g] = P.aux[g];
+    R.bias[g] = P.bias[g];
+  }
+  R.partial = P.partial;
+  R.G = s.Gm * s.Gn;
+  R.A = static_cast<int32_t>(s.swap ? s.cols_g : s.rows_g);
+  R.B = static_cast<int32_t>(s.swap ? s.rows_g : s.cols_g);
+  R.ld_out = P.ld_out;
+  R.ld_aux = P.ld_aux;
+  R.out_f32 = P.out_f32;
+  R.epi = P.epi;
+  R.n_split = n_split;
+  R.n_rep = P.n_rep;
+  R.bf16_chain = L.bf16_chain ? 1 : 0;
+  const int64_t total4 = static_cast<int64_t>(R.G) * R.A * R.B / 4;
+  const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(total4, 256), di.sms * 8)));
+  tp_splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(R);
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// db[o] = sum over rows (and, in order, over the src_per_out sources of o)
+// of the bf16 [rows, N] sources; n_src / src_per_out outputs.
+tp_status bias_grad(const void* const* src, int n_src, int src_per_out, void* const* out, int64_t rows,
+                    int64_t N, tp_dtype dt, cudaStream_t stream) {
+  if (N == 0) return TP_OK;
+  BiasGradParams B;
+  std::memset(&B, 0, sizeof(B));
+  for (int i = 0; i < n_src; ++i) B.src[i] = src[i];
+  const int n_out = n_src / src_per_out;
+  for (int o = 0; o < n_out; ++o) B.out[o] = out[o];
+  B.src_per_out = src_per_out;
+  B.N = static_cast<int32_t>(N);
+  B.rows = rows;
+  B.out_f32 = dt == TP_FP32 ? 1 : 0;
+  const dim3 grid(static_cast<unsigned>(cdiv(N, BG_COLS)), static_cast<unsigned>(n_out));
+  tp_bias_grad_kernel<<<grid, BG_COLS / 8 * BG_LANES, 0, stream>>>(B);
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 tp_status run_launch(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
                      const DevInfo& di) {
   return run_launch_phases(L, out_dtype, ws, stream, di, 3);
@@ -470,10 +518,18 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
   GemmParams& P = L.P;
   P.status = static_cast<uint32_t*>(ws);
   P.out_f32 = out_dtype == TP_FP32 ? 1 : 0;
+  const int G = s.Gm * s.Gn;
+  bool any_bias = false;
+  for (int g = 0; g < G; ++g) any_bias = any_bias || P.bias[g] != nullptr;
+  if (s.kb_total == 0 && any_bias) {
+    // K == 0 with a bias: out = epilogue(bias), from the second-stage kernel
+    // summing zero partials.
+    if (!(phases & 1)) return TP_OK;
+    return launch_reduce(L, s, 0, stream, di);
+  }
   if (s.kb_total == 0) {
     if (!(phases & 1)) return TP_OK;
     // K == 0: the product is zero; GeLU(0) = 0 and G * GeLU'(.) = 0 too.
-    const int G = s.Gm * s.Gn;
     const int64_t A = s.swap ? s.cols_g : s.rows_g;
     const int64_t B = s.swap ? s.rows_g : s.cols_g;
     for (int g = 0; g < G; ++g) {
@@ -494,29 +550,7 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
   const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
                          : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
   if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
-  if (s.n_split > 1 && (phases & 2)) {
-    ReduceParams R;
-    std::memset(&R, 0, sizeof(R));
-    for (int g = 0; g < MAX_GROUPS; ++g) {
-      R.out[g] = P.out[g];
-      R.aux[g] = P.aux[g];
-    }
-    R.partial = P.partial;
-    R.G = s.Gm * s.Gn;
-    R.A = static_cast<int32_t>(s.swap ? s.cols_g : s.rows_g);
-    R.B = static_cast<int32_t>(s.swap ? s.rows_g : s.cols_g);
-    R.ld_out = P.ld_out;
-    R.ld_aux = P.ld_aux;
-    R.out_f32 = P.out_f32;
-    R.epi = P.epi;
-    R.n_split = s.n_split;
-    R.n_rep = P.n_rep;
-    R.bf16_chain = L.bf16_chain ? 1 : 0;
-    const int64_t total4 = static_cast<int64_t>(R.G) * R.A * R.B / 4;
-    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(total4, 256), di.sms * 8)));
-    tp_splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(R);
-    if (cudaGetLastError() != cudaSuccess) return TP_ERR_CUDA;
-  }
+  if (s.n_split > 1 && (phases & 2)) return launch_reduce(L, s, s.n_split, stream, di);
   return TP_OK;
 }
 
@@ -713,9 +747,10 @@ tp_status tp_get_device_status(void* ws, cudaStream_t stream) {
 
 // ---------------------------------------------------------------- row parallel
 
-static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* w, void* const* y,
-                              int n_out, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
-                              tp_dtype dt, void* ws, size_t ws_bytes, cudaStream_t stream) {
+static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* w, const void* bias,
+                              void* const* y, int n_out, int p, int64_t M, int64_t N, int64_t K,
+                              int64_t chunk_m, tp_dtype dt, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, dt));
   if (rs) {
     if (M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
@@ -727,6 +762,7 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   TP_TRY(check_ptrs(x, p, work && K > 0));
   TP_TRY(check_ptrs(w, p, work && K > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(y), n_out, work));
+  TP_TRY(check_ptr(bias, work && bias != nullptr));
   const tp_op op = rs ? TP_OP_ROW_RS : TP_OP_ROW_AR;
   std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m, dt);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
@@ -736,6 +772,7 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
     std::vector<Range> ins, outs;
     add_ranges(&ins, x, p, M * K * 2);
     add_ranges(&ins, w, p, K * N * 2);
+    if (bias != nullptr) ins.push_back({bias, static_cast<size_t>(N * 2)});
     add_ranges(&outs, const_cast<const void* const*>(y), n_out, (rs ? Mp : M) * N * esize(dt));
     if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
   }
@@ -769,8 +806,12 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   if (!rs) {
     for (int i = 0; i < n_out; ++i) P.out[i] = y[i];
     P.n_rep = n_out;
+    P.bias[0] = bias;  // once, after the reduction; replicas share it
   } else {
-    for (int j = 0; j < p; ++j) P.out[j] = y[j];
+    for (int j = 0; j < p; ++j) {
+      P.out[j] = y[j];
+      P.bias[j] = bias;
+    }
     if (!s.swap) P.a_row_gm = static_cast<int32_t>(Mp);
     else P.b_col_gn = static_cast<int32_t>(Mp);
   }
@@ -778,24 +819,26 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   return run_launch(L, dt, ws, stream, di);
 }
 
-tp_status tp_row_linear_fwd_allreduce(const void* const* x, const void* const* w, void* const* y,
-                                      int n_out, int p, int64_t M, int64_t N, int64_t K,
-                                      int64_t chunk_m, tp_dtype out_dtype, void* ws,
+tp_status tp_row_linear_fwd_allreduce(const void* const* x, const void* const* w, const void* bias,
+                                      void* const* y, int n_out, int p, int64_t M, int64_t N,
+                                      int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
                                       size_t ws_bytes, cudaStream_t stream) {
-  return row_fwd_impl(false, x, w, y, n_out, p, M, N, K, chunk_m, out_dtype, ws, ws_bytes, stream);
+  return row_fwd_impl(false, x, w, bias, y, n_out, p, M, N, K, chunk_m, out_dtype, ws, ws_bytes,
+                      stream);
 }
 
 tp_status tp_row_linear_fwd_reducescatter(const void* const* x, const void* const* w,
-                                          void* const* y, int p, int64_t M, int64_t N, int64_t K,
-                                          int64_t chunk_m, tp_dtype out_dtype, void* ws,
-                                          size_t ws_bytes, cudaStream_t stream) {
-  return row_fwd_impl(true, x, w, y, p, p, M, N, K, chunk_m, out_dtype, ws, ws_bytes, stream);
+                                          const void* bias, void* const* y, int p, int64_t M,
+                                          int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype,
+                                          void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return row_fwd_impl(true, x, w, bias, y, p, p, M, N, K, chunk_m, out_dtype, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- column parallel
 
 static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, const void* const* w,
-                              void* const* y, void* const* preact, tp_epilogue epi, int p,
+                              const void* const* bias, void* const* y, void* const* preact,
+                              tp_epilogue epi, int p,
                               int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype dt,
                               void* ws, size_t ws_bytes, cudaStream_t stream, void* x_gathered) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, dt));
@@ -809,6 +852,7 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
   const bool want_h = epi == TP_EPI_GELU && preact != nullptr;
   TP_TRY(check_ptrs(const_cast<const void* const*>(preact), p, work && want_h));
   TP_TRY(check_ptr(x_gathered, x_gathered != nullptr));
+  TP_TRY(check_ptrs(bias, p, work && bias != nullptr));
   const tp_op op = ag ? TP_OP_AG_MM : TP_OP_COL_FWD;
   std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m, dt);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
@@ -818,6 +862,7 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
     if (ag) add_ranges(&ins, xs, p, Mp * K * 2);
     else if (x1 != nullptr) ins.push_back({x1, static_cast<size_t>(M * K * 2)});
     add_ranges(&ins, w, p, K * N * 2);
+    if (work) add_ranges(&ins, bias, p, N * 2);
     add_ranges(&outs, const_cast<const void* const*>(y), p, M * N * esize(dt));
     if (want_h) add_ranges(&outs, const_cast<const void* const*>(preact), p, M * N * esize(dt));
     if (x_gathered != nullptr) outs.push_back({x_gathered, static_cast<size_t>(M * K * 2)});
@@ -869,6 +914,7 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
     for (int k = 0; k < p; ++k) {
       P.out[k] = y[k];
       P.aux[k] = want_h ? preact[k] : nullptr;
+      P.bias[k] = bias ? bias[k] : nullptr;
     }
   } else {
     // group (gm, gn): standard gm = source shard s, gn = shard k;
@@ -882,6 +928,7 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
         const int64_t off = static_cast<int64_t>(src) * Mp * N * es;
         P.out[gm * p + gn] = static_cast<uint8_t*>(y[k]) + off;
         P.aux[gm * p + gn] = want_h ? static_cast<uint8_t*>(preact[k]) + off : nullptr;
+        P.bias[gm * p + gn] = bias ? bias[k] : nullptr;
       }
     }
   }
@@ -889,19 +936,19 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
   return run_launch(L, dt, ws, stream, di);
 }
 
-tp_status tp_col_linear_fwd(const void* x, const void* const* w, void* const* y,
-                            void* const* preact, tp_epilogue epi, int p, int64_t M, int64_t N,
-                            int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
+tp_status tp_col_linear_fwd(const void* x, const void* const* w, const void* const* bias,
+                            void* const* y, void* const* preact, tp_epilogue epi, int p, int64_t M,
+                            int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
                             size_t ws_bytes, cudaStream_t stream) {
-  return col_like_fwd(false, nullptr, x, w, y, preact, epi, p, M, N, K, chunk_m, out_dtype, ws,
+  return col_like_fwd(false, nullptr, x, w, bias, y, preact, epi, p, M, N, K, chunk_m, out_dtype, ws,
                       ws_bytes, stream, nullptr);
 }
 
-tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* y,
-                       void* x_gathered, tp_epilogue epi, void* const* preact, int p, int64_t M,
-                       int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
-                       size_t ws_bytes, cudaStream_t stream) {
-  return col_like_fwd(true, x, nullptr, w, y, preact, epi, p, M, N, K, chunk_m, out_dtype, ws,
+tp_status tp_ag_matmul(const void* const* x, const void* const* w, const void* const* bias,
+                       void* const* y, void* x_gathered, tp_epilogue epi, void* const* preact, int p,
+                       int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype,
+                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return col_like_fwd(true, x, nullptr, w, bias, y, preact, epi, p, M, N, K, chunk_m, out_dtype, ws,
                       ws_bytes, stream, x_gathered);
 }
 
@@ -943,16 +990,18 @@ static tp_status weight_grad(const Shape& s, const void* const* xk, const void* 
 }
 
 tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* const* dy, void* dx,
-                            void* const* dw, int p, int64_t M, int64_t N, int64_t K,
+                            void* const* dw, void* const* db, int p, int64_t M, int64_t N, int64_t K,
                             int64_t chunk_m, tp_dtype out_dtype, void* ws, size_t ws_bytes,
                             cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
-  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  if (dx == nullptr && dw == nullptr && db == nullptr) return TP_ERR_INVALID_ARG;
   const bool dx_work = dx != nullptr && M > 0 && K > 0;
   const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  const bool db_work = db != nullptr && N > 0;
   TP_TRY(check_ptr(dx, dx_work));
   TP_TRY(check_ptrs(w, p, dx_work && N > 0));
-  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || ((dw_work || db_work) && M > 0)));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(db), p, db_work));
   TP_TRY(check_ptr(x, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   std::vector<Shape> shapes = op_shapes(TP_OP_COL_BWD, p, M, N, K, chunk_m, out_dtype);
@@ -964,9 +1013,10 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
     add_ranges(&ins, dy, p, M * N * 2);
     if (dx) outs.push_back({dx, static_cast<size_t>(M * K * esize(out_dtype))});
     if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (db) add_ranges(&outs, const_cast<const void* const*>(db), p, N * esize(out_dtype));
     if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
   }
-  if (!dx_work && !dw_work) return TP_OK;
+  if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
   if (dx_work) {
@@ -1000,20 +1050,23 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
     TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
   if (dw_work) TP_TRY(weight_grad(shapes[1], nullptr, x, dy, nullptr, dw, p, M, N, K, out_dtype, ws, stream, di));
+  if (db_work) TP_TRY(bias_grad(dy, p, 1, db, M, N, out_dtype, stream));   // db_k = sum of dY_k's rows
   return TP_OK;
 }
 
 tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const void* dy,
-                            void* const* dx, void* const* dw, const void* const* preact, int p,
-                            int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype out_dtype,
-                            void* ws, size_t ws_bytes, cudaStream_t stream) {
+                            void* const* dx, void* const* dw, void* db, const void* const* preact,
+                            int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                            tp_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
   const bool dx_work = dx != nullptr && M > 0 && K > 0;
   const bool dw_work = dw != nullptr && K > 0 && N > 0;
-  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  const bool db_work = db != nullptr && N > 0;
+  if (dx == nullptr && dw == nullptr && db == nullptr) return TP_ERR_INVALID_ARG;
   TP_TRY(check_ptrs(const_cast<const void* const*>(dx), p, dx_work));
   TP_TRY(check_ptrs(w, p, dx_work && N > 0));
-  TP_TRY(check_ptr(dy, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptr(dy, (dx_work && N > 0) || ((dw_work || db_work) && M > 0)));
+  TP_TRY(check_ptr(db, db_work));
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
@@ -1027,9 +1080,10 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
     add_ranges(&ins, preact, p, M * K * 2);
     if (dx) add_ranges(&outs, const_cast<const void* const*>(dx), p, M * K * esize(out_dtype));
     if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (db) outs.push_back({db, static_cast<size_t>(N * esize(out_dtype))});
     if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
   }
-  if (!dx_work && !dw_work) return TP_OK;
+  if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
   if (dx_work) {
@@ -1068,6 +1122,7 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
     TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
   if (dw_work) TP_TRY(weight_grad(shapes[1], x, nullptr, nullptr, dy, dw, p, M, N, K, out_dtype, ws, stream, di));
+  if (db_work) TP_TRY(bias_grad(&dy, 1, 1, &db, M, N, out_dtype, stream));   // db = sum of dY's rows
   return TP_OK;
 }
 
@@ -1077,18 +1132,21 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
 // ---------------------------------------------------------------- sequence-parallel backward
 
 extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w, const void* const* dy,
-                                      void* const* dx, void* const* dw, int p, int64_t M, int64_t N,
-                                      int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
-                                      size_t ws_bytes, cudaStream_t stream) {
+                                      void* const* dx, void* const* dw, void* const* db, int p,
+                                      int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                      tp_dtype out_dtype, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
   if (M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
-  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  if (dx == nullptr && dw == nullptr && db == nullptr) return TP_ERR_INVALID_ARG;
   const int64_t Mp = M / p;
   const bool dx_work = dx != nullptr && M > 0 && K > 0;
   const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  const bool db_work = db != nullptr && N > 0;
   TP_TRY(check_ptrs(const_cast<const void* const*>(dx), p, dx_work));
   TP_TRY(check_ptrs(w, p, dx_work && N > 0));
-  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || ((dw_work || db_work) && M > 0)));
+  TP_TRY(check_ptrs(const_cast<const void* const*>(db), p, db_work));
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   std::vector<Shape> shapes = op_shapes(TP_OP_AG_MM_BWD, p, M, N, K, chunk_m, out_dtype);
@@ -1100,9 +1158,10 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
     add_ranges(&ins, dy, p, M * N * 2);
     if (dx) add_ranges(&outs, const_cast<const void* const*>(dx), p, Mp * K * esize(out_dtype));
     if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (db) add_ranges(&outs, const_cast<const void* const*>(db), p, N * esize(out_dtype));
     if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
   }
-  if (!dx_work && !dw_work) return TP_OK;
+  if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
   if (dx_work) {
@@ -1162,24 +1221,28 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
     L.variant = V_MM;
     TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
+  if (db_work) TP_TRY(bias_grad(dy, p, 1, db, M, N, out_dtype, stream));   // db_k = sum of dY_k's M rows
   return TP_OK;
 }
 
 extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const void* const* w,
                                                      const void* const* dy, void* const* dx,
-                                                     void* const* dw, const void* const* preact, int p,
-                                                     int64_t M, int64_t N, int64_t K, int64_t chunk_m,
+                                                     void* const* dw, void* db,
+                                                     const void* const* preact, int p, int64_t M,
+                                                     int64_t N, int64_t K, int64_t chunk_m,
                                                      tp_dtype out_dtype, void* ws, size_t ws_bytes,
                                                      cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
   if (M % p != 0) return TP_ERR_UNSUPPORTED_SHAPE;
-  if (dx == nullptr && dw == nullptr) return TP_ERR_INVALID_ARG;
+  if (dx == nullptr && dw == nullptr && db == nullptr) return TP_ERR_INVALID_ARG;
   const int64_t Mp = M / p;
   const bool dx_work = dx != nullptr && M > 0 && K > 0;
   const bool dw_work = dw != nullptr && K > 0 && N > 0;
+  const bool db_work = db != nullptr && N > 0;
   TP_TRY(check_ptrs(const_cast<const void* const*>(dx), p, dx_work));
   TP_TRY(check_ptrs(w, p, dx_work && N > 0));
-  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || (dw_work && M > 0)));
+  TP_TRY(check_ptrs(dy, p, (dx_work && N > 0) || ((dw_work || db_work) && M > 0)));
+  TP_TRY(check_ptr(db, db_work));
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
@@ -1193,9 +1256,10 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
     add_ranges(&ins, preact, p, M * K * 2);
     if (dx) add_ranges(&outs, const_cast<const void* const*>(dx), p, M * K * esize(out_dtype));
     if (dw) add_ranges(&outs, const_cast<const void* const*>(dw), p, K * N * esize(out_dtype));
+    if (db) outs.push_back({db, static_cast<size_t>(N * esize(out_dtype))});
     if (any_overlap(outs, ins)) return TP_ERR_INVALID_ARG;
   }
-  if (!dx_work && !dw_work) return TP_OK;
+  if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
   const size_t es = esize(out_dtype);
@@ -1267,6 +1331,8 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
     L.variant = V_MM;
     TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
+  // db = sum over the p token shards of dY, in shard order, of their rows
+  if (db_work) TP_TRY(bias_grad(dy, p, p, &db, Mp, N, out_dtype, stream));
   return TP_OK;
 }
 
@@ -1371,6 +1437,6 @@ extern "C" tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, c
   if (M == 0 || N == 0) return TP_OK;
   void* scratch = nullptr;
   TP_TRY(noalloc_scratch(&scratch));
-  return row_fwd_impl(false, x, w, y, n_out, p, M, N, K, chunk_m, out_dtype, scratch,
+  return row_fwd_impl(false, x, w, nullptr, y, n_out, p, M, N, K, chunk_m, out_dtype, scratch,
                       TP_NOALLOC_SCRATCH_BYTES, stream);
 }

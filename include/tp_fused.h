@@ -99,34 +99,38 @@ size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64
                          tp_dtype out_dtype);
 
 /* Row-parallel forward, MatMul+AllReduce layout.  [M027 §01; TP §2.4, §四]
- *   Y = sum_{r=0}^{p-1} X_r . W_r, accumulated in rank order, written once.
+ *   Y = sum_{r=0}^{p-1} X_r . W_r (+ b), accumulated in rank order, written once.
  *   x[r]: X_r [M, K] (rank r's column block of the layer input)
  *   w[r]: W_r [K, N] (rank r's row block of the weight)
+ *   bias: b [N] bf16 or NULL, added once after the reduction (in fp32,
+ *         before the output rounding).  [TP §四: Y = AllReduce(X_k A_k) + b]
  *   y[i]: Y [M, N] for i < n_out.  n_out == 1 writes the full Y once;
  *         n_out == p writes p bit-identical replicas (one per rank).    */
-tp_status tp_row_linear_fwd_allreduce(const void* const* x, const void* const* w,
+tp_status tp_row_linear_fwd_allreduce(const void* const* x, const void* const* w, const void* bias,
                                       void* const* y, int n_out, int p,
                                       int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                                       tp_dtype out_dtype, void* ws, size_t ws_bytes,
                                       cudaStream_t stream);
 
 /* Row-parallel forward, MatMul+ReduceScatter layout.  [M027 §01; TP §2.7]
- *   Same reduction; rank j receives rows [j*M/p, (j+1)*M/p) of Y.
+ *   Same reduction (and bias); rank j receives rows [j*M/p, (j+1)*M/p) of Y.
  *   y[j]: [M/p, N].  Requires M % p == 0.                                */
 tp_status tp_row_linear_fwd_reducescatter(const void* const* x, const void* const* w,
-                                          void* const* y, int p,
+                                          const void* bias, void* const* y, int p,
                                           int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                                           tp_dtype out_dtype, void* ws, size_t ws_bytes,
                                           cudaStream_t stream);
 
 /* Column-parallel forward.  [TP §2.3, §三, §7.1]
- *   H_k = X . A_k for k = 0..p-1 (one grouped launch, no reduction).
+ *   H_k = X . A_k (+ b_k) for k = 0..p-1 (one grouped launch, no reduction).
  *   x: X [M, K] (replicated input); w[k]: A_k [K, N]; y[k]: [M, N].
+ *   bias: NULL, or bias[k] = b_k [N] bf16, rank k's block of the bias,
+ *         added before the activation.  [TP §三: Y_k = X A_k + b_k]
  *   epi == TP_EPI_NONE: y[k] = H_k.
  *   epi == TP_EPI_GELU: y[k] = GeLU(H_k); if preact != NULL, preact[k]
  *   ([M, N], same dtype as y) receives H_k for the backward pass.         */
-tp_status tp_col_linear_fwd(const void* x, const void* const* w, void* const* y,
-                            void* const* preact, tp_epilogue epi, int p,
+tp_status tp_col_linear_fwd(const void* x, const void* const* w, const void* const* bias,
+                            void* const* y, void* const* preact, tp_epilogue epi, int p,
                             int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                             tp_dtype out_dtype, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
@@ -135,10 +139,13 @@ tp_status tp_col_linear_fwd(const void* x, const void* const* w, void* const* y,
  *   dX = sum_{k=0}^{p-1} dY_k . A_k^T  (the backward AllReduce, fused,
  *        accumulated in rank order, written once) -> dx [M, K] if dx != NULL
  *   dA_k = X^T . dY_k (local)                     -> dw[k] [K, N] if dw != NULL
+ *   db_k = sum over the M rows of dY_k (the gradient of b_k; summed in a
+ *          fixed order, so deterministic)         -> db[k] [N] if db != NULL
  *   x: X [M, K] (only read when dw != NULL); w[k]: A_k [K, N] (only read
- *   when dx != NULL); dy[k]: dY_k [M, N].  At least one of dx, dw is given. */
+ *   when dx != NULL); dy[k]: dY_k [M, N].  At least one of dx, dw, db is
+ *   given; all outputs have dtype out_dtype.                             */
 tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* const* dy,
-                            void* dx, void* const* dw, int p,
+                            void* dx, void* const* dw, void* const* db, int p,
                             int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                             tp_dtype out_dtype, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
@@ -146,22 +153,24 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
 /* Row-parallel backward (no reduction).  [TP §四, §六, §7.1]
  *   dX_k = dY . A_k^T, times GeLU'(H_k) when preact != NULL -> dx[k] [M, K]
  *   dA_k = X_k^T . dY                                        -> dw[k] [K, N]
+ *   db   = sum over the M rows of dY (the bias' gradient)    -> db [N]
  *   x[k]: X_k [M, K] (only read when dw != NULL); w[k]: A_k [K, N];
- *   dy: dY [M, N]; preact[k]: H_k [M, K] bf16 or NULL.                   */
+ *   dy: dY [M, N]; preact[k]: H_k [M, K] bf16 or NULL.  Each of dx, dw,
+ *   db may be NULL, not all three.                                       */
 tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const void* dy,
-                            void* const* dx, void* const* dw, const void* const* preact,
+                            void* const* dx, void* const* dw, void* db, const void* const* preact,
                             int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                             tp_dtype out_dtype, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
 
 /* AllGather+MatMul.  [M027 §01-§02; TP §2.6, §11.3]
- *   Y_k = [X_0; X_1; ...; X_{p-1}] . A_k.  The M-tiles of rank s's rows read
- *   X_s directly, in shard order; the gathered X is written to x_gathered
- *   ([M, K]) only when that pointer is non-NULL.
+ *   Y_k = [X_0; X_1; ...; X_{p-1}] . A_k (+ b_k).  The M-tiles of rank s's
+ *   rows read X_s directly, in shard order; the gathered X is written to
+ *   x_gathered ([M, K]) only when that pointer is non-NULL.
  *   x[s]: X_s [M/p, K]; w[k]: A_k [K, N]; y[k]: [M, N];
- *   epi / preact as in tp_col_linear_fwd.  Requires M % p == 0.           */
-tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* y,
-                       void* x_gathered, tp_epilogue epi, void* const* preact, int p,
+ *   bias / epi / preact as in tp_col_linear_fwd.  Requires M % p == 0.    */
+tp_status tp_ag_matmul(const void* const* x, const void* const* w, const void* const* bias,
+                       void* const* y, void* x_gathered, tp_epilogue epi, void* const* preact, int p,
                        int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                        tp_dtype out_dtype, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
@@ -174,10 +183,12 @@ tp_status tp_ag_matmul(const void* const* x, const void* const* w, void* const* 
  *   dA_k = [X_0; ...; X_{p-1}]^T . dY_k  (contraction over all M tokens; the
  *          row shards X_s are read in place, in shard order)
  *          -> dw[k] [K, N] if dw != NULL
+ *   db_k = sum over the M rows of dY_k -> db[k] [N] if db != NULL
  *   x[s]: X_s [M/p, K] (read when dw != NULL); w[k]: A_k [K, N];
  *   dy[k]: dY_k [M, N].  Requires M % p == 0.                              */
 tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w, const void* const* dy,
-                           void* const* dx, void* const* dw, int p, int64_t M, int64_t N, int64_t K,
+                           void* const* dx, void* const* dw, void* const* db, int p, int64_t M,
+                           int64_t N, int64_t K,
                            int64_t chunk_m, tp_dtype out_dtype, void* ws, size_t ws_bytes,
                            cudaStream_t stream);
 
@@ -187,12 +198,15 @@ tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w, const voi
  *          given (AllGather of the output gradient; the M-tiles of shard s
  *          read dY_s in place) -> dx[r] [M, K] if dx != NULL
  *   dA_r = X_r^T . [dY_0; ...; dY_{p-1}] -> dw[r] [K, N] if dw != NULL
+ *   db   = sum over all rows of dY_0, ..., dY_{p-1}, shard by shard
+ *          -> db [N] if db != NULL
  *   x[r]: X_r [M, K] (read when dw != NULL); w[r]: A_r [K, N];
  *   dy[s]: dY_s [M/p, N]; preact[r]: H_r [M, K] bf16 or NULL.
  *   Requires M % p == 0.                                                    */
 tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const void* const* w,
                                           const void* const* dy, void* const* dx, void* const* dw,
-                                          const void* const* preact, int p, int64_t M, int64_t N,
+                                          void* db, const void* const* preact, int p, int64_t M,
+                                          int64_t N,
                                           int64_t K, int64_t chunk_m, tp_dtype out_dtype, void* ws,
                                           size_t ws_bytes, cudaStream_t stream);
 

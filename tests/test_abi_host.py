@@ -107,8 +107,8 @@ def arr(*ptrs):
     return (ctypes.c_void_p * len(ptrs))(*ptrs)
 
 
-def row_ar(tp, x, w, y, n_out, p, M, N, K, chunk=0, dt=0, ws=B + (1 << 28), wsb=1 << 20):
-    return tp._lib.tp_row_linear_fwd_allreduce(x, w, y, n_out, p, M, N, K, chunk, dt, ws, wsb, None)
+def row_ar(tp, x, w, y, n_out, p, M, N, K, chunk=0, dt=0, ws=B + (1 << 28), wsb=1 << 20, bias=None):
+    return tp._lib.tp_row_linear_fwd_allreduce(x, w, bias, y, n_out, p, M, N, K, chunk, dt, ws, wsb, None)
 
 
 def test_row_ar_argument_checks(tp):
@@ -130,6 +130,9 @@ def test_row_ar_argument_checks(tp):
     assert row_ar(tp, x, w, y, 1, 2, M, N, K, wsb=16) == tp.TP_ERR_WORKSPACE_TOO_SMALL
     # output overlapping an input shard
     assert row_ar(tp, x, w, arr(A + 4096 + 64), 1, 2, M, N, K) == tp.TP_ERR_INVALID_ARG
+    # a misaligned bias, and a bias overlapping the output
+    assert row_ar(tp, x, w, y, 1, 2, M, N, K, bias=A + (1 << 22) + 2) == tp.TP_ERR_ALIGNMENT
+    assert row_ar(tp, x, w, y, 1, 2, M, N, K, bias=A + (1 << 24) + 32) == tp.TP_ERR_INVALID_ARG
     # M == 0: nothing to do, accepted without touching the device
     assert row_ar(tp, x, w, y, 1, 2, 0, N, K) == tp.TP_OK
 
@@ -138,9 +141,9 @@ def test_rs_and_ag_need_m_divisible_by_p(tp):
     x = arr(A, A + 4096, A + 8192)
     w = arr(A + 65536, A + 69632, A + 73728)
     y = arr(B, B + 4096, B + 8192)
-    st = tp._lib.tp_row_linear_fwd_reducescatter(x, w, y, 3, 16, 8, 8, 0, 0, B + (1 << 28), 1 << 20, None)
+    st = tp._lib.tp_row_linear_fwd_reducescatter(x, w, None, y, 3, 16, 8, 8, 0, 0, B + (1 << 28), 1 << 20, None)
     assert st == tp.TP_ERR_UNSUPPORTED_SHAPE
-    st = tp._lib.tp_ag_matmul(x, w, y, None, 0, None, 3, 16, 8, 8, 0, 0, B + (1 << 28), 1 << 20, None)
+    st = tp._lib.tp_ag_matmul(x, w, None, y, None, 0, None, 3, 16, 8, 8, 0, 0, B + (1 << 28), 1 << 20, None)
     assert st == tp.TP_ERR_UNSUPPORTED_SHAPE
 
 
@@ -149,16 +152,22 @@ def test_col_and_bwd_argument_checks(tp):
     y = arr(B, B + 4096)
     ws = B + (1 << 28)
     # bad epilogue for the forward
-    assert tp._lib.tp_col_linear_fwd(A + 65536, w, y, None, 2, 2, 16, 8, 8, 0, 0, ws, 1 << 20, None) \
+    assert tp._lib.tp_col_linear_fwd(A + 65536, w, None, y, None, 2, 2, 16, 8, 8, 0, 0, ws, 1 << 20, None) \
         == tp.TP_ERR_INVALID_ARG
     # GeLU with a preact list holding a null pointer
-    assert tp._lib.tp_col_linear_fwd(A + 65536, w, y, arr(B + 65536, 0), 1, 2, 16, 8, 8, 0, 0, ws,
+    assert tp._lib.tp_col_linear_fwd(A + 65536, w, None, y, arr(B + 65536, 0), 1, 2, 16, 8, 8, 0, 0, ws,
                                      1 << 20, None) == tp.TP_ERR_INVALID_ARG
-    # column backward without dx
-    assert tp._lib.tp_col_linear_bwd(A + 65536, w, arr(A + 131072, A + 135168), None, None, 2, 16, 8, 8,
-                                     0, 0, ws, 1 << 20, None) == tp.TP_ERR_INVALID_ARG
-    # row backward with neither output
-    assert tp._lib.tp_row_linear_bwd(None, w, A + 65536, None, None, None, 2, 16, 8, 8, 0, 0, ws,
+    # a bias list holding a null pointer
+    assert tp._lib.tp_col_linear_fwd(A + 65536, w, arr(A + 98304, 0), y, None, 0, 2, 16, 8, 8, 0, 0, ws,
                                      1 << 20, None) == tp.TP_ERR_INVALID_ARG
+    # column backward with no output at all
+    assert tp._lib.tp_col_linear_bwd(A + 65536, w, arr(A + 131072, A + 135168), None, None, None, 2, 16, 8,
+                                     8, 0, 0, ws, 1 << 20, None) == tp.TP_ERR_INVALID_ARG
+    # row backward with no output at all
+    assert tp._lib.tp_row_linear_bwd(None, w, A + 65536, None, None, None, None, 2, 16, 8, 8, 0, 0, ws,
+                                     1 << 20, None) == tp.TP_ERR_INVALID_ARG
+    # a bias gradient overlapping the output gradient it is summed from
+    assert tp._lib.tp_row_linear_bwd(None, w, A + 65536, None, None, A + 65536 + 64, None, 2, 16, 8, 8, 0,
+                                     0, ws, 1 << 20, None) == tp.TP_ERR_INVALID_ARG
     # status query needs a workspace
     assert tp._lib.tp_get_device_status(None, None) == tp.TP_ERR_INVALID_ARG

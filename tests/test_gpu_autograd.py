@@ -167,6 +167,80 @@ def test_sequence_parallel_layers(ag):
         assert_close(host_f64(mlp.w2[r].grad), ref, False, f"MLP dW2_{r}")
 
 
+def test_mlp_with_biases_plain_and_sequence_parallel(ag):
+    """The MLP block with b1 (split with FC1's columns, before the GeLU) and
+    b2 (added once after the reduction), its bias gradients db1_k = row sums
+    of dH_k and db2 = row sums of dY; then the sequence-parallel module."""
+    import torch
+    p, M, h, ffn = 2, 256, 128, 512
+    nk = ffn // p
+    x = normals((M, h), 75, 0)
+    w1 = normals((h, ffn), 75, 1, 0.05)
+    w2 = normals((ffn, h), 75, 2, 0.05)
+    b1 = normals((ffn,), 75, 3)
+    b2 = normals((h,), 75, 4)
+    g = normals((M, h), 75, 5)
+    w1s = [np.ascontiguousarray(w1[:, k * nk:(k + 1) * nk]) for k in range(p)]
+    w2s = [np.ascontiguousarray(w2[k * nk:(k + 1) * nk]) for k in range(p)]
+    b1s = [np.ascontiguousarray(b1[k * nk:(k + 1) * nk]) for k in range(p)]
+    zr, hr = oracle.col_fwd(x, w1s, apply_gelu=True, biases=b1s)
+    zb = [oracle.round_bf16(a) for a in zr]
+    hb = [oracle.round_bf16(a) for a in hr]
+    dzb = [oracle.round_bf16(a) for a in oracle.row_bwd_dx(w2s, g, preacts=hb)]
+    for sp in (False, True):
+        mlp = ag.ParallelMLP(dev(w1), dev(w2), p, b1=dev(b1), b2=dev(b2), sequence_parallel=sp)
+        if not sp:
+            X = leaf(x)
+            Y = mlp(X)
+            assert_close(host_f64(Y), oracle.row_fwd_allreduce(zb, w2s, bias=b2), False, "Y")
+            Y.backward(dev(g))
+            assert_close(host_f64(X.grad), oracle.col_bwd_dx(w1s, dzb), False, "dX")
+        else:
+            Mp = M // p
+            X = [leaf(np.ascontiguousarray(x[s * Mp:(s + 1) * Mp])) for s in range(p)]
+            Y = mlp(X)
+            ref = oracle.row_fwd_allreduce(zb, w2s, bias=b2)
+            for s in range(p):
+                assert_close(host_f64(Y[s]), ref[s * Mp:(s + 1) * Mp], False, f"Y_{s}")
+            torch.autograd.backward(Y, [dev(np.ascontiguousarray(g[s * Mp:(s + 1) * Mp])) for s in range(p)])
+            dxr = oracle.col_bwd_dx(w1s, dzb)
+            for s in range(p):
+                assert_close(host_f64(X[s].grad), dxr[s * Mp:(s + 1) * Mp], False, f"dX_{s}")
+        assert_close(host_f64(mlp.b2.grad), oracle.bias_grad(g), False, "db2")
+        for k in range(p):
+            assert_close(host_f64(mlp.b1[k].grad), oracle.bias_grad(dzb[k]), False, f"db1_{k}")
+        for k, ref in enumerate(oracle.row_bwd_dw(zb, g)):
+            assert_close(host_f64(mlp.w2[k].grad), ref, False, f"dW2_{k}")
+
+
+def test_linear_modules_with_bias(ag):
+    import torch
+    p, M, h, f = 4, 128, 128, 256
+    x = normals((M, h), 76, 0)
+    w1 = normals((h, f), 76, 1, 0.05)
+    b1 = normals((f,), 76, 2)
+    w2 = normals((f, h), 76, 3, 0.05)
+    b2 = normals((h,), 76, 4)
+    g = normals((M, h), 76, 5)
+    col = ag.ColumnParallelLinear(dev(w1), p, bias=dev(b1))
+    row = ag.RowParallelLinear(dev(w2), p, bias=dev(b2))
+    X = leaf(x)
+    Y = row(list(col(X)))
+    fs = f // p
+    w1s = [np.ascontiguousarray(w1[:, k * fs:(k + 1) * fs]) for k in range(p)]
+    b1s = [np.ascontiguousarray(b1[k * fs:(k + 1) * fs]) for k in range(p)]
+    w2s = [np.ascontiguousarray(w2[k * fs:(k + 1) * fs]) for k in range(p)]
+    hb = [oracle.round_bf16(a) for a in oracle.col_fwd(x, w1s, biases=b1s)[0]]
+    assert_close(host_f64(Y), oracle.row_fwd_allreduce(hb, w2s, bias=b2), False, "Y")
+    Y.backward(dev(g))
+    dhb = [oracle.round_bf16(a) for a in oracle.row_bwd_dx(w2s, g)]
+    assert_close(host_f64(row.bias.grad), oracle.bias_grad(g), False, "db2")
+    for k in range(p):
+        assert_close(host_f64(col.biases[k].grad), oracle.bias_grad(dhb[k]), False, f"db1_{k}")
+    assert_close(host_f64(X.grad), oracle.col_bwd_dx(w1s, dhb), False, "dX")
+    assert torch.is_tensor(Y)
+
+
 def test_rejects_non_bf16(ag):
     import torch
     x = torch.zeros((16, 16), dtype=torch.float32, device="cuda")

@@ -312,6 +312,128 @@ def test_deterministic_and_chunk_invariant(tp):
         assert_close(host_f64(y), ref, False, f"chunk {c}")
 
 
+# ------------------------------------------------------------------ bias epilogues and bias gradients
+
+def ibias(n, seed):
+    return ints((1, n), seed)[0]
+
+
+BIAS_ROW_CASES = [  # p, M, N, K, chunk_m: split-K (second-stage bias), operand-swapped, K == 0
+    (2, 300, 520, 200, 0), (3, 130, 136, 72, 32), (4, 64, 264, 64, 16), (2, 40, 72, 0, 0)]
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K,chunk", BIAS_ROW_CASES)
+def test_row_bias_exact(tp, p, M, N, K, chunk, f32):
+    """Y = sum_r X_r W_r + b (b once, after the reduction), AllReduce with
+    replicas and ReduceScatter."""
+    xs = [ints((M, K), 600 + r) for r in range(p)]
+    ws = [ints((K, N), 610 + r) for r in range(p)]
+    b = ibias(N, 620)
+    ref = oracle.row_fwd_allreduce(xs, ws, bias=b)
+    dx_, dw_ = [dev(a) for a in xs], [dev(c) for c in ws]
+    y = outs([(M, N)] * p, f32)
+    wsp = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, chunk)
+    tp.tp_row_linear_fwd_allreduce(dx_, dw_, [g.t for g in y], wsp, chunk, bias=dev(b))
+    for g in y:
+        check_exact(g, ref, f32)
+    Mr = M - M % p
+    ys = outs([(Mr // p, N)] * p, f32)
+    tp.tp_row_linear_fwd_reducescatter([a[:Mr] for a in dx_], dw_, [g.t for g in ys],
+                                       ws_for(tp, tp.TP_OP_ROW_RS, p, Mr, N, K, chunk), chunk, bias=dev(b))
+    for g, r in zip(ys, oracle.row_fwd_reducescatter([a[:Mr] for a in xs], ws, bias=b)):
+        check_exact(g, r, f32)
+    assert tp.tp_get_device_status(wsp) == tp.TP_OK
+
+
+@pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
+def test_row_bias_direct_epilogue_both_tile_paths(tp, tile_mode):
+    """Enough tiles for no split: the bias is added in the GEMM's own
+    epilogue, on 128x256 tiles and on CTA-pair 256x256 tiles."""
+    p, M, N, K = 2, 2048, 2560, 64
+    xs = [ints((M, K), 630 + r) for r in range(p)]
+    ws = [ints((K, N), 632 + r) for r in range(p)]
+    b = ibias(N, 634)
+    y = outs([(M, N)], True)
+    tp.tp_row_linear_fwd_allreduce([dev(a) for a in xs], [dev(c) for c in ws], [y[0].t],
+                                   ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0), bias=dev(b))
+    check_exact(y[0], oracle.row_fwd_allreduce(xs, ws, bias=b), True)
+
+
+@pytest.mark.parametrize("p,M,N,K,chunk", [(2, 300, 264, 136, 0), (3, 77, 136, 72, 64), (2, 2048, 1280, 64, 0),
+                                           (2, 24, 72, 0, 0)])
+def test_column_and_allgather_bias(tp, p, M, N, K, chunk):
+    """H_k = X A_k + b_k before the GeLU: H exact on integers, GeLU(H) within
+    the fp32 tolerance; the AllGather+MatMul form routes b_k by shard k."""
+    x = ints((M, K), 640)
+    ws = [ints((K, N), 641 + k) for k in range(p)]
+    bs = [ibias(N, 650 + k) for k in range(p)]
+    W, Bs = [dev(c) for c in ws], [dev(c) for c in bs]
+    # GeLU with the pre-activation saved (fp32 outputs, one dtype per call)
+    zr, hr = oracle.col_fwd(x, ws, apply_gelu=True, biases=bs)
+    yf = outs([(M, N)] * p, True)
+    h = outs([(M, N)] * p, True)
+    tp.tp_col_linear_fwd(dev(x), W, [g.t for g in yf], ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, chunk),
+                         epi=tp.TP_EPI_GELU, preact=[g.t for g in h], chunk_m=chunk, bias=Bs)
+    for k in range(p):
+        check_exact(h[k], hr[k], True)
+        yf[k].check_bands()
+        assert_close(host_f64(yf[k].t), zr[k], True, f"GeLU(H_{k})")
+    # no activation, bf16 outputs
+    y = outs([(M, N)] * p, False)
+    tp.tp_col_linear_fwd(dev(x), W, [g.t for g in y], ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, chunk),
+                         chunk_m=chunk, bias=Bs)
+    hplain, _ = oracle.col_fwd(x, ws, biases=bs)
+    for k in range(p):
+        check_exact(y[k], hplain[k], False)
+    # AllGather+MatMul over the row shards of X
+    Mr = M - M % p
+    xs = [np.ascontiguousarray(x[s * (Mr // p):(s + 1) * (Mr // p)]) for s in range(p)]
+    ya = outs([(Mr, N)] * p, True)
+    tp.tp_ag_matmul([dev(a) for a in xs], W, [g.t for g in ya], ws_for(tp, tp.TP_OP_AG_MM, p, Mr, N, K, chunk),
+                    chunk_m=chunk, bias=Bs)
+    yr, _, _ = oracle.ag_matmul(xs, ws, biases=bs)
+    for k in range(p):
+        check_exact(ya[k], yr[k], True)
+
+
+@pytest.mark.parametrize("f32", [True, False])
+@pytest.mark.parametrize("p,M,N,K", [(2, 300, 72, 64), (4, 1024, 264, 136), (3, 96, 520, 72), (2, 0, 136, 64)])
+def test_bias_gradients_exact(tp, p, M, N, K, f32):
+    """db = the row sums of dY on integer inputs (exact in fp32): column
+    backward (one per shard), row backward, AllGather+MatMul backward (with
+    dW in the same call) and the ReduceScatter backward (summed over the
+    token shards in order).  M == 0 gives zeros."""
+    assert M % p == 0
+    Mp = M // p
+    dys = [ints((M, N), 660 + k) for k in range(p)]
+    x = ints((M, K), 680)
+    W = [dev(ints((K, N), 670 + k)) for k in range(p)]
+    DY = [dev(d) for d in dys]
+    db = outs([(N,)] * p, f32)
+    tp.tp_col_linear_bwd(None, W, DY, None, None, ws_for(tp, tp.TP_OP_COL_BWD, p, M, N, K, 0),
+                         db=[g.t for g in db])
+    for g, d in zip(db, dys):
+        check_exact(g, oracle.bias_grad(d), f32)
+    db1 = outs([(N,)], f32)
+    tp.tp_row_linear_bwd(None, W, DY[0], None, None, ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0), db=db1[0].t)
+    check_exact(db1[0], oracle.bias_grad(dys[0]), f32)
+    xs = [np.ascontiguousarray(x[s * Mp:(s + 1) * Mp]) for s in range(p)]
+    dw = outs([(K, N)] * p, f32)
+    db = outs([(N,)] * p, f32)
+    tp.tp_ag_matmul_bwd([dev(a) for a in xs], W, DY, None, [g.t for g in dw],
+                        ws_for(tp, tp.TP_OP_AG_MM_BWD, p, M, N, K, 0), db=[g.t for g in db])
+    for g, d in zip(db, dys):
+        check_exact(g, oracle.bias_grad(d), f32)
+    for g, r in zip(dw, oracle.ag_matmul_bwd_dw(xs, dys)):
+        check_exact(g, r, f32)
+    shards = [np.ascontiguousarray(dys[0][s * Mp:(s + 1) * Mp]) for s in range(p)]
+    dbr = outs([(N,)], f32)
+    tp.tp_row_linear_bwd_reducescatter(None, W, [dev(a) for a in shards], None, None,
+                                       ws_for(tp, tp.TP_OP_ROW_RS_BWD, p, M, N, K, 0), db=dbr[0].t)
+    check_exact(dbr[0], oracle.bias_grad(shards), f32)
+
+
 # ------------------------------------------------------------------ calls from other threads
 
 def test_call_from_a_fresh_thread(tp):
@@ -363,7 +485,7 @@ def test_edge_sizes(tp):
     xk = [torch.empty((5, 0), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     wk = [torch.empty((0, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     yk = torch.full((5, N), 7.0, dtype=torch.bfloat16, device="cuda")
-    st = tp._lib.tp_row_linear_fwd_allreduce(tp._arr(xk), tp._arr(wk), tp._arr([yk]), 1, p, 5, N, 0, 0, 0,
+    st = tp._lib.tp_row_linear_fwd_allreduce(tp._arr(xk), tp._arr(wk), None, tp._arr([yk]), 1, p, 5, N, 0, 0, 0,
                                              tp._ptr(tp.workspace(0, p, 5, N, 0)), 256,
                                              torch.cuda.current_stream().cuda_stream)
     assert st == tp.TP_OK
