@@ -236,14 +236,180 @@ __device__ __forceinline__ void epi_store1(const GemmParams& P, float v, void* o
   else reinterpret_cast<__nv_bfloat16*>(out)[off_out] = __float2bfloat16_rn(v);
 }
 
+// ---------------------------------------------------------------- staged epilogue
+//
+// Each epilogue warp owns 32 accumulator rows (one per lane) and stages one
+// chunk of them at a time in a 4 KiB shared-memory buffer of 32 rows x 128
+// bytes, so that global stores (and the loads of H for GeLU') move whole
+// 128-byte lines: lane l handles 16-byte unit l % U of row l / U (U units
+// per row), instead of one 16-byte piece of each of 32 rows.  Unit u of row r
+// sits at r * 128 + 16 * (u ^ (r % 8)): writing a row per lane and reading a
+// line per 8 lanes are both free of bank conflicts.
+
+constexpr uint32_t STAGE_BYTES_PER_WARP = 32 * 128;
+
+__device__ __forceinline__ uint32_t stg_off(int r, int u) {
+  return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// rows [0, rows_valid) x units [0, units_valid) of the staged chunk -> global
+template <int U>
+__device__ __forceinline__ void stage_store(const uint8_t* stg, uint8_t* dst, int64_t ld_bytes,
+                                            int rows_valid, int units_valid, int lane) {
+  constexpr int RPI = 32 / U;  // rows per instruction
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const int r = k * RPI + lane / U;
+    const int u = lane % U;
+    if (r < rows_valid && u < units_valid)
+      *reinterpret_cast<uint4*>(dst + r * ld_bytes + u * 16) =
+          *reinterpret_cast<const uint4*>(stg + stg_off(r, u));
+  }
+}
+
+// global -> staged chunk (the same footprint); rows or units outside the
+// valid range are left unwritten
+template <int U>
+__device__ __forceinline__ void stage_load(uint8_t* stg, const uint8_t* src, int64_t ld_bytes,
+                                           int rows_valid, int units_valid, int lane) {
+  constexpr int RPI = 32 / U;
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const int r = k * RPI + lane / U;
+    const int u = lane % U;
+    if (r < rows_valid && u < units_valid)
+      *reinterpret_cast<uint4*>(stg + stg_off(r, u)) =
+          *reinterpret_cast<const uint4*>(src + r * ld_bytes + u * 16);
+  }
+}
+
+// This lane's row of a chunk: 8 units of packed values (bf16: 8 per unit,
+// fp32: 4 per unit) into the staging buffer.
+template <bool F32, int NV>
+__device__ __forceinline__ void stage_row(uint8_t* stg, int lane, const float (&v)[NV]) {
+  static_assert(NV == (F32 ? 32 : 64), "one 128-byte row");
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    uint4 q;
+    if (F32) {
+      q = make_uint4(__float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]), __float_as_uint(v[4 * u + 2]),
+                     __float_as_uint(v[4 * u + 3]));
+    } else {
+      q = make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                     pack_bf16x2(v[8 * u + 4], v[8 * u + 5]), pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+    }
+    *reinterpret_cast<uint4*>(stg + stg_off(lane, u)) = q;
+  }
+}
+
+// One chunk of NV columns (128 bytes of output per row) starting at tile
+// column c0: TMEM -> bias -> (H out) -> GeLU / GeLU' -> staged stores.
+template <bool F32>
+__device__ __forceinline__ void drain_chunk_staged(const GemmParams& P, int32_t g, int32_t gi0, int32_t gj0,
+                                                   uint32_t taddr, uint8_t* stg, int lane) {
+  constexpr int NV = F32 ? 32 : 64;
+  constexpr int ESZ = F32 ? 4 : 2;
+  float v[NV];
+  {
+    uint32_t r0[32];
+    tmem_ld_32x32b_x32(taddr, r0);
+    if constexpr (NV == 64) {
+      uint32_t r1[32];
+      tmem_ld_32x32b_x32(taddr + 32, r1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = __uint_as_float(r0[i]);
+        v[32 + i] = __uint_as_float(r1[i]);
+      }
+    } else {
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
+    }
+  }
+  const int rows_valid = min(32, P.rows_g - gi0);
+  const int cols_valid = min(NV, P.cols_g - gj0);     // a multiple of 8 (or <= 0)
+  const int units_valid = cols_valid * ESZ / 16;
+  if (P.bias[g] != nullptr) {
+    const uint16_t* b = static_cast<const uint16_t*>(P.bias[g]) + gj0;
+#pragma unroll
+    for (int i = 0; i < NV; i += 8) {
+      if (i < cols_valid) {
+        const uint4 q = *reinterpret_cast<const uint4*>(b + i);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[i + 2 * k] += bf16_bits_to_f(static_cast<uint16_t>(w[k] & 0xFFFFu));
+          v[i + 2 * k + 1] += bf16_bits_to_f(static_cast<uint16_t>(w[k] >> 16));
+        }
+      }
+    }
+  }
+  if (P.epi == EPI_GELU) {
+    if (P.aux[g] != nullptr) {
+      stage_row<F32>(stg, lane, v);
+      __syncwarp();
+      uint8_t* dst = static_cast<uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * ESZ;
+      stage_store<8>(stg, dst, P.ld_aux * ESZ, rows_valid, units_valid, lane);
+      __syncwarp();
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = gelu_f(v[i]);
+  } else if (P.epi == EPI_DGELU) {
+    // H is bf16: NV * 2 bytes per row
+    constexpr int UH = NV * 2 / 16;
+    const uint8_t* src = static_cast<const uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * 2;
+    stage_load<UH>(stg, src, P.ld_aux * 2, rows_valid, cols_valid * 2 / 16, lane);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < UH; ++u) {
+      const uint4 h = *reinterpret_cast<const uint4*>(stg + stg_off(lane, u));
+      const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[8 * u + 2 * k] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[k] & 0xFFFFu)));
+        v[8 * u + 2 * k + 1] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[k] >> 16)));
+      }
+    }
+    __syncwarp();
+  }
+  stage_row<F32>(stg, lane, v);
+  __syncwarp();
+  for (int rep = 0; rep < P.n_rep; ++rep) {
+    uint8_t* dst = static_cast<uint8_t*>(P.out[g + rep]) + (static_cast<int64_t>(gi0) * P.ld_out + gj0) * ESZ;
+    stage_store<8>(stg, dst, P.ld_out * ESZ, rows_valid, units_valid, lane);
+  }
+  __syncwarp();
+}
+
 // Epilogue of one accumulator for one epilogue warp: columns
 // [half*BN/2, (half+1)*BN/2) of TMEM row `t_row` (this thread's lane), i.e.
 // GEMM row `gi` of group `g`; raw fp32 partials when the launch splits K.
+// With a staging buffer (non-transposed orientation, no split) the output
+// goes through drain_chunk_staged in 128-byte-per-row chunks.
 template <int BN, bool OUT_T>
 __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, int32_t sp, int32_t g,
-                                           int32_t gi, bool row_ok, uint32_t t_row, int half) {
+                                           int32_t gi, bool row_ok, uint32_t t_row, int half,
+                                           uint8_t* stg) {
   constexpr int HALF = BN / 2;
   constexpr int CW = HALF < 32 ? HALF : 32;
+  if constexpr (!OUT_T && HALF % 64 == 0) {
+    if (P.n_split == 1 && stg != nullptr) {
+      const int lane = threadIdx.x & 31;
+      const int32_t gi0 = gi - lane;
+      if (P.out_f32) {
+#pragma unroll 1
+        for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 32)
+          drain_chunk_staged<true>(P, g, gi0, u.nt * BN + c0, t_row + c0, stg, lane);
+      } else {
+#pragma unroll 1
+        for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 64)
+          drain_chunk_staged<false>(P, g, gi0, u.nt * BN + c0, t_row + c0, stg, lane);
+      }
+      return;
+    }
+  }
 #pragma unroll 1
   for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += CW) {
     uint32_t r[32];
@@ -331,8 +497,13 @@ struct GemmCfg {
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
                                       : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static_assert(NUM_BARS * 8 + 16 <= 256, "barriers and the TMEM slot fit in 256 bytes");
+  // epilogue staging (non-transposed outputs): 4 KiB per epilogue warp
+  static constexpr uint32_t STG_OFF = STAGES * STAGE_BYTES + 256;
+  static constexpr uint32_t STG_BYTES = OUT_T ? 0u : NUM_EPI_WARPS * STAGE_BYTES_PER_WARP;
   // +1024 so the ring can be aligned to 1024 bytes inside dynamic smem
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STG_OFF + STG_BYTES;
+  static_assert(SMEM_BYTES <= 232448, "227 KiB of dynamic shared memory per CTA");
   static constexpr int HALF = BN / 2;                 // columns per epilogue warp
   static constexpr int CW = HALF < 32 ? HALF : 32;  // epilogue columns per TMEM load
 };
@@ -516,7 +687,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int32_t sp = t % P.n_split;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      drain_tile<BN, OUT_T>(P, u, sp, g, gi, row_ok, t_row, half);
+      uint8_t* stg = OUT_T ? nullptr
+                           : base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
+      drain_tile<BN, OUT_T>(P, u, sp, g, gi, row_ok, t_row, half, stg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -566,7 +739,10 @@ struct PairCfg {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static_assert(NUM_BARS * 8 + 16 <= 256, "barriers and the TMEM slot fit in 256 bytes");
+  static constexpr uint32_t STG_OFF = STAGES * STAGE_BYTES + 256;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STG_OFF + NUM_EPI_WARPS * STAGE_BYTES_PER_WARP;
+  static_assert(SMEM_BYTES <= 232448, "227 KiB of dynamic shared memory per CTA");
 };
 
 template <bool A_MN, bool B_MN, int BKP>
@@ -765,7 +941,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = gi < P.rows_g;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * Cfg::BN);
-      drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half);
+      uint8_t* stg = base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
+      drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half, stg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
