@@ -488,7 +488,8 @@ def profile_case():
     hh = [torch.empty((M, NK), **bf) for _ in range(P)]
     y = torch.empty((M, H), **bf)
     g = [torch.empty((M, NK), **bf) for _ in range(P)]
-    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, P, M, NK, H, 0), (tp.TP_OP_ROW_AR, P, M, H, NK, 0),
+                             (tp.TP_OP_ROW_BWD, P, M, H, NK, 0)])
     for _ in range(2):
         tp.tp_col_linear_fwd(y, w1, z, ws, epi=tp.TP_EPI_GELU, preact=hh)   # X.W + GeLU
         tp.tp_row_linear_fwd_allreduce(x, w, [y], ws)                         # X.W, fused AllReduce

@@ -83,6 +83,12 @@ struct GemmParams {
   uint64_t timeout_ns;
   int32_t debug_drop_q;      // test hook: CTA 0's producer never arms its k-block number
                              // debug_drop_q (-1: off), so a wait runs out of time
+  // CTA-pair kernel, last partial wave: units t >= tail_start are k-slices,
+  // tail_split per tile, of the tiles tail_start, tail_start + 1, ...
+  int32_t tail_start;
+  int32_t tail_split;        // 1: no slicing
+  float* tail_part;          // fp32 partials of the slices, per (tile, slice, CTA, warp)
+  uint32_t* tail_cnt;        // per (tile, CTA, epilogue warp): slices finished (zero at launch)
 };
 
 struct Unit {
@@ -121,6 +127,25 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& P, int32_t t) {
   u.q0 = sp * P.kb_per_split;
   u.q1 = min(kb_total, u.q0 + P.kb_per_split);
   return u;
+}
+
+// Pair-kernel unit t: a whole tile, or (t >= tail_start) k-slice tk of tail
+// tile tj (tj = -1 for a whole tile).  The slices of a tile split its
+// k-blocks into tail_split contiguous ranges.
+__device__ __forceinline__ Unit decode_pair_unit(const GemmParams& P, int32_t t, int32_t& tj, int32_t& tk) {
+  if (P.tail_split > 1 && t >= P.tail_start) {
+    const int32_t i = t - P.tail_start;
+    tj = i / P.tail_split;
+    tk = i % P.tail_split;
+    Unit u = decode_unit(P, P.tail_start + tj);
+    const int32_t q0 = u.q0, n = u.q1 - u.q0;
+    u.q0 = q0 + tk * n / P.tail_split;
+    u.q1 = q0 + (tk + 1) * n / P.tail_split;
+    return u;
+  }
+  tj = -1;
+  tk = 0;
+  return decode_unit(P, t);
 }
 
 // Bounded wait; false on timeout (latched) or when another role aborted.
@@ -302,32 +327,35 @@ __device__ __forceinline__ void stage_row(uint8_t* stg, int lane, const float (&
   }
 }
 
-// One chunk of NV columns (128 bytes of output per row) starting at tile
-// column c0: TMEM -> bias -> (H out) -> GeLU / GeLU' -> staged stores.
+// NV accumulator columns of this lane's TMEM row starting at taddr.
+template <int NV>
+__device__ __forceinline__ void load_chunk_tmem(uint32_t taddr, float (&v)[NV]) {
+  uint32_t r0[32];
+  tmem_ld_32x32b_x32(taddr, r0);
+  if constexpr (NV == 64) {
+    uint32_t r1[32];
+    tmem_ld_32x32b_x32(taddr + 32, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = __uint_as_float(r0[i]);
+      v[32 + i] = __uint_as_float(r1[i]);
+    }
+  } else {
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
+  }
+}
+
+// One chunk of NV columns (128 bytes of output per row) of the warp's 32
+// rows, starting at group column gj0, values v (this lane's row): bias ->
+// (H out) -> GeLU / GeLU' -> staged stores.
 template <bool F32>
-__device__ __forceinline__ void drain_chunk_staged(const GemmParams& P, int32_t g, int32_t gi0, int32_t gj0,
-                                                   uint32_t taddr, uint8_t* stg, int lane) {
+__device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t g, int32_t gi0, int32_t gj0,
+                                                    float (&v)[F32 ? 32 : 64], uint8_t* stg, int lane) {
   constexpr int NV = F32 ? 32 : 64;
   constexpr int ESZ = F32 ? 4 : 2;
-  float v[NV];
-  {
-    uint32_t r0[32];
-    tmem_ld_32x32b_x32(taddr, r0);
-    if constexpr (NV == 64) {
-      uint32_t r1[32];
-      tmem_ld_32x32b_x32(taddr + 32, r1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = __uint_as_float(r0[i]);
-        v[32 + i] = __uint_as_float(r1[i]);
-      }
-    } else {
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
-    }
-  }
   const int rows_valid = min(32, P.rows_g - gi0);
   const int cols_valid = min(NV, P.cols_g - gj0);     // a multiple of 8 (or <= 0)
   const int units_valid = cols_valid * ESZ / 16;
@@ -383,6 +411,52 @@ __device__ __forceinline__ void drain_chunk_staged(const GemmParams& P, int32_t 
   __syncwarp();
 }
 
+// Sum, in slice order, of the tail partials of this lane's row for NV
+// columns starting at 32-column chunk c32 of the warp's region.
+template <int NV>
+__device__ __forceinline__ void load_chunk_parts(const float4* const* parts, int nparts, int c32, int lane,
+                                                 float (&v)[NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = 0.f;
+  for (int k = 0; k < nparts; ++k) {
+#pragma unroll
+    for (int h = 0; h < NV / 32; ++h) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float4 q = __ldcg(parts[k] + ((c32 + h) * 8 + m) * 32 + lane);
+        float* d = &v[32 * h + 4 * m];
+        if (k == 0) {
+          d[0] = q.x; d[1] = q.y; d[2] = q.z; d[3] = q.w;
+        } else {
+          d[0] += q.x; d[1] += q.y; d[2] += q.z; d[3] += q.w;
+        }
+      }
+    }
+  }
+}
+
+// The warp's 128-column half of a tail tile through the staged epilogue,
+// values summed from the tail partials.
+__device__ __forceinline__ void drain_half_from_parts(const GemmParams& P, int32_t g, int32_t gi0, int32_t gj_half,
+                                                   uint8_t* stg, const float4* const* parts, int nparts) {
+  const int lane = threadIdx.x & 31;
+  if (P.out_f32) {
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      float v[32];
+      load_chunk_parts<32>(parts, nparts, c / 32, lane, v);
+      finish_chunk_staged<true>(P, g, gi0, gj_half + c, v, stg, lane);
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 64) {
+      float v[64];
+      load_chunk_parts<64>(parts, nparts, c / 32, lane, v);
+      finish_chunk_staged<false>(P, g, gi0, gj_half + c, v, stg, lane);
+    }
+  }
+}
+
 // Epilogue of one accumulator for one epilogue warp: columns
 // [half*BN/2, (half+1)*BN/2) of TMEM row `t_row` (this thread's lane), i.e.
 // GEMM row `gi` of group `g`; raw fp32 partials when the launch splits K.
@@ -394,18 +468,24 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
                                            uint8_t* stg) {
   constexpr int HALF = BN / 2;
   constexpr int CW = HALF < 32 ? HALF : 32;
-  if constexpr (!OUT_T && HALF % 64 == 0) {
+  if constexpr (!OUT_T && HALF == 128) {
     if (P.n_split == 1 && stg != nullptr) {
       const int lane = threadIdx.x & 31;
       const int32_t gi0 = gi - lane;
       if (P.out_f32) {
 #pragma unroll 1
-        for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 32)
-          drain_chunk_staged<true>(P, g, gi0, u.nt * BN + c0, t_row + c0, stg, lane);
+        for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 32) {
+          float v[32];
+          load_chunk_tmem<32>(t_row + c0, v);
+          finish_chunk_staged<true>(P, g, gi0, u.nt * BN + c0, v, stg, lane);
+        }
       } else {
 #pragma unroll 1
-        for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 64)
-          drain_chunk_staged<false>(P, g, gi0, u.nt * BN + c0, t_row + c0, stg, lane);
+        for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 64) {
+          float v[64];
+          load_chunk_tmem<64>(t_row + c0, v);
+          finish_chunk_staged<false>(P, g, gi0, u.nt * BN + c0, v, stg, lane);
+        }
       }
       return;
     }
@@ -729,6 +809,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 constexpr int PAIR_BK = 128;  // k-block depth of the pair kernel: 64 KiB stages, fewer round trips
 
+// Epilogue of one k-slice of a tail tile, for one epilogue warp (its 32 rows
+// x 128 columns, half `half` of the CTA's 128 x 256 accumulator):
+//   1. the slice's fp32 accumulator goes to its partial, lane-major (float4
+//      m of 32-column chunk c of lane l at ((c * 8 + m) * 32 + l): every warp
+//      store and load moves 512 contiguous bytes);
+//   2. the warp counts itself finished on its (tile, CTA, warp) counter;
+//   3. the warp that finishes last sums the tail_split partials in slice
+//      order 0, 1, ... (the same order whichever warp is last, so the result
+//      is deterministic), resets the counter, and runs the normal epilogue.
+// No warp waits for another.  Returns after the accumulator has been read.
+__device__ __forceinline__ void drain_tail_slice(const GemmParams& P, const Unit& u, int32_t tj, int32_t tk,
+                                                 uint32_t crank, int32_t g, int32_t gi, uint32_t t_row, int half,
+                                                 int wslot, uint8_t* stg) {
+  const int lane = threadIdx.x & 31;
+  const size_t region = 32 * 32;  // float4 per warp region (32 rows x 128 columns)
+  auto part_of = [&](int32_t k) {
+    return reinterpret_cast<float4*>(P.tail_part) +
+           ((static_cast<size_t>(tj) * P.tail_split + k) * 2 + crank) * (NUM_EPI_WARPS * region) +
+           static_cast<size_t>(wslot) * region;
+  };
+  float4* mine = part_of(tk);
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float v[32];
+    load_chunk_tmem<32>(t_row + half * 128 + c * 32, v);
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      mine[(c * 8 + m) * 32 + lane] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+  }
+  __threadfence();
+  __syncwarp();
+  uint32_t last = 0;
+  if (lane == 0) {
+    uint32_t* cnt = P.tail_cnt + (static_cast<size_t>(tj) * 2 + crank) * NUM_EPI_WARPS + wslot;
+    const uint32_t old = atomicAdd(cnt, 1u);
+    last = old == static_cast<uint32_t>(P.tail_split - 1);
+    if (last) atomicExch(cnt, 0u);
+  }
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (!last) return;
+  __threadfence();
+  const float4* parts[4];
+  for (int k = 0; k < 4; ++k) parts[k] = k < P.tail_split ? part_of(k) : nullptr;
+  drain_half_from_parts(P, g, gi - lane, u.nt * 256 + half * 128, stg, parts, P.tail_split);
+}
+
 template <bool A_MN, bool B_MN, int BKP>
 struct PairCfg {
   static constexpr int BN = 256;                       // pair tile N
@@ -745,7 +871,10 @@ struct PairCfg {
   static_assert(SMEM_BYTES <= 232448, "227 KiB of dynamic shared memory per CTA");
 };
 
-template <bool A_MN, bool B_MN, int BKP>
+// TAIL: the launch runs its last partial wave as k-slices (P.tail_split >
+// 1).  A separate instantiation, so that launches without slices carry none
+// of that code.
+template <bool A_MN, bool B_MN, int BKP, bool TAIL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tp_gemm_pair_kernel(const __grid_constant__ GemmParams P) {
   using Cfg = PairCfg<A_MN, B_MN, BKP>;
@@ -807,7 +936,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int32_t n_issued = 0;
       bool ok = true;
       for (int32_t t = first; t < P.num_units && ok; t += stride) {
-        const Unit u = decode_unit(P, t);
+        int32_t tj = -1, tk = 0;
+        const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
         const int32_t arow = P.a_row_gm * u.gm + u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM;
         const int32_t bcol = P.b_col_gn * u.gn + u.nt * Cfg::BN + static_cast<int32_t>(crank) * Cfg::BNH;
         for (int32_t q = u.q0; q < u.q1; ++q) {
@@ -883,7 +1013,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int32_t t = first; t < P.num_units && ok; t += stride) {
-        const Unit u = decode_unit(P, t);
+        int32_t tj = -1, tk = 0;
+        const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, P, abort_flag, 2u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
@@ -931,7 +1062,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int32_t t = first; t < P.num_units; t += stride) {
-      const Unit u = decode_unit(P, t);
+      int32_t tj = -1, tk = 0;
+      const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
       bool ok = wait_bar(tfull_bar(acc), acc_phase, P, abort_flag, 4u);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
@@ -942,7 +1074,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * Cfg::BN);
       uint8_t* stg = base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
-      drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half, stg);
+      if (TAIL && tj >= 0) drain_tail_slice(P, u, tj, tk, crank, g, gi, t_row, half, warp - 2, stg);
+      else drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half, stg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));

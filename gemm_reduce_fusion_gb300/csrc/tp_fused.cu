@@ -45,6 +45,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 std::atomic<uint64_t> g_timeout_override_ns{0};
 std::atomic<int64_t> g_debug_drop_q{-1};
 std::atomic<int64_t> g_debug_tile_mode{0};  // 0 auto, 1 single-CTA tiles only, 2 CTA pairs whenever possible
+std::atomic<int64_t> g_debug_no_tail{0};    // 1: no k-slices in the last wave of pair launches
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -159,10 +160,10 @@ enum Variant : int {
   V_MM2,       //                           X^T . dY
 };
 
-template <bool A_MN, bool B_MN>
-cudaError_t launch_pair(const GemmParams& P, int clusters, cudaStream_t s) {
+template <bool A_MN, bool B_MN, bool TAIL>
+cudaError_t launch_pair_t(const GemmParams& P, int clusters, cudaStream_t s) {
   using Cfg = PairCfg<A_MN, B_MN, PAIR_BK>;
-  auto k = tp_gemm_pair_kernel<A_MN, B_MN, PAIR_BK>;
+  auto k = tp_gemm_pair_kernel<A_MN, B_MN, PAIR_BK, TAIL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::SMEM_BYTES));
   if (e != cudaSuccess) return e;
@@ -179,7 +180,7 @@ cudaError_t launch_pair(const GemmParams& P, int clusters, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // no more clusters than can be resident at once (persistent tiles)
-  static int max_active[64] = {};
+  static int max_active[64] = {};  // per device and instantiation
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
     if (max_active[dev] == 0) {
@@ -194,6 +195,12 @@ cudaError_t launch_pair(const GemmParams& P, int clusters, cudaStream_t s) {
   e = cudaLaunchKernelEx(&cfg, k, P);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <bool A_MN, bool B_MN>
+cudaError_t launch_pair(const GemmParams& P, int clusters, cudaStream_t s) {
+  return P.tail_split > 1 ? launch_pair_t<A_MN, B_MN, true>(P, clusters, s)
+                          : launch_pair_t<A_MN, B_MN, false>(P, clusters, s);
 }
 
 template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
@@ -243,11 +250,49 @@ struct Shape {
   int64_t m_tiles = 0, n_tiles = 0, units0 = 0, kb_total = 0;
   int n_split = 1;
   int64_t kb_per_split = 0;
+  // CTA pairs: the tiles of a last partial wave run as tail_split k-slices
+  int64_t tail_start = 0;
+  int tail_split = 1;
   bool empty() const { return rows_g == 0 || cols_g == 0; }
+  int64_t tail_tiles() const { return tail_split > 1 ? units0 - tail_start : 0; }
+  size_t tail_cnt_bytes() const {
+    return static_cast<size_t>((tail_tiles() * 2 * NUM_EPI_WARPS * 4 + 255) / 256 * 256);
+  }
   size_t partial_bytes() const {
+    if (tail_split > 1)  // counters, then one fp32 256 x 256 tile per slice
+      return tail_cnt_bytes() + static_cast<size_t>(tail_tiles()) * tail_split * 256 * 256 * 4u;
     return n_split > 1 ? static_cast<size_t>(n_split) * Gm * Gn * rows_g * cols_g * 4u : 0;
   }
 };
+
+// Last partial wave of a CTA-pair launch: W full waves of C = #SM/2
+// clusters leave R = units0 % C tiles for the last wave.  Cutting each of
+// them into s k-slices makes R*s units that finish in ceil(R*s / C) / s of a
+// wave instead of one; take the smallest s (up to 4) with the shortest tail,
+// keeping at least 4 k-blocks per slice.
+void plan_tail(Shape* s) {
+  const int64_t C = kPlanSMs / 2;
+  const int64_t R = s->units0 % C;
+  const int64_t kb_pair = s->S * cdiv(s->kseg, PAIR_BK);
+  if (s->units0 < C || R == 0 || g_debug_no_tail.load() != 0) return;
+  double best = 1.0;
+  int best_s = 1;
+  for (int sp = 2; sp <= 4; ++sp) {
+    if (kb_pair / sp < 4) break;
+    const double t = static_cast<double>(cdiv(R * sp, C)) / sp;
+    if (t < best - 1e-9) {
+      best = t;
+      best_s = sp;
+    }
+  }
+  // slices cost a partial round trip and a heavier end of the launch; take
+  // them where the saving is at least 6 % of the launch (few full waves)
+  const double W = static_cast<double>(s->units0 / C);
+  if (best_s > 1 && (1.0 - best) / (W + 1.0) >= 0.06) {
+    s->tail_split = best_s;
+    s->tail_start = s->units0 - R;
+  }
+}
 
 void finish_shape(Shape* s) {
   s->m_tiles = cdiv(s->rows_g, BM);
@@ -257,6 +302,8 @@ void finish_shape(Shape* s) {
   s->n_split = 1;
   s->kb_per_split = s->kb_total;
   s->pair = false;
+  s->tail_start = 0;
+  s->tail_split = 1;
   if (s->units0 == 0 || s->kb_total == 0) return;
   // 256x256 tiles on CTA pairs when a group has at least 256 rows and the
   // pair tiles still fill the clusters; otherwise 128x256 tiles (with split-K
@@ -271,6 +318,7 @@ void finish_shape(Shape* s) {
       s->m_tiles = pm;
       s->units0 = pu;
       s->chunk_tiles = cdiv(s->chunk_tiles, 2);
+      plan_tail(s);
       return;
     }
   }
@@ -442,7 +490,9 @@ void fill_common(GemmParams* P, const Shape& s) {
   P->kb_per_seg = static_cast<int32_t>(cdiv(s.kseg, s.pair ? PAIR_BK : BK));
   P->n_split = s.n_split;
   P->kb_per_split = static_cast<int32_t>(s.pair ? s.S * P->kb_per_seg : s.kb_per_split);
-  P->num_units = static_cast<int32_t>(s.units0 * s.n_split);
+  P->num_units = static_cast<int32_t>(s.units0 * s.n_split + s.tail_tiles() * (s.tail_split - 1));
+  P->tail_start = static_cast<int32_t>(s.tail_start);
+  P->tail_split = s.tail_split;
   P->rows_g = static_cast<int32_t>(s.rows_g);
   P->cols_g = static_cast<int32_t>(s.cols_g);
   P->n_rep = 1;
@@ -547,6 +597,14 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     return TP_OK;
   }
   if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  if (s.tail_split > 1 && (phases & 1)) {
+    uint8_t* base = static_cast<uint8_t*>(ws) + kStatusBytes;
+    P.tail_cnt = reinterpret_cast<uint32_t*>(base);
+    P.tail_part = reinterpret_cast<float*>(base + s.tail_cnt_bytes());
+    // the slice counters start every launch at zero, whatever an earlier
+    // launch that stopped on a timeout left behind
+    if (cudaMemsetAsync(base, 0, s.tail_cnt_bytes(), stream) != cudaSuccess) return TP_ERR_CUDA;
+  }
   const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
                          : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
   if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
@@ -658,6 +716,10 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_TILE_MODE:
       if (value < 0 || value > 2) return TP_ERR_INVALID_ARG;
       g_debug_tile_mode.store(value);
+      return TP_OK;
+    case TP_DEBUG_NO_TAIL_SLICES:
+      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
+      g_debug_no_tail.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;

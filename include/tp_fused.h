@@ -298,8 +298,16 @@ tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* 
  *     one CTA or 256x256 tiles on a CTA pair; 1 forces single-CTA tiles; 2
  *     uses CTA pairs for every non-swapped launch (parity testing of both
  *     tile paths at small, ragged sizes).
+ *   TP_DEBUG_NO_TAIL_SLICES: 1 runs the last partial wave of a CTA-pair
+ *     launch as whole tiles instead of k-slices; 0 (default) lets the
+ *     planner slice it.
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
-typedef enum { TP_DEBUG_TIMEOUT_MS = 0, TP_DEBUG_DROP_LOAD = 1, TP_DEBUG_TILE_MODE = 2 } tp_debug_key;
+typedef enum {
+  TP_DEBUG_TIMEOUT_MS = 0,
+  TP_DEBUG_DROP_LOAD = 1,
+  TP_DEBUG_TILE_MODE = 2,
+  TP_DEBUG_NO_TAIL_SLICES = 3
+} tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 
 /* Static description of a status code. */

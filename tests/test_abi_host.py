@@ -82,15 +82,25 @@ def test_workspace_size(tp):
     assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 0, 16, 16, 16, 0) == 256
 
 
+def test_workspace_holds_the_last_wave_slices(tp):
+    """bf16 outputs on CTA pairs: 4096 x 4096 is 256 pair tiles, 3 full waves
+    of 76 clusters and 28 tiles cut into 2 k-slices: one fp32 256 x 256 tile
+    per slice, after the slice counters (one per tile, CTA and epilogue warp)."""
+    bf = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0, tp.TP_BF16)
+    assert bf == 256 + 28 * 2 * 8 * 4 + 28 * 2 * 256 * 256 * 4
+    # a whole number of waves (152 tiles) needs no slices
+    assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 2, 4864, 2048, 1024, 0, tp.TP_BF16) == 256
+
+
 def test_fp32_workspace_holds_the_precise_splits(tp):
     """fp32 outputs: no accumulator takes more than 2048 of the contraction.
     p = 4 ranks of K = 4096 (16384 in all) need 8 fp32 copies of Y; a
     contraction of 2048 or less needs none."""
-    bf = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0, tp.TP_BF16)
     f32 = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0, tp.TP_FP32)
-    assert bf == 256
     assert f32 == 256 + 8 * 4096 * 4096 * 4
-    assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 512, 0, tp.TP_FP32) == 256
+    # (a short contraction plans as with bf16 outputs: CTA pairs with last-wave slices)
+    assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 512, 0, tp.TP_FP32) == \
+        tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 512, 0, tp.TP_BF16)
     # column backward with enough tiles to need no split for occupancy: dX
     # contracts over p * N = 8192 (4 splits), dW over M = 4096 (2 splits)
     cb = tp.tp_workspace_size(tp.TP_OP_COL_BWD, 4, 4096, 2048, 2048, 0, tp.TP_FP32)

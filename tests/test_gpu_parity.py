@@ -434,6 +434,101 @@ def test_bias_gradients_exact(tp, p, M, N, K, f32):
     check_exact(dbr[0], oracle.bias_grad(shards), f32)
 
 
+# ------------------------------------------------------------------ last-wave k-slices (CTA pairs)
+#
+# A CTA-pair launch whose tile count leaves a last partial wave of R tiles
+# (R <= half the clusters) runs those tiles as 2-4 k-slices; the warp that
+# finishes a slice last sums the slices in slice order.  Integer inputs:
+# exact, for every epilogue on the slice path.
+
+def test_tail_slices_row_allreduce_and_reducescatter_exact(tp):
+    p, M, N, K = 2, 2048, 2560, 1024      # 80 pair tiles: 4 in the last wave, 4 slices each
+    xs = [ints((M, K), 700 + r) for r in range(p)]
+    ws = [ints((K, N), 702 + r) for r in range(p)]
+    b = ibias(N, 704)
+    X, W = [dev(a) for a in xs], [dev(c) for c in ws]
+    ref = oracle.row_fwd_allreduce(xs, ws, bias=b)
+    for f32 in (True, False):
+        y = outs([(M, N)] * p, f32)
+        tp.tp_row_linear_fwd_allreduce(X, W, [g.t for g in y], ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0),
+                                       bias=dev(b))
+        for g in y:
+            check_exact(g, ref, f32)
+    p, M, N, K = 4, 2048, 2560, 512       # ReduceScatter: groups along M, 80 pair tiles
+    xs = [ints((M, K), 706 + r) for r in range(p)]
+    ws = [ints((K, N), 710 + r) for r in range(p)]
+    ys = outs([(M // p, N)] * p, True)
+    tp.tp_row_linear_fwd_reducescatter([dev(a) for a in xs], [dev(c) for c in ws], [g.t for g in ys],
+                                       ws_for(tp, tp.TP_OP_ROW_RS, p, M, N, K, 0))
+    for g, r in zip(ys, oracle.row_fwd_reducescatter(xs, ws)):
+        check_exact(g, r, True)
+
+
+def test_tail_slices_column_gelu_and_backward_exact(tp):
+    """Ragged M and N inside the sliced tiles: column forward with bias,
+    GeLU and the saved H; row backward with GeLU' (H read back); weight
+    gradients (both operands MN-major)."""
+    p, M, N, K = 4, 1000, 1240, 1024      # 4 x 4 x 5 = 80 pair tiles, 2 slices
+    x = ints((M, K), 720)
+    ws = [ints((K, N), 721 + k) for k in range(p)]
+    bs = [ibias(N, 726 + k) for k in range(p)]
+    y = outs([(M, N)] * p, True)
+    h = outs([(M, N)] * p, True)
+    tp.tp_col_linear_fwd(dev(x), [dev(c) for c in ws], [g.t for g in y], ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, 0),
+                         epi=tp.TP_EPI_GELU, preact=[g.t for g in h], bias=[dev(c) for c in bs])
+    zr, hr = oracle.col_fwd(x, ws, apply_gelu=True, biases=bs)
+    for k in range(p):
+        check_exact(h[k], hr[k], True)
+        y[k].check_bands()
+        assert_close(host_f64(y[k].t), zr[k], True, f"GeLU(H_{k})")
+    # row backward: dX_k = dY W_k^T * GeLU'(H_k); here W_k is [K=1240, N=1024]
+    Kr, Nr = 1240, 1024
+    w2 = [ints((Kr, Nr), 730 + k) for k in range(p)]
+    dy = ints((M, Nr), 735)
+    hb = [synth.normal_bf16((M, Kr), synth.seed_for(61, k)) for k in range(p)]
+    dx = outs([(M, Kr)] * p, True)
+    tp.tp_row_linear_bwd(None, [dev(c) for c in w2], dev(dy), [g.t for g in dx], None,
+                         ws_for(tp, tp.TP_OP_ROW_BWD, p, M, Nr, Kr, 0), preact=[dev(a) for a in hb])
+    for g, r in zip(dx, oracle.row_bwd_dx(w2, dy, preacts=hb)):
+        g.check_bands()
+        assert_close(host_f64(g.t), r, True, "dX * GeLU'")
+    # the same without GeLU': exact
+    dx2 = outs([(M, Kr)] * p, True)
+    tp.tp_row_linear_bwd(None, [dev(c) for c in w2], dev(dy), [g.t for g in dx2], None,
+                         ws_for(tp, tp.TP_OP_ROW_BWD, p, M, Nr, Kr, 0))
+    for g, r in zip(dx2, oracle.row_bwd_dx(w2, dy)):
+        check_exact(g, r, True)
+    # weight gradients dW_k = X_k^T dY: [1240, 1280] per k, 4 x 5 x 5 = 100 pair tiles
+    Mw, Kw, Nw = 1024, 1240, 1280
+    xw = [ints((Mw, Kw), 740 + k) for k in range(p)]
+    dyw = ints((Mw, Nw), 745)
+    ww = [ints((Kw, Nw), 746 + k) for k in range(p)]
+    dw = outs([(Kw, Nw)] * p, True)
+    tp.tp_row_linear_bwd([dev(a) for a in xw], [dev(c) for c in ww], dev(dyw), None, [g.t for g in dw],
+                         ws_for(tp, tp.TP_OP_ROW_BWD, p, Mw, Nw, Kw, 0))
+    for g, r in zip(dw, oracle.row_bwd_dw(xw, dyw)):
+        check_exact(g, r, True)
+
+
+def test_tail_slices_deterministic(tp):
+    """Which warp finishes a slice last changes from run to run; the result
+    does not (normal inputs, fp32 and bf16 outputs)."""
+    import torch
+    p, M, N, K = 2, 2048, 2560, 1024
+    X = [dev(synth.normal_bf16((M, K), synth.seed_for(62, r))) for r in range(p)]
+    W = [dev(synth.normal_bf16((K, N), synth.seed_for(62, 4 + r), 0.02)) for r in range(p)]
+    wsp = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0)
+    for dt in (torch.float32, torch.bfloat16):
+        first = torch.empty((M, N), dtype=dt, device="cuda")
+        tp.tp_row_linear_fwd_allreduce(X, W, [first], wsp)
+        for _ in range(4):
+            again = torch.empty_like(first)
+            tp.tp_row_linear_fwd_allreduce(X, W, [again], wsp)
+            assert torch.equal(first, again)
+    ref = oracle.row_fwd_allreduce([host_bits(a) for a in X], [host_bits(b) for b in W])
+    assert_close(host_f64(first), ref, False, "sliced AllReduce")
+
+
 # ------------------------------------------------------------------ calls from other threads
 
 def test_call_from_a_fresh_thread(tp):
