@@ -244,12 +244,12 @@ class MLPStep:
 
 # which kernel variant each call launches (one launch per call at these sizes)
 CALL_KERNEL = {
-    "col_fwd_gelu": "tp_gemm_pair_kernel<K-major A, MN-major B> (X.W, 256x256 on a CTA pair)",
-    "row_fwd_allreduce": "tp_gemm_pair_kernel<K-major A, MN-major B> (X.W, 256x256 on a CTA pair)",
-    "row_bwd_dx_dgelu": "tp_gemm_pair_kernel<K-major A, K-major B> (dY.W^T, 256x256 on a CTA pair)",
-    "col_bwd_dx": "tp_gemm_pair_kernel<K-major A, K-major B> (dY.W^T, 256x256 on a CTA pair)",
-    "row_bwd_dw": "tp_gemm_pair_kernel<MN-major A, MN-major B> (X^T.dY, 256x256 on a CTA pair)",
-    "col_bwd_dw": "tp_gemm_pair_kernel<MN-major A, MN-major B> (X^T.dY, 256x256 on a CTA pair)",
+    "col_fwd_gelu": "tp_gemm_pair_kernel<0,1,128,0> (X.W, 256x256 tiles on CTA pairs)",
+    "row_fwd_allreduce": "tp_gemm_pair_kernel<0,1,128,1> (X.W, 256x256 tiles on CTA pairs, last wave in k-slices)",
+    "row_bwd_dx_dgelu": "tp_gemm_pair_kernel<0,0,128,0> (dY.W^T, 256x256 tiles on CTA pairs)",
+    "col_bwd_dx": "tp_gemm_pair_kernel<0,0,128,1> (dY.W^T, 256x256 tiles on CTA pairs, last wave in k-slices)",
+    "row_bwd_dw": "tp_gemm_pair_kernel<1,1,128,0> (X^T.dY, 256x256 tiles on CTA pairs)",
+    "col_bwd_dw": "tp_gemm_pair_kernel<1,1,128,0> (X^T.dY, 256x256 tiles on CTA pairs)",
 }
 
 
@@ -292,17 +292,18 @@ def cpu_inputs(tokens):
     return x, w1, w2, dy
 
 
-def cpu_baseline(target_s=10.0):
-    """Time the oracle on a token sample sized for about `target_s` seconds."""
+def cpu_baseline(target_s=12.0):
+    """Time the oracle on a token sample sized for about `target_s` seconds
+    (the sample grows until one timed step takes at least half of that)."""
     tokens = 64
     x, w1, w2, dy = cpu_inputs(M)
-    t0 = time.perf_counter()
-    oracle_step(x[:tokens], w1, w2, dy[:tokens])
-    dt = time.perf_counter() - t0
-    tokens = int(min(M, max(64, tokens * target_s / max(dt, 1e-3))) // 64 * 64)
-    t0 = time.perf_counter()
-    oracle_step(x[:tokens], w1, w2, dy[:tokens])
-    dt = time.perf_counter() - t0
+    while True:
+        t0 = time.perf_counter()
+        oracle_step(x[:tokens], w1, w2, dy[:tokens])
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 2 or tokens >= M:
+            break
+        tokens = int(min(M, max(2 * tokens, tokens * target_s / max(dt, 1e-3))) // 64 * 64)
     flops = STEP_FLOPS * tokens / M
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"one MLP fwd+bwd step over {tokens} of the {M} tokens with the full weights "
@@ -470,7 +471,8 @@ def run_ours(args):
 def profile_case():
     """Each kernel variant of the step at the step's shapes (about 1 GB
     resident), a bounded case for ncu captures.  Launch order:
-    [col fwd + GeLU (X.W), row fwd AllReduce (X.W), row bwd dX (dY.W^T)] x 2,
+    [col fwd + GeLU (X.W), row fwd AllReduce (X.W, last wave in k-slices),
+    row bwd dX (dY.W^T), col bwd fused dX (dY.W^T, last wave in k-slices)] x 2,
     then row bwd dW (X^T.dY) x 2."""
     import torch
     import gemm_reduce_fusion_gb300 as tp
@@ -489,11 +491,13 @@ def profile_case():
     y = torch.empty((M, H), **bf)
     g = [torch.empty((M, NK), **bf) for _ in range(P)]
     ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, P, M, NK, H, 0), (tp.TP_OP_ROW_AR, P, M, H, NK, 0),
-                             (tp.TP_OP_ROW_BWD, P, M, H, NK, 0)])
+                             (tp.TP_OP_ROW_BWD, P, M, H, NK, 0), (tp.TP_OP_COL_BWD, P, M, NK, H, 0)])
+    dx = torch.empty((M, H), **bf)
     for _ in range(2):
         tp.tp_col_linear_fwd(y, w1, z, ws, epi=tp.TP_EPI_GELU, preact=hh)   # X.W + GeLU
         tp.tp_row_linear_fwd_allreduce(x, w, [y], ws)                         # X.W, fused AllReduce
         tp.tp_row_linear_bwd(None, w, y, g, None, ws)                         # dY.W^T
+        tp.tp_col_linear_bwd(None, w1, g, dx, None, ws)                       # dY.W^T, fused dX
     wgrad = [torch.empty((NK, H), **bf) for _ in range(P)]
     for _ in range(2):
         tp.tp_row_linear_bwd(x, w, y, None, wgrad, ws)                        # X^T.dY
@@ -543,7 +547,8 @@ def workloads(torch, tp):
         DW2 = [torch.empty((nk, h), **bf) for _ in range(p)]
         DX = torch.empty((M, h), **bf)
         DW1 = [torch.empty((h, nk), **bf) for _ in range(p)]
-        ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_BWD, p, M, h, nk, 0)])
+        ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_AR, p, M, h, nk, 0),
+                                 (tp.TP_OP_ROW_BWD, p, M, h, nk, 0), (tp.TP_OP_COL_BWD, p, M, nk, h, 0)])
         return dict(calls=[
             ("col_fwd_gelu", lambda: tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
             ("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(Z, d["w2"], [Y], ws)),
@@ -754,7 +759,8 @@ def run_precision_report(args):
         p = len(xs)
         M, K = xs[0].shape
         N = wsh[0].shape[1]
-        calls = [(tp.TP_OP_ROW_AR, p, M, N, K, 0, tp.TP_FP32), (tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, 0)]
+        calls = [(tp.TP_OP_ROW_AR, p, M, N, K, 0, tp.TP_FP32), (tp.TP_OP_ROW_AR, p, M, N, K, 0),
+                 (tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, 0)]
         w_ = ws(calls)
         ref = torch.empty((M, N), dtype=torch.float32, device="cuda")
         tp.tp_row_linear_fwd_allreduce(xs, wsh, [ref], w_)
@@ -784,7 +790,8 @@ def run_precision_report(args):
     Z = [torch.empty((M, nk), **bf) for _ in range(p)]
     Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
     w0 = ws([(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_BWD, p, M, h, nk, 0, tp.TP_FP32),
-             (tp.TP_OP_COL_BWD, p, M, nk, h, 0, tp.TP_FP32)])
+             (tp.TP_OP_COL_BWD, p, M, nk, h, 0, tp.TP_FP32), (tp.TP_OP_ROW_BWD, p, M, h, nk, 0),
+             (tp.TP_OP_COL_BWD, p, M, nk, h, 0)])
     tp.tp_col_linear_fwd(d["x"], d["w1"], Z, w0, epi=tp.TP_EPI_GELU, preact=Hh)
     row_layer("MLP FC2 forward (p=4, 4096 tokens, h=4096, ffn=16384)", Z, d["w2"])
     # gradients: bf16 results of the fused backward vs its fp32-output results
