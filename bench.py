@@ -472,7 +472,8 @@ def profile_case():
     """Each kernel variant of the step at the step's shapes (about 1 GB
     resident), a bounded case for ncu captures.  Launch order:
     [col fwd + GeLU (X.W), row fwd AllReduce (X.W, last wave in k-slices),
-    row bwd dX (dY.W^T), col bwd fused dX (dY.W^T, last wave in k-slices)] x 2,
+    row bwd dX with GeLU' (dY.W^T), col bwd fused dX (dY.W^T, last wave in
+    k-slices)] x 2,
     then row bwd dW (X^T.dY) x 2."""
     import torch
     import gemm_reduce_fusion_gb300 as tp
@@ -496,7 +497,7 @@ def profile_case():
     for _ in range(2):
         tp.tp_col_linear_fwd(y, w1, z, ws, epi=tp.TP_EPI_GELU, preact=hh)   # X.W + GeLU
         tp.tp_row_linear_fwd_allreduce(x, w, [y], ws)                         # X.W, fused AllReduce
-        tp.tp_row_linear_bwd(None, w, y, g, None, ws)                         # dY.W^T
+        tp.tp_row_linear_bwd(None, w, y, g, None, ws, preact=hh)              # dY.W^T * GeLU'(H)
         tp.tp_col_linear_bwd(None, w1, g, dx, None, ws)                       # dY.W^T, fused dX
     wgrad = [torch.empty((NK, H), **bf) for _ in range(P)]
     for _ in range(2):

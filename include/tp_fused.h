@@ -36,15 +36,19 @@
  *    chunk (rounded up to a multiple of 16).
  *  - Outputs must not overlap inputs (checked; TP_ERR_INVALID_ARG).
  *  - `ws` is a device workspace of at least tp_workspace_size(...) bytes,
- *    16-byte aligned.  It holds the device status word and, for the split-K
- *    path, fp32 partials.  Calls that share a workspace must be ordered
- *    on the same stream.
+ *    16-byte aligned, zero-filled before its first use.  It holds the
+ *    device status word (which stays zero unless a device wait times out)
+ *    and, when a launch needs them, fp32 partials: split-K partials, or the
+ *    k-slices of the last partial wave of a CTA-pair launch together with
+ *    their counters (which the library clears before each such launch).
+ *    Calls that share a workspace must be ordered on the same stream.
  *  - Errors: argument checks run on the host before anything is enqueued
  *    and return a tp_status; on error nothing is launched.  A device-side
  *    wait that runs out of time latches TP_ERR_DEVICE_TIMEOUT into the
  *    workspace status word; tp_get_device_status() reads (and clears) it.
  *  - Determinism: identical inputs give bitwise-identical outputs.
- *  - Degenerate sizes: M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *  - Degenerate sizes: M == 0 or N == 0 is a no-op; K == 0 writes the
+ *    epilogue of a zero product (zeros, or the bias and its activation).
  */
 #ifndef TP_FUSED_H_
 #define TP_FUSED_H_
@@ -276,7 +280,9 @@ tp_status tp_get_device_status(void* ws, cudaStream_t stream);
  *  - All calls on a device share the one array.  Calls that may overlap on
  *    the GPU (different streams without ordering between them) race on it;
  *    order them on one stream.  Nothing in the array has to start at zero:
- *    every partial a call reads was written earlier by that same call.
+ *    every partial a call reads was written earlier by that same call, and
+ *    slice counters are cleared (cudaMemsetAsync, no allocation) before the
+ *    launch that uses them.
  *  - Device-side timeouts are latched in the array but not reported; use
  *    tp_row_linear_fwd_allreduce with a workspace to read them.            */
 #define TP_NOALLOC_SCRATCH_BYTES (16u << 20)
