@@ -741,8 +741,11 @@ int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K) {
   if (M <= 0) return 0;
   if (p < 1) p = 1;
   // Model constants: dense bf16 tensor rate and HBM copy rate of a GB300,
-  // and the L2 capacity below which a weight set is streamed once per call.
-  const double peak = 1.9e15, bw = 6.7e12, l2 = 96.0 * (1 << 20);
+  // and the weight-set size below which the weights stay in L2 from one
+  // chunk to the next: half of the 129 MB L2, since the activations, the
+  // outputs and the other half of each wave's operands share it (a 100 MB
+  // weight set re-read per 512-row chunk cost the QKV projection 8 %).
+  const double peak = 1.9e15, bw = 6.7e12, l2 = 48.0 * (1 << 20);
   double flops = 0, wbytes = 0, in_row = 0, out_row = 0;
   switch (op) {
     case TP_OP_ROW_AR: case TP_OP_ROW_RS:
