@@ -704,6 +704,7 @@ def run_sweep(args):
     ws = _ws_for(torch, tp, [(op, p, M, n, k, c) for c in chunks for op, n, k in
                              [(tp.TP_OP_COL_FWD, nk, h), (tp.TP_OP_ROW_AR, h, nk), (tp.TP_OP_ROW_AR_UNFUSED, h, nk)]])
     tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)
+    measured = []   # (chunk_m, c, m, fused FC2 ms)
     for c in chunks:
         n = tp.tp_num_chunks(M, c)
         fc1, _, _, _ = _time_calls(torch, [("f", lambda: tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU,
@@ -722,6 +723,13 @@ def run_sweep(args):
                           "fc2_model_pipelined_ms": tp.tp_pipeline_time(cm, mm, n),
                           "fc2_model_serial_ms": n * (cm + mm),
                           "fc2_unfused_whole_ms": full_unfused}), flush=True)
+        measured.append((c, cm, mm, fc2))
+    pick = tp.tp_choose_chunk_m_measured(M, [r[0] for r in measured], [r[1] for r in measured],
+                                         [r[2] for r in measured])
+    fastest = min(measured, key=lambda r: r[3])[0]
+    print(json.dumps({"sweep": "GPT-3-scale FC pair, p=8, M=2048", "chunk_m_from_measured_c_m": pick,
+                      "chunk_m_scheduler_model": tp.tp_choose_chunk_m(tp.TP_OP_ROW_AR, p, M, h, nk),
+                      "chunk_m_fastest_fused_fc2": fastest}), flush=True)
 
 
 def _err_stats(torch, got, ref):

@@ -85,6 +85,8 @@ def _load() -> ctypes.CDLL:
         "tp_pipeline_time": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, L]),
         "tp_num_chunks": (L, [L, L]),
         "tp_choose_chunk_m": (L, [I, I, L, L, L]),
+        "tp_choose_chunk_m_measured": (L, [L, ctypes.POINTER(L), ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double), I]),
         "tp_get_device_status": (I, [P, P]),
         "tp_status_string": (ctypes.c_char_p, [I]),
         "tp_debug_set": (I, [I, L]),
@@ -174,6 +176,15 @@ def tp_num_chunks(M: int, chunk_m: int) -> int:
 
 def tp_choose_chunk_m(op: int, p: int, M: int, N: int, K: int) -> int:
     return int(_lib.tp_choose_chunk_m(op, p, M, N, K))
+
+
+def tp_choose_chunk_m_measured(M: int, chunks: Sequence[int], c: Sequence[float], m: Sequence[float]) -> int:
+    """The candidate chunk_m whose timeline from measured per-chunk c and m is shortest."""
+    n = len(chunks)
+    if not (len(c) == len(m) == n):
+        raise ValueError("one c and one m per candidate chunk")
+    return int(_lib.tp_choose_chunk_m_measured(M, (ctypes.c_int64 * n)(*chunks), (ctypes.c_double * n)(*c),
+                                               (ctypes.c_double * n)(*m), n))
 
 
 def workspace(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0, device="cuda",

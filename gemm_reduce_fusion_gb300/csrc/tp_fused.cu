@@ -294,6 +294,9 @@ void plan_tail(Shape* s) {
   }
 }
 
+// Planner option for one call: last-wave slices allowed (the default) or not.
+thread_local bool t_plan_tails = true;
+
 void finish_shape(Shape* s) {
   s->m_tiles = cdiv(s->rows_g, BM);
   s->n_tiles = cdiv(s->cols_g, s->bn);
@@ -318,7 +321,7 @@ void finish_shape(Shape* s) {
       s->m_tiles = pm;
       s->units0 = pu;
       s->chunk_tiles = cdiv(s->chunk_tiles, 2);
-      plan_tail(s);
+      if (t_plan_tails) plan_tail(s);
       return;
     }
   }
@@ -461,6 +464,20 @@ size_t workspace_for(const std::vector<Shape>& shapes) {
   size_t need = 0;
   for (const Shape& s : shapes) need = std::max(need, s.partial_bytes());
   return kStatusBytes + need;
+}
+
+// The launches of a call for a workspace of ws_bytes: the fastest plan, or,
+// when the workspace is too small for its last-wave slices, the same plan
+// without them (which then needs no more than the smaller workspace, or the
+// call fails the workspace check).
+std::vector<Shape> plan_call(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m, tp_dtype dt,
+                             size_t ws_bytes) {
+  std::vector<Shape> v = op_shapes(op, p, M, N, K, chunk_m, dt);
+  if (workspace_for(v) <= ws_bytes) return v;
+  t_plan_tails = false;
+  std::vector<Shape> w = op_shapes(op, p, M, N, K, chunk_m, dt);
+  t_plan_tails = true;
+  return workspace_for(w) <= ws_bytes ? w : v;
 }
 
 // ------------------------------------------------------------------ launching a plan
@@ -789,6 +806,22 @@ int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K) {
   return std::min(best, M);
 }
 
+int64_t tp_choose_chunk_m_measured(int64_t M, const int64_t* chunk, const double* c, const double* m,
+                                   int n) {
+  if (n <= 0 || M <= 0 || chunk == nullptr || c == nullptr || m == nullptr) return 0;
+  int64_t best = 0;
+  double best_t = 0.0;
+  for (int i = 0; i < n; ++i) {
+    if (chunk[i] <= 0) continue;
+    const double t = tp_pipeline_time(c[i], m[i], tp_num_chunks(M, chunk[i]));
+    if (best == 0 || t < best_t) {
+      best = chunk[i];
+      best_t = t;
+    }
+  }
+  return best;
+}
+
 size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                          tp_dtype out_dtype) {
   if (p < 1 || p > kMaxP || M < 0 || N < 0 || K < 0 || chunk_m < 0) return kStatusBytes;
@@ -829,7 +862,7 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   TP_TRY(check_ptrs(const_cast<const void* const*>(y), n_out, work));
   TP_TRY(check_ptr(bias, work && bias != nullptr));
   const tp_op op = rs ? TP_OP_ROW_RS : TP_OP_ROW_AR;
-  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m, dt);
+  std::vector<Shape> shapes = plan_call(op, p, M, N, K, chunk_m, dt, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   if (!work) return TP_OK;
   const int64_t Mp = M / p;
@@ -919,7 +952,7 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
   TP_TRY(check_ptr(x_gathered, x_gathered != nullptr));
   TP_TRY(check_ptrs(bias, p, work && bias != nullptr));
   const tp_op op = ag ? TP_OP_AG_MM : TP_OP_COL_FWD;
-  std::vector<Shape> shapes = op_shapes(op, p, M, N, K, chunk_m, dt);
+  std::vector<Shape> shapes = plan_call(op, p, M, N, K, chunk_m, dt, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   const int64_t Mp = M / p;
   {
@@ -1069,7 +1102,7 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
   TP_TRY(check_ptrs(const_cast<const void* const*>(db), p, db_work));
   TP_TRY(check_ptr(x, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
-  std::vector<Shape> shapes = op_shapes(TP_OP_COL_BWD, p, M, N, K, chunk_m, out_dtype);
+  std::vector<Shape> shapes = plan_call(TP_OP_COL_BWD, p, M, N, K, chunk_m, out_dtype, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1135,7 +1168,7 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
-  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_BWD, p, M, N, K, chunk_m, out_dtype);
+  std::vector<Shape> shapes = plan_call(TP_OP_ROW_BWD, p, M, N, K, chunk_m, out_dtype, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1214,7 +1247,7 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
   TP_TRY(check_ptrs(const_cast<const void* const*>(db), p, db_work));
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
-  std::vector<Shape> shapes = op_shapes(TP_OP_AG_MM_BWD, p, M, N, K, chunk_m, out_dtype);
+  std::vector<Shape> shapes = plan_call(TP_OP_AG_MM_BWD, p, M, N, K, chunk_m, out_dtype, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1311,7 +1344,7 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
   TP_TRY(check_ptrs(x, p, dw_work && M > 0));
   TP_TRY(check_ptrs(const_cast<const void* const*>(dw), p, dw_work));
   TP_TRY(check_ptrs(preact, p, dx_work && preact != nullptr));
-  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_RS_BWD, p, M, N, K, chunk_m, out_dtype);
+  std::vector<Shape> shapes = plan_call(TP_OP_ROW_RS_BWD, p, M, N, K, chunk_m, out_dtype, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   {
     std::vector<Range> ins, outs;
@@ -1415,7 +1448,7 @@ extern "C" tp_status tp_row_linear_fwd_unfused(const void* const* x, const void*
   TP_TRY(check_ptrs(x, p, work && K > 0));
   TP_TRY(check_ptrs(w, p, work && K > 0));
   TP_TRY(check_ptr(y, work));
-  std::vector<Shape> shapes = op_shapes(TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk_m, out_dtype);
+  std::vector<Shape> shapes = plan_call(TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk_m, out_dtype, ws_bytes);
   TP_TRY(check_ws(ws, ws_bytes, workspace_for(shapes)));
   if (!work) return TP_OK;
   {
@@ -1497,7 +1530,8 @@ extern "C" tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, c
                                                          int64_t chunk_m, tp_dtype out_dtype,
                                                          cudaStream_t stream) {
   TP_TRY(check_sizes(p, M, N, K, chunk_m, out_dtype));
-  if (workspace_for(op_shapes(TP_OP_ROW_AR, p, M, N, K, chunk_m, out_dtype)) > TP_NOALLOC_SCRATCH_BYTES)
+  if (workspace_for(plan_call(TP_OP_ROW_AR, p, M, N, K, chunk_m, out_dtype, TP_NOALLOC_SCRATCH_BYTES)) >
+      TP_NOALLOC_SCRATCH_BYTES)
     return TP_ERR_WORKSPACE_TOO_SMALL;
   if (M == 0 || N == 0) return TP_OK;
   void* scratch = nullptr;

@@ -41,6 +41,9 @@
  *    and, when a launch needs them, fp32 partials: split-K partials, or the
  *    k-slices of the last partial wave of a CTA-pair launch together with
  *    their counters (which the library clears before each such launch).
+ *    tp_workspace_size() is the size of the fastest plan; a smaller
+ *    workspace that still holds the plan without last-wave slices is
+ *    accepted, and the call then runs without them.
  *    Calls that share a workspace must be ordered on the same stream.
  *  - Errors: argument checks run on the host before anything is enqueued
  *    and return a tp_status; on error nothing is launched.  A device-side
@@ -252,6 +255,17 @@ int64_t tp_num_chunks(int64_t M, int64_t chunk_m);
  * reduced rows.  Host only; never fails (returns >= 1, or 0 when M <= 0). */
 int64_t tp_choose_chunk_m(tp_op op, int p, int64_t M, int64_t N, int64_t K);
 
+/* The chunk size to use given MEASURED per-chunk times.  [M027 §03-§04:
+ * try candidate chunkings, measure the small-chunk compute and
+ * communication, pick the shortest timeline]
+ *   chunk[i], c[i], m[i] for i < n: a candidate chunk_m and the measured
+ *   compute and communication time of one of its chunks (any time unit).
+ *   Returns the candidate whose tp_pipeline_time(c, m, ceil(M / chunk))
+ *   is smallest (the first one on ties), or 0 when n <= 0, M <= 0, or a
+ *   pointer is NULL.  Host only.                                         */
+int64_t tp_choose_chunk_m_measured(int64_t M, const int64_t* chunk, const double* c, const double* m,
+                                   int n);
+
 /* Synchronises `stream`, returns the latched device status of `ws`
  * (TP_OK or TP_ERR_DEVICE_TIMEOUT) and clears it.                         */
 tp_status tp_get_device_status(void* ws, cudaStream_t stream);
@@ -270,9 +284,8 @@ tp_status tp_get_device_status(void* ws, cudaStream_t stream);
  * TP_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library holds
  * until the process exits.
  *
- *  - A call whose scratch need (tp_workspace_size(TP_OP_ROW_AR, ...,
- *    out_dtype))
- *    exceeds TP_NOALLOC_SCRATCH_BYTES is rejected with
+ *  - A call that needs more scratch than TP_NOALLOC_SCRATCH_BYTES, even
+ *    without last-wave slices (see `ws` above), is rejected with
  *    TP_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call

@@ -33,6 +33,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["tp_row_linear_fwd_allreduce", "tp_row_linear_fwd_reducescatter", "tp_col_linear_fwd",
               "tp_col_linear_bwd", "tp_ag_matmul", "tp_row_linear_bwd", "tp_workspace_size",
+              "tp_choose_chunk_m_measured",
               "tp_pipeline_time", "tp_choose_chunk_m", "tp_get_device_status", "tp_status_string"]:
         assert n in names
 
@@ -71,6 +72,21 @@ def test_choose_chunk_m_is_valid(tp):
             assert 1 <= c <= M
     assert tp.tp_choose_chunk_m(0, 2, 0, 8, 8) == 0
     assert tp.tp_choose_chunk_m(tp.TP_OP_COL_FWD, 8, 16, 6144, 12288) == 16
+
+
+def test_choose_chunk_m_from_measured_times(tp):
+    """The page's two-engine example: M = 128 in 4 chunks of 32 with c = 3,
+    m = 2 gives 14 against 20 unchunked (c = 12, m = 8 for one chunk of
+    128); the shortest timeline wins, checked against the oracle's closed
+    form."""
+    chunks, c, m = [128, 32], [12.0, 3.0], [8.0, 2.0]
+    assert tp.tp_choose_chunk_m_measured(128, chunks, c, m) == 32
+    ts = [oracle.pipeline_time(ci, mi, oracle.n_chunks(128, k)) for k, ci, mi in zip(chunks, c, m)]
+    assert ts == [20.0, 14.0]
+    # small chunks whose compute no longer shrinks lose (the page's warning)
+    assert tp.tp_choose_chunk_m_measured(128, [128, 16], [12.0, 3.0], [8.0, 2.0]) == 128
+    assert tp.tp_choose_chunk_m_measured(128, [], [], []) == 0
+    assert tp.tp_choose_chunk_m_measured(0, [32], [1.0], [1.0]) == 0
 
 
 def test_workspace_size(tp):

@@ -510,6 +510,32 @@ def test_tail_slices_column_gelu_and_backward_exact(tp):
         check_exact(g, r, True)
 
 
+def test_workspace_without_room_for_slices_runs_whole_tiles(tp):
+    """A workspace smaller than tp_workspace_size() but large enough for the
+    plan without last-wave slices is accepted: same result bit for bit on
+    integer inputs, and a workspace below that is still rejected."""
+    import torch
+    p, M, N, K = 2, 2048, 2560, 1024
+    xs = [ints((M, K), 750 + r) for r in range(p)]
+    ws = [ints((K, N), 752 + r) for r in range(p)]
+    X, W = [dev(a) for a in xs], [dev(c) for c in ws]
+    full = tp.tp_workspace_size(tp.TP_OP_ROW_AR, p, M, N, K, 0)
+    assert full > 256
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    y = outs([(M, N)], True)
+    tp.tp_row_linear_fwd_allreduce(X, W, [y[0].t], small)
+    check_exact(y[0], oracle.row_fwd_allreduce(xs, ws), True)
+    assert tp.tp_get_device_status(small) == tp.TP_OK
+    # a skinny call that needs split-K partials even without slices
+    p, M, N, K = 8, 16, 2048, 1024
+    x8 = [dev(ints((M, K), 760 + r)) for r in range(p)]
+    w8 = [dev(ints((K, N), 770 + r)) for r in range(p)]
+    y8 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_row_linear_fwd_allreduce(x8, w8, [y8], small, chunk_m=16)
+    assert e.value.status == tp.TP_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_tail_slices_deterministic(tp):
     """Which warp finishes a slice last changes from run to run; the result
     does not (normal inputs, fp32 and bf16 outputs)."""
