@@ -56,7 +56,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=100,
+                    help="steps of the end-to-end run (host buffers, copies overlapped with compute)")
     ap.add_argument("--sweep", action="store_true",
                     help="chunk_m sweep of the GPT-3-scale FC pair: fused time vs the timeline model")
     ap.add_argument("--configs", action="store_true",
@@ -66,6 +67,8 @@ def parse():
                     help="0: planner chooses 128x256 or CTA-pair 256x256 tiles; 1: 128x256 only; 2: pairs")
     ap.add_argument("--profile-case", action="store_true",
                     help="run each GEMM variant of the step twice at the step's shapes (for ncu)")
+    ap.add_argument("--trace", action="store_true",
+                    help="per-chunk timeline of single fused launches (the two-engine timeline, measured)")
     ap.add_argument("--precision-report", action="store_true",
                     help="output error of the fused path vs the unfused baseline with fp32 or bf16 collectives")
     return ap.parse_args()
@@ -849,6 +852,87 @@ def run_precision_report(args):
     row_layer("GPT-3-scale FC2 forward (p=8, M=2048, K_r=6144, N=12288)", Z, d["w2"])
 
 
+def _trace_launch(torch, tp, fn, cap=1 << 16):
+    """Run fn() once with the timeline trace on; per-unit records, time-ordered."""
+    buf = torch.zeros((cap, 4), dtype=torch.int64, device="cuda")
+    fn()                                   # warm: tensor maps, caches
+    torch.cuda.synchronize()
+    buf.zero_()
+    tp.tp_trace_set(buf, cap)
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        tp.tp_trace_set(None)
+    rec = [tuple(int(v) for v in r) for r in buf.cpu().tolist() if r[0] != 0]
+    return rec
+
+
+def _timeline(rec):
+    """Per-chunk compute and drain windows of one traced launch ([M027] §03:
+    compute c and communication m per chunk; here c is the chunk's MMA
+    window and m the drain after its last accumulator completes) and the
+    share of drain time that overlapped later MMAs on the same CTA/cluster."""
+    t0 = min(r[0] for r in rec)
+    chunks = {}
+    for start, full, drained, tag in rec:
+        chunks.setdefault(tag >> 32, []).append((start, full, drained))
+    per = []
+    for ch in sorted(chunks):
+        u = chunks[ch]
+        c0, c1 = min(x[0] for x in u), max(x[1] for x in u)
+        d1 = max(x[2] for x in u)
+        per.append({"chunk": ch, "mma_us": [round((c0 - t0) / 1e3, 2), round((c1 - t0) / 1e3, 2)],
+                    "drained_us": round((d1 - t0) / 1e3, 2), "c_us": round((c1 - c0) / 1e3, 2),
+                    "m_us": round((d1 - c1) / 1e3, 2)})
+    by_who = {}
+    for start, full, drained, tag in rec:
+        by_who.setdefault(tag & 0xFFFFFFFF, []).append((start, full, drained))
+    drain = over = 0
+    for units in by_who.values():
+        units.sort()
+        for a, b in zip(units, units[1:] + [None]):
+            drain += a[2] - a[1]
+            if b is not None:
+                over += max(0, min(a[2], b[1]) - max(a[1], b[0]))
+    total = (max(r[2] for r in rec) - t0) / 1e3
+    return per, total, (over / drain if drain else 0.0)
+
+
+def run_trace(args):
+    """Measured chunk timelines of single fused launches beside the pages'
+    model T = c + (n-1) max(c, m) + m built from the measured c and m."""
+    import torch
+    torch.cuda.set_device(0)
+    import gemm_reduce_fusion_gb300 as tp
+    import synth
+    cases = []
+    d1 = _dev_all(torch, synth.config1_inputs())
+    y1 = torch.empty((128, 2048), dtype=torch.bfloat16, device="cuda")
+    ws1 = _ws_for(torch, tp, [(tp.TP_OP_ROW_AR, 2, 128, 2048, 1024, 32)])
+    cases.append(("worked example: row AllReduce p=2, M=128, chunk_m=32",
+                  lambda: tp.tp_row_linear_fwd_allreduce(d1["x"], d1["w"], [y1], ws1, 32)))
+    M, p, h, nk = 2048, 8, 12288, 6144
+    d5 = _dev_all(torch, synth.config5_inputs(M))
+    z5 = [torch.empty((M, nk), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    y5 = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+    for c in (256, 1024, 2048):
+        ws5 = _ws_for(torch, tp, [(tp.TP_OP_ROW_AR, p, M, h, nk, c)])
+        cases.append((f"GPT-3-scale FC2 row AllReduce p=8, M=2048, chunk_m={c}",
+                      lambda c=c, ws5=ws5: tp.tp_row_linear_fwd_allreduce(z5, d5["w2"], [y5], ws5, c)))
+    for name, fn in cases:
+        rec = _trace_launch(torch, tp, fn)
+        per, total, overlap = _timeline(rec)
+        n = len(per)
+        cbar = sum(x["c_us"] for x in per) / n
+        mbar = sum(x["m_us"] for x in per) / n
+        print(json.dumps({"trace": name, "units": len(rec), "n_chunks": n, "launch_us": round(total, 2),
+                          "mean_c_us": round(cbar, 2), "mean_m_us": round(mbar, 2),
+                          "model_pipelined_us": round(tp.tp_pipeline_time(cbar, mbar, n), 2),
+                          "model_serial_us": round(n * (cbar + mbar), 2),
+                          "drain_overlapped_with_mma": round(overlap, 3), "chunks": per[:8]}), flush=True)
+
+
 def main():
     args = parse()
     if args.tile_mode and args.impl == "ours":
@@ -868,6 +952,9 @@ def main():
         return
     if args.precision_report:
         run_precision_report(args)
+        return
+    if args.trace:
+        run_trace(args)
         return
     run_ours(args)
 

@@ -90,6 +90,7 @@ def _load() -> ctypes.CDLL:
         "tp_get_device_status": (I, [P, P]),
         "tp_status_string": (ctypes.c_char_p, [I]),
         "tp_debug_set": (I, [I, L]),
+        "tp_trace_set": (I, [P, L]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -193,6 +194,12 @@ def workspace(op: int, p: int, M: int, N: int, K: int, chunk_m: int = 0, device=
     import torch
     n = tp_workspace_size(op, p, M, N, K, chunk_m, out_dtype)
     return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def tp_trace_set(buf, cap_units: int = 0) -> None:
+    """Trace the GEMM launches that follow into ``buf`` (a zeroed CUDA
+    int64 tensor of cap_units x 4), or stop tracing with ``buf=None``."""
+    _check(_lib.tp_trace_set(_ptr(buf), cap_units if buf is not None else 0), "tp_trace_set")
 
 
 def tp_debug_set(key: int, value: int) -> int:

@@ -89,10 +89,16 @@ struct GemmParams {
   int32_t tail_split;        // 1: no slicing
   float* tail_part;          // fp32 partials of the slices, per (tile, slice, CTA, warp)
   uint32_t* tail_cnt;        // per (tile, CTA, epilogue warp): slices finished (zero at launch)
+  // optional timeline trace (nullptr: off): per unit t < trace_cap, four
+  // words: first MMA issued, accumulator seen full, last warp drained (ns
+  // of %globaltimer), and (chunk << 32 | CTA or cluster index)
+  unsigned long long* trace;
+  int32_t trace_cap;
 };
 
 struct Unit {
   int32_t gm, gn, mt, nt, q0, q1;
+  int32_t ch;  // chunk of the chunked axis this tile belongs to
 };
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& P, int32_t t) {
@@ -123,10 +129,26 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& P, int32_t t) {
   u.mt = GM % P.m_tiles;
   u.gn = GN / P.n_tiles;
   u.nt = GN % P.n_tiles;
+  u.ch = c;
   const int32_t kb_total = P.S * P.kb_per_seg;
   u.q0 = sp * P.kb_per_split;
   u.q1 = min(kb_total, u.q0 + P.kb_per_split);
   return u;
+}
+
+// Timeline trace (see GemmParams::trace).
+__device__ __forceinline__ void trace_mma_start(const GemmParams& P, int32_t t, int32_t ch, uint32_t who) {
+  if (P.trace != nullptr && t < P.trace_cap) {
+    P.trace[4 * static_cast<size_t>(t)] = globaltimer_ns();
+    P.trace[4 * static_cast<size_t>(t) + 3] = (static_cast<unsigned long long>(ch) << 32) | who;
+  }
+}
+__device__ __forceinline__ void trace_acc_full(const GemmParams& P, int32_t t) {
+  if (P.trace != nullptr && t < P.trace_cap) P.trace[4 * static_cast<size_t>(t) + 1] = globaltimer_ns();
+}
+__device__ __forceinline__ void trace_drained(const GemmParams& P, int32_t t) {
+  if (P.trace != nullptr && t < P.trace_cap)
+    atomicMax(&P.trace[4 * static_cast<size_t>(t) + 2], static_cast<unsigned long long>(globaltimer_ns()));
 }
 
 // Pair-kernel unit t: a whole tile, or (t >= tail_start) k-slice tk of tail
@@ -713,6 +735,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Unit u = decode_unit(P, t);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, P, abort_flag, 2u)) break;
         tc_fence_after();
+        trace_mma_start(P, t, u.ch, blockIdx.x);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int32_t q = u.q0; q < u.q1; ++q) {
           if (!wait_bar(full_bar(stage), phase, P, abort_flag, 3u)) {
@@ -769,7 +792,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       uint8_t* stg = OUT_T ? nullptr
                            : base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
+      if (warp == 2 && lane == 0) trace_acc_full(P, t);
       drain_tile<BN, OUT_T>(P, u, sp, g, gi, row_ok, t_row, half, stg);
+      if (lane == 0) trace_drained(P, t);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -1017,6 +1042,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, P, abort_flag, 2u)) break;
         tc_fence_after();
+        trace_mma_start(P, t, u.ch, blockIdx.x >> 1);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
         for (int32_t q = u.q0; q < u.q1; ++q) {
           if (!wait_bar(full_bar(stage), phase, P, abort_flag, 3u)) {
@@ -1074,8 +1100,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * Cfg::BN);
       uint8_t* stg = base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
+      if (leader && warp == 2 && lane == 0) trace_acc_full(P, t);
       if (TAIL && tj >= 0) drain_tail_slice(P, u, tj, tk, crank, g, gi, t_row, half, warp - 2, stg);
       else drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half, stg);
+      if (lane == 0) trace_drained(P, t);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));

@@ -46,6 +46,8 @@ std::atomic<uint64_t> g_timeout_override_ns{0};
 std::atomic<int64_t> g_debug_drop_q{-1};
 std::atomic<int64_t> g_debug_tile_mode{0};  // 0 auto, 1 single-CTA tiles only, 2 CTA pairs whenever possible
 std::atomic<int64_t> g_debug_no_tail{0};    // 1: no k-slices in the last wave of pair launches
+std::atomic<unsigned long long*> g_trace{nullptr};  // timeline trace buffer of the next launches
+std::atomic<int64_t> g_trace_cap{0};
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -515,6 +517,8 @@ void fill_common(GemmParams* P, const Shape& s) {
   P->n_rep = 1;
   P->timeout_ns = device_timeout_ns();
   P->debug_drop_q = static_cast<int32_t>(g_debug_drop_q.load());
+  P->trace = g_trace.load();
+  P->trace_cap = static_cast<int32_t>(std::min<int64_t>(g_trace_cap.load(), INT32_MAX));
 }
 
 size_t esize(tp_dtype d) { return d == TP_FP32 ? 4 : 2; }
@@ -740,6 +744,14 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;
+}
+
+tp_status tp_trace_set(void* buf, int64_t cap_units) {
+  if (cap_units < 0 || (buf == nullptr) != (cap_units == 0)) return TP_ERR_INVALID_ARG;
+  if (buf != nullptr && !aligned16(buf)) return TP_ERR_ALIGNMENT;
+  g_trace.store(static_cast<unsigned long long*>(buf));
+  g_trace_cap.store(cap_units);
+  return TP_OK;
 }
 
 double tp_pipeline_time(double c, double m, int64_t n_chunks) {

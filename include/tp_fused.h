@@ -329,6 +329,21 @@ typedef enum {
 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 
+/* Timeline trace of the GEMM launches that follow (process-wide, for
+ * measuring the chunk pipeline: [M027 §03, the two-engine timeline]).
+ *   buf: device buffer of cap_units x 4 uint64, zero-filled by the caller
+ *        before each traced launch; NULL (with cap_units 0) stops tracing.
+ *   Unit t of a launch (t < cap_units; units are the launch's tiles, or
+ *   split-K / last-wave slices, in the launch's chunk-major order) records
+ *     [0] %globaltimer (ns) when its first MMA was issued,
+ *     [1] when the epilogue saw its accumulator complete,
+ *     [2] when the last epilogue warp finished writing it out,
+ *     [3] (chunk index << 32) | CTA (single-CTA tiles) or cluster index.
+ *   Every traced launch writes from unit 0, so trace one launch at a time.
+ * Returns TP_ERR_INVALID_ARG for a negative size or a NULL/size mismatch,
+ * TP_ERR_ALIGNMENT for a buffer not 16-byte aligned.                      */
+tp_status tp_trace_set(void* buf, int64_t cap_units);
+
 /* Static description of a status code. */
 const char* tp_status_string(tp_status s);
 

@@ -89,6 +89,15 @@ def test_choose_chunk_m_from_measured_times(tp):
     assert tp.tp_choose_chunk_m_measured(0, [32], [1.0], [1.0]) == 0
 
 
+def test_trace_set_argument_checks(tp):
+    lib = tp._lib
+    assert lib.tp_trace_set(None, 5) == tp.TP_ERR_INVALID_ARG       # size without a buffer
+    assert lib.tp_trace_set(A, 0) == tp.TP_ERR_INVALID_ARG          # buffer without a size
+    assert lib.tp_trace_set(A, -1) == tp.TP_ERR_INVALID_ARG
+    assert lib.tp_trace_set(A + 8, 16) == tp.TP_ERR_ALIGNMENT
+    assert lib.tp_trace_set(None, 0) == tp.TP_OK                    # off
+
+
 def test_workspace_size(tp):
     assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0) >= 256
     # a skinny call plans a split-K and needs room for fp32 partials

@@ -555,6 +555,35 @@ def test_tail_slices_deterministic(tp):
     assert_close(host_f64(first), ref, False, "sliced AllReduce")
 
 
+# ------------------------------------------------------------------ timeline trace
+
+def test_timeline_trace_records_every_unit(tp):
+    """A traced launch records each unit once, in order start <= full <=
+    drained, tags every chunk, and leaves the result bit-identical."""
+    import torch
+    p, M, N, K, chunk = 2, 512, 520, 200, 128     # 4 chunks of 128 rows on 128x256 tiles
+    xs = [dev(ints((M, K), 780 + r)) for r in range(p)]
+    ws = [dev(ints((K, N), 782 + r)) for r in range(p)]
+    wsp = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, chunk)
+    plain = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tp.tp_row_linear_fwd_allreduce(xs, ws, [plain], wsp, chunk)
+    buf = torch.zeros((4096, 4), dtype=torch.int64, device="cuda")
+    traced = torch.empty_like(plain)
+    tp.tp_trace_set(buf, 4096)
+    try:
+        tp.tp_row_linear_fwd_allreduce(xs, ws, [traced], wsp, chunk)
+        torch.cuda.synchronize()
+    finally:
+        tp.tp_trace_set(None)
+    assert torch.equal(plain, traced)
+    rec = buf.cpu().numpy()
+    used = rec[rec[:, 0] != 0]
+    assert len(used) >= 4 * 3                              # 4 chunks x 3 column tiles (x splits)
+    assert np.all(used[:, 0] <= used[:, 1]) and np.all(used[:, 1] <= used[:, 2])
+    assert sorted(set((used[:, 3] >> 32).tolist())) == [0, 1, 2, 3]
+    assert not np.any(rec[len(used):, 0])                  # units are numbered from 0, densely
+
+
 # ------------------------------------------------------------------ calls from other threads
 
 def test_call_from_a_fresh_thread(tp):
