@@ -88,12 +88,15 @@ struct GemmParams {
   int32_t tail_start;
   int32_t tail_split;        // 1: no slicing
   float* tail_part;          // fp32 partials of the slices, per (tile, slice, CTA, warp)
-  uint32_t* tail_cnt;        // per (tile, CTA, epilogue warp): slices finished (zero at launch)
+  unsigned long long* tail_cnt;  // per (tile, CTA, epilogue warp): slices finished (see finish_slice)
   // optional timeline trace (nullptr: off): per unit t < trace_cap, four
   // words: first MMA issued, accumulator seen full, last warp drained (ns
   // of %globaltimer), and (chunk << 32 | CTA or cluster index)
   unsigned long long* trace;
   int32_t trace_cap;
+  // this launch's number (never 0): slice counters left by an earlier launch,
+  // finished or stopped, read as zero
+  unsigned long long epoch;
 };
 
 struct Unit {
@@ -433,10 +436,11 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
   __syncwarp();
 }
 
-// Sum, in slice order, of the tail partials of this lane's row for NV
-// columns starting at 32-column chunk c32 of the warp's region.
+// Sum, in slice order k = 0, 1, ..., of the partials of this lane's row for
+// NV columns starting at 32-column chunk c32 of the warp's region; slice k's
+// region starts at base + k * kstride (float4 units).
 template <int NV>
-__device__ __forceinline__ void load_chunk_parts(const float4* const* parts, int nparts, int c32, int lane,
+__device__ __forceinline__ void load_chunk_parts(const float4* base, size_t kstride, int nparts, int c32, int lane,
                                                  float (&v)[NV]) {
 #pragma unroll
   for (int i = 0; i < NV; ++i) v[i] = 0.f;
@@ -445,7 +449,7 @@ __device__ __forceinline__ void load_chunk_parts(const float4* const* parts, int
     for (int h = 0; h < NV / 32; ++h) {
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const float4 q = __ldcg(parts[k] + ((c32 + h) * 8 + m) * 32 + lane);
+        const float4 q = __ldcg(base + k * kstride + ((c32 + h) * 8 + m) * 32 + lane);
         float* d = &v[32 * h + 4 * m];
         if (k == 0) {
           d[0] = q.x; d[1] = q.y; d[2] = q.z; d[3] = q.w;
@@ -460,23 +464,82 @@ __device__ __forceinline__ void load_chunk_parts(const float4* const* parts, int
 // The warp's 128-column half of a tail tile through the staged epilogue,
 // values summed from the tail partials.
 __device__ __forceinline__ void drain_half_from_parts(const GemmParams& P, int32_t g, int32_t gi0, int32_t gj_half,
-                                                   uint8_t* stg, const float4* const* parts, int nparts) {
+                                                      uint8_t* stg, const float4* base, size_t kstride, int nparts) {
   const int lane = threadIdx.x & 31;
   if (P.out_f32) {
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
       float v[32];
-      load_chunk_parts<32>(parts, nparts, c / 32, lane, v);
+      load_chunk_parts<32>(base, kstride, nparts, c / 32, lane, v);
       finish_chunk_staged<true>(P, g, gi0, gj_half + c, v, stg, lane);
     }
   } else {
 #pragma unroll 1
     for (int c = 0; c < 128; c += 64) {
       float v[64];
-      load_chunk_parts<64>(parts, nparts, c / 32, lane, v);
+      load_chunk_parts<64>(base, kstride, nparts, c / 32, lane, v);
       finish_chunk_staged<false>(P, g, gi0, gj_half + c, v, stg, lane);
     }
   }
+}
+
+// Counts this warp's slice of a (tile, warp) region as finished; true for
+// the warp whose slice is the last of n.  A counter holds (launch epoch <<
+// 16 | slices finished); one left by another launch counts as zero, so no
+// clearing is needed between launches.  Each compare-and-swap that fails
+// means another of the region's n warps succeeded, so at most n attempts
+// are needed; past that bound the status word latches an error.
+__device__ __forceinline__ bool finish_slice(const GemmParams& P, unsigned long long* cnt, int n) {
+  __threadfence();
+  __syncwarp();
+  uint32_t last = 0;
+  if ((threadIdx.x & 31) == 0) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
+    unsigned long long next = 0;
+    bool done = false;
+    for (int i = 0; i <= n + 4 && !done; ++i) {
+      next = (cur >> 16) == P.epoch ? cur + 1 : ((P.epoch << 16) | 1ull);
+      const unsigned long long prev = atomicCAS(cnt, cur, next);
+      done = prev == cur;
+      cur = prev;
+    }
+    if (!done) atomicOr(P.status, ST_TIMEOUT | (5u << 4));
+    last = done && (next & 0xFFFFull) == static_cast<unsigned long long>(n);
+  }
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (last) __threadfence();
+  return last != 0;
+}
+
+// One k-slice of a 256-column accumulator, for one epilogue warp (32 rows x
+// 128 columns, half `half`): the slice's fp32 accumulator goes to its
+// partial, lane-major (float4 m of 32-column chunk c of lane l at
+// ((c * 8 + m) * 32 + l): every warp store and load moves 512 contiguous
+// bytes); the warp that finishes its region's last slice sums the n slices
+// in slice order 0, 1, ... (the same order whichever warp is last, so the
+// result is deterministic) and runs the staged epilogue.  No warp waits for
+// another.  Regions: ((tile * n + k) * ncta + cta) * NUM_EPI_WARPS + warp.
+__device__ __forceinline__ void drain_slice_wide(const GemmParams& P, const Unit& u, float* part,
+                                                 unsigned long long* cnt,
+                                                 int32_t tile, int32_t k, int32_t n, int ncta, uint32_t cta,
+                                                 int32_t g, int32_t gi, uint32_t t_row, int half, int wslot,
+                                                 uint8_t* stg) {
+  const int lane = threadIdx.x & 31;
+  constexpr size_t region = 32 * 32;  // float4 per warp region (32 rows x 128 columns)
+  const size_t kstride = static_cast<size_t>(ncta) * NUM_EPI_WARPS * region;
+  const float4* base = reinterpret_cast<const float4*>(part) + static_cast<size_t>(tile) * n * kstride +
+                       (static_cast<size_t>(cta) * NUM_EPI_WARPS + wslot) * region;
+  float4* mine = const_cast<float4*>(base) + k * kstride;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float v[32];
+    load_chunk_tmem<32>(t_row + half * 128 + c * 32, v);
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      mine[(c * 8 + m) * 32 + lane] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+  }
+  if (!finish_slice(P, cnt + (static_cast<size_t>(tile) * ncta + cta) * NUM_EPI_WARPS + wslot, n)) return;
+  drain_half_from_parts(P, g, gi - lane, u.nt * 256 + half * 128, stg, base, kstride, n);
 }
 
 // Epilogue of one accumulator for one epilogue warp: columns
@@ -834,52 +897,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 constexpr int PAIR_BK = 128;  // k-block depth of the pair kernel: 64 KiB stages, fewer round trips
 
-// Epilogue of one k-slice of a tail tile, for one epilogue warp (its 32 rows
-// x 128 columns, half `half` of the CTA's 128 x 256 accumulator):
-//   1. the slice's fp32 accumulator goes to its partial, lane-major (float4
-//      m of 32-column chunk c of lane l at ((c * 8 + m) * 32 + l): every warp
-//      store and load moves 512 contiguous bytes);
-//   2. the warp counts itself finished on its (tile, CTA, warp) counter;
-//   3. the warp that finishes last sums the tail_split partials in slice
-//      order 0, 1, ... (the same order whichever warp is last, so the result
-//      is deterministic), resets the counter, and runs the normal epilogue.
-// No warp waits for another.  Returns after the accumulator has been read.
-__device__ __forceinline__ void drain_tail_slice(const GemmParams& P, const Unit& u, int32_t tj, int32_t tk,
-                                                 uint32_t crank, int32_t g, int32_t gi, uint32_t t_row, int half,
-                                                 int wslot, uint8_t* stg) {
-  const int lane = threadIdx.x & 31;
-  const size_t region = 32 * 32;  // float4 per warp region (32 rows x 128 columns)
-  auto part_of = [&](int32_t k) {
-    return reinterpret_cast<float4*>(P.tail_part) +
-           ((static_cast<size_t>(tj) * P.tail_split + k) * 2 + crank) * (NUM_EPI_WARPS * region) +
-           static_cast<size_t>(wslot) * region;
-  };
-  float4* mine = part_of(tk);
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    float v[32];
-    load_chunk_tmem<32>(t_row + half * 128 + c * 32, v);
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-      mine[(c * 8 + m) * 32 + lane] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
-  }
-  __threadfence();
-  __syncwarp();
-  uint32_t last = 0;
-  if (lane == 0) {
-    uint32_t* cnt = P.tail_cnt + (static_cast<size_t>(tj) * 2 + crank) * NUM_EPI_WARPS + wslot;
-    const uint32_t old = atomicAdd(cnt, 1u);
-    last = old == static_cast<uint32_t>(P.tail_split - 1);
-    if (last) atomicExch(cnt, 0u);
-  }
-  last = __shfl_sync(0xFFFFFFFFu, last, 0);
-  if (!last) return;
-  __threadfence();
-  const float4* parts[4];
-  for (int k = 0; k < 4; ++k) parts[k] = k < P.tail_split ? part_of(k) : nullptr;
-  drain_half_from_parts(P, g, gi - lane, u.nt * 256 + half * 128, stg, parts, P.tail_split);
-}
-
 template <bool A_MN, bool B_MN, int BKP>
 struct PairCfg {
   static constexpr int BN = 256;                       // pair tile N
@@ -1101,7 +1118,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * Cfg::BN);
       uint8_t* stg = base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
       if (leader && warp == 2 && lane == 0) trace_acc_full(P, t);
-      if (TAIL && tj >= 0) drain_tail_slice(P, u, tj, tk, crank, g, gi, t_row, half, warp - 2, stg);
+      if (TAIL && tj >= 0)
+        drain_slice_wide(P, u, P.tail_part, P.tail_cnt, tj, tk, P.tail_split, 2, crank, g, gi, t_row, half,
+                         warp - 2, stg);
       else drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half, stg);
       if (lane == 0) trace_drained(P, t);
       tc_fence_before();

@@ -48,6 +48,7 @@ std::atomic<int64_t> g_debug_tile_mode{0};  // 0 auto, 1 single-CTA tiles only, 
 std::atomic<int64_t> g_debug_no_tail{0};    // 1: no k-slices in the last wave of pair launches
 std::atomic<unsigned long long*> g_trace{nullptr};  // timeline trace buffer of the next launches
 std::atomic<int64_t> g_trace_cap{0};
+std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (slice counters)
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -258,7 +259,7 @@ struct Shape {
   bool empty() const { return rows_g == 0 || cols_g == 0; }
   int64_t tail_tiles() const { return tail_split > 1 ? units0 - tail_start : 0; }
   size_t tail_cnt_bytes() const {
-    return static_cast<size_t>((tail_tiles() * 2 * NUM_EPI_WARPS * 4 + 255) / 256 * 256);
+    return static_cast<size_t>((tail_tiles() * 2 * NUM_EPI_WARPS * 8 + 255) / 256 * 256);
   }
   size_t partial_bytes() const {
     if (tail_split > 1)  // counters, then one fp32 256 x 256 tile per slice
@@ -618,13 +619,12 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     return TP_OK;
   }
   if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  if (s.tail_split > 1 && (phases & 1)) {
+  // slice counters tagged with another launch's number read as zero
+  P.epoch = g_launch_epoch.fetch_add(1) + 1;
+  if (s.tail_split > 1) {
     uint8_t* base = static_cast<uint8_t*>(ws) + kStatusBytes;
-    P.tail_cnt = reinterpret_cast<uint32_t*>(base);
+    P.tail_cnt = reinterpret_cast<unsigned long long*>(base);
     P.tail_part = reinterpret_cast<float*>(base + s.tail_cnt_bytes());
-    // the slice counters start every launch at zero, whatever an earlier
-    // launch that stopped on a timeout left behind
-    if (cudaMemsetAsync(base, 0, s.tail_cnt_bytes(), stream) != cudaSuccess) return TP_ERR_CUDA;
   }
   const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
                          : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));

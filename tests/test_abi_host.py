@@ -100,7 +100,8 @@ def test_trace_set_argument_checks(tp):
 
 def test_workspace_size(tp):
     assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0) >= 256
-    # a skinny call plans a split-K and needs room for fp32 partials
+    # a skinny call plans an operand-swapped split-K whose fp32 partials,
+    # one copy of Y per split, go to the second-stage kernel
     small = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 8, 16, 12288, 6144, 16)
     assert small > 256 and (small - 256) % (16 * 12288 * 4) == 0
     # invalid requests still return the minimum
@@ -110,9 +111,9 @@ def test_workspace_size(tp):
 def test_workspace_holds_the_last_wave_slices(tp):
     """bf16 outputs on CTA pairs: 4096 x 4096 is 256 pair tiles, 3 full waves
     of 76 clusters and 28 tiles cut into 2 k-slices: one fp32 256 x 256 tile
-    per slice, after the slice counters (one per tile, CTA and epilogue warp)."""
+    per slice, after the 8-byte slice counters (one per tile, CTA and epilogue warp)."""
     bf = tp.tp_workspace_size(tp.TP_OP_ROW_AR, 4, 4096, 4096, 4096, 0, tp.TP_BF16)
-    assert bf == 256 + 28 * 2 * 8 * 4 + 28 * 2 * 256 * 256 * 4
+    assert bf == 256 + 28 * 2 * 8 * 8 + 28 * 2 * 256 * 256 * 4
     # a whole number of waves (152 tiles) needs no slices
     assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 2, 4864, 2048, 1024, 0, tp.TP_BF16) == 256
 
