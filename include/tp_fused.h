@@ -40,7 +40,8 @@
  *    device status word (which stays zero unless a device wait times out)
  *    and, when a launch needs them, fp32 partials: split-K partials, or the
  *    k-slices of the last partial wave of a CTA-pair launch together with
- *    their counters (which the library clears before each such launch).
+ *    their counters (tagged with a per-launch number, so a counter left
+ *    by any earlier launch, finished or stopped, reads as zero).
  *    tp_workspace_size() is the size of the fastest plan; a smaller
  *    workspace that still holds the plan without last-wave slices is
  *    accepted, and the call then runs without them.
@@ -294,8 +295,8 @@ tp_status tp_get_device_status(void* ws, cudaStream_t stream);
  *    the GPU (different streams without ordering between them) race on it;
  *    order them on one stream.  Nothing in the array has to start at zero:
  *    every partial a call reads was written earlier by that same call, and
- *    slice counters are cleared (cudaMemsetAsync, no allocation) before the
- *    launch that uses them.
+ *    slice counters carry the number of the launch that wrote them, so
+ *    stale ones read as zero.
  *  - Device-side timeouts are latched in the array but not reported; use
  *    tp_row_linear_fwd_allreduce with a workspace to read them.            */
 #define TP_NOALLOC_SCRATCH_BYTES (16u << 20)
