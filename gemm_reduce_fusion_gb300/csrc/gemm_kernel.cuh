@@ -1194,7 +1194,21 @@ __global__ void tp_splitk_reduce_kernel(const __grid_constant__ ReduceParams R) 
         acc.w = bf16_round_f(acc.w + bf16_round_f(v.w));
       }
     } else {
-      for (int s = 1; s < R.n_split; ++s) {
+      // four splits' loads in flight at a time; the additions stay in split order
+      int s = 1;
+      for (; s + 3 < R.n_split; s += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const float4*>(R.partial + (s + j) * split_stride + e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc.x += v[j].x;
+          acc.y += v[j].y;
+          acc.z += v[j].z;
+          acc.w += v[j].w;
+        }
+      }
+      for (; s < R.n_split; ++s) {
         const float4 v = *reinterpret_cast<const float4*>(R.partial + s * split_stride + e);
         acc.x += v.x;
         acc.y += v.y;
