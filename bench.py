@@ -699,6 +699,37 @@ def _time_calls(torch, calls, steps, warmup, flush_buf=None):
     return med(times), {n: med(v) for n, v in per.items()}, min(times), sorted(times)[int(0.9 * (len(times) - 1))]
 
 
+# The same GEMMs on the unsharded problem, (M, K, N) each, as plain library
+# matmuls: context for each workload (a GEMM library on the concatenated
+# weights, with no reduction or gather to do), not part of the measured path.
+UNSHARDED_GEMMS = {
+    "config1": [(128, 2048, 2048)] * 2,
+    "config2": [(4096, 4096, 16384), (4096, 16384, 4096), (4096, 4096, 16384), (16384, 4096, 4096),
+                (4096, 16384, 4096), (4096, 4096, 16384)],
+    "config3": [(4096, 4096, 12288), (4096, 4096, 4096), (4096, 4096, 4096), (4096, 4096, 4096),
+                (4096, 12288, 4096), (4096, 4096, 12288)],
+    "config4": [(8192, 8192, 28672), (8192, 28672, 8192)],
+    "config4_fwd_bwd": [(8192, 8192, 28672), (8192, 28672, 8192), (8192, 8192, 28672), (28672, 8192, 8192),
+                        (8192, 28672, 8192), (8192, 8192, 28672)],
+    "config5_m2048": [(2048, 12288, 49152), (2048, 49152, 12288)],
+    "config5_m16": [(16, 12288, 49152), (16, 49152, 12288)],
+}
+
+
+def _time_unsharded(torch, gemms, steps, warmup, flush_buf):
+    """Median per-step ms of torch.matmul over the unsharded GEMMs."""
+    bufs = []
+    for m, k, n in gemms:
+        bufs.append((torch.randn((m, k), device="cuda").to(torch.bfloat16),
+                     torch.randn((k, n), device="cuda").mul_(0.02).to(torch.bfloat16),
+                     torch.empty((m, n), dtype=torch.bfloat16, device="cuda")))
+    calls = [(f"matmul{i}", (lambda a=a, b=b, c=c: torch.matmul(a, b, out=c))) for i, (a, b, c) in enumerate(bufs)]
+    ms, _, _, _ = _time_calls(torch, calls, steps, warmup, flush_buf)
+    del bufs, calls
+    torch.cuda.empty_cache()
+    return ms
+
+
 def run_configs(args):
     import torch
     torch.cuda.set_device(0)
@@ -717,9 +748,16 @@ def run_configs(args):
         if w["bytes"]:
             gbs = w["bytes"] / (ms / 1e3) / 1e9
             line.update({"hbm_gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"], "bytes_per_step": w["bytes"]})
-        print(json.dumps(line), flush=True)
         del w
         torch.cuda.empty_cache()
+        if name in UNSHARDED_GEMMS:
+            cms = _time_unsharded(torch, UNSHARDED_GEMMS[name], max(10, args.steps), max(3, args.warmup),
+                                  flush if line["l2"].startswith("flushed") else None)
+            line.update({"unsharded_torch_matmul_ms": cms,
+                         "fused_speed_vs_unsharded_torch_matmul": cms / ms,
+                         "context": "torch.matmul (library GEMM) on the unsharded problem's GEMMs, same FLOPs, "
+                                    "no reduction or gather; not part of the measured path"})
+        print(json.dumps(line), flush=True)
 
 
 def run_sweep(args):
