@@ -26,6 +26,7 @@ constexpr int kMaxP = 8;
 constexpr int kPlanSMs = 152;            // SM count the split-K plan assumes (GB300)
 constexpr size_t kStatusBytes = 256;     // workspace head: status word, padded
 constexpr int kStagesWide = 4;           // 128x256 tiles: 48 KiB per stage
+constexpr int kPairKChunks = PAIR_BK / 64;  // 64-wide K chunks per pair k-block (K-major operand maps)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // fp32-output mode: at most this many 64-deep k-blocks (K = 2048) are
 // accumulated in one tensor-core accumulator; longer contractions are split
@@ -899,7 +900,7 @@ static tp_status row_fwd_impl(bool rs, const void* const* x, const void* const* 
   if (K > 0) {
     for (int r = 0; r < p; ++r) {
       if (!s.swap) {
-        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM, m3 ? (s.pair ? kPairKChunks : 1) : 0) ||
             !encode_map(&P.tmB[r], w[r], N, K, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
           return TP_ERR_CUDA;
       } else {
@@ -1007,11 +1008,11 @@ static tp_status col_like_fwd(bool ag, const void* const* xs, const void* x1, co
     const int tok_box = s.swap ? s.bn : BM;
     if (!ag) {
       CUtensorMap* xm = s.swap ? &P.tmB[0] : &P.tmA[0];
-      if (!encode_map(xm, x1, K, M, K, tok_box, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
+      if (!encode_map(xm, x1, K, M, K, tok_box, m3 ? (s.pair ? kPairKChunks : 1) : 0)) return TP_ERR_CUDA;
     } else {
       for (int t = 0; t < p; ++t) {
         CUtensorMap* xm = s.swap ? &P.tmB[t] : &P.tmA[t];
-        if (!encode_map(xm, xs[t], K, Mp, K, tok_box, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
+        if (!encode_map(xm, xs[t], K, Mp, K, tok_box, m3 ? (s.pair ? kPairKChunks : 1) : 0)) return TP_ERR_CUDA;
       }
     }
   }
@@ -1141,8 +1142,8 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
-              !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0))
+          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM, m3 ? (s.pair ? kPairKChunks : 1) : 0) ||
+              !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? kPairKChunks : 1) : 0))
             return TP_ERR_CUDA;
         } else {
           if (!encode_map(&P.tmA[k], w[k], N, K, N, BM, m3 ? 1 : 0) ||
@@ -1208,13 +1209,13 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
+          if (!encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? kPairKChunks : 1) : 0)) return TP_ERR_CUDA;
         } else {
           if (!encode_map(&P.tmA[k], w[k], N, K, N, BM, m3 ? 1 : 0)) return TP_ERR_CUDA;
         }
       }
       if (!s.swap) {
-        if (!encode_map(&P.tmA[0], dy, N, M, N, BM, m3 ? (s.pair ? 2 : 1) : 0)) return TP_ERR_CUDA;
+        if (!encode_map(&P.tmA[0], dy, N, M, N, BM, m3 ? (s.pair ? kPairKChunks : 1) : 0)) return TP_ERR_CUDA;
       } else {
         if (!encode_map(&P.tmB[0], dy, N, M, N, s.bn, m3 ? 1 : 0)) return TP_ERR_CUDA;
       }
@@ -1286,8 +1287,8 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
     if (N > 0) {
       for (int k = 0; k < p; ++k) {
         if (!s.swap) {
-          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
-              !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0))
+          if (!encode_map(&P.tmA[k], dy[k], N, M, N, BM, m3 ? (s.pair ? kPairKChunks : 1) : 0) ||
+              !encode_map(&P.tmB[k], w[k], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? kPairKChunks : 1) : 0))
             return TP_ERR_CUDA;
         } else {
           if (!encode_map(&P.tmA[k], w[k], N, K, N, BM, m3 ? 1 : 0) ||
@@ -1386,8 +1387,8 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
       for (int t = 0; t < p; ++t) {
         // shard t of dY (source rows) and weight A_t (output r = t)
         if (!s.swap) {
-          if (!encode_map(&P.tmA[t], dy[t], N, Mp, N, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
-              !encode_map(&P.tmB[t], w[t], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? 2 : 1) : 0))
+          if (!encode_map(&P.tmA[t], dy[t], N, Mp, N, BM, m3 ? (s.pair ? kPairKChunks : 1) : 0) ||
+              !encode_map(&P.tmB[t], w[t], N, K, N, s.pair ? 128 : 256, m3 ? (s.pair ? kPairKChunks : 1) : 0))
             return TP_ERR_CUDA;
         } else {
           if (!encode_map(&P.tmA[t], w[t], N, K, N, BM, m3 ? 1 : 0) ||
@@ -1483,7 +1484,7 @@ extern "C" tp_status tp_row_linear_fwd_unfused(const void* const* x, const void*
   if (K > 0) {
     for (int r = 0; r < p; ++r) {
       if (!s.swap) {
-        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM, m3 ? (s.pair ? 2 : 1) : 0) ||
+        if (!encode_map(&P.tmA[r], x[r], K, M, K, BM, m3 ? (s.pair ? kPairKChunks : 1) : 0) ||
             !encode_map(&P.tmB[r], w[r], N, K, N, s.pair ? PAIR_BK : 64, m3 ? (s.pair ? 2 : 4) : 0))
           return TP_ERR_CUDA;
       } else {
