@@ -16,17 +16,25 @@
 //              empty barriers and to the accumulator-full barrier;
 //   warps 2-9  epilogue: tcgen05.ld the finished accumulator (warp w reads
 //              TMEM lanes 32*(w%4)..+31; warps 2-5 take the left half of the
-//              columns, warps 6-9 the right half), apply GeLU / GeLU' / cast,
-//              store, then release the accumulator -- overlapping the next
+//              columns, warps 6-9 the right half), apply bias / GeLU / GeLU'
+//              / cast, stage 128-byte rows in shared memory and store whole
+//              lines, then release the accumulator -- overlapping the next
 //              tile's MMAs on the other accumulator.
 //
 // Tiles are visited chunk-major: all tiles of rows chunk c (over every
-// N-tile) precede those of chunk c+1, m fastest within a chunk, so a chunk's
-// write-out overlaps the next chunk's MMAs ("ai-infra-kb M027", §02-§03).
+// N-tile) precede those of chunk c+1, in bands of N-tiles within a chunk,
+// so a chunk's write-out overlaps the next chunk's MMAs ("ai-infra-kb
+// M027", §02-§03).  Two kernels share this structure: tp_gemm_kernel (one
+// CTA per 128 x BN tile, optionally operand-swapped for token tiles below
+// 128, with split-K and a second-stage kernel) and tp_gemm_pair_kernel
+// (CTA pairs, 256 x 256 tiles via tcgen05.mma.cta_group::2, whose last
+// partial wave may run as k-slices that the last-finishing warp sums).
 //
 // Every mbarrier wait is bounded in time: on expiry the kernel latches an
 // error bit in the status word, tells the other roles to stop, waits (again
 // bounded) for its own TMA loads and MMAs in flight, frees TMEM and returns.
+// An optional trace records per-unit %globaltimer stamps (see
+// GemmParams::trace).
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -219,55 +227,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// v[e] += b[e] for 8 consecutive bf16 bias values (16-byte aligned).
-__device__ __forceinline__ void add_bias8(float (&v)[8], const uint16_t* b) {
-  const uint4 q = *reinterpret_cast<const uint4*>(b);
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] += bf16_bits_to_f(static_cast<uint16_t>(w[i] & 0xFFFFu));
-    v[2 * i + 1] += bf16_bits_to_f(static_cast<uint16_t>(w[i] >> 16));
-  }
-}
 
-// Epilogue transform of 8 consecutive values; `aux` points at the matching 8
-// elements of H (DGELU reads them, GELU writes them when non-null).
-__device__ __forceinline__ void epi8(const GemmParams& P, float (&v)[8], void* aux) {
-  if (P.epi == EPI_GELU) {
-    if (aux != nullptr) {
-      if (P.out_f32) {
-        float4* a = reinterpret_cast<float4*>(aux);
-        a[0] = make_float4(v[0], v[1], v[2], v[3]);
-        a[1] = make_float4(v[4], v[5], v[6], v[7]);
-      } else {
-        *reinterpret_cast<uint4*>(aux) =
-            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                       pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = gelu_f(v[i]);
-  } else if (P.epi == EPI_DGELU) {
-    const uint4 h = *reinterpret_cast<const uint4*>(aux);
-    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[i] & 0xFFFFu)));
-      v[2 * i + 1] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[i] >> 16)));
-    }
-  }
-}
 
-__device__ __forceinline__ void store8(void* dst, bool f32, const float (&v)[8]) {
-  if (f32) {
-    float4* d = reinterpret_cast<float4*>(dst);
-    d[0] = make_float4(v[0], v[1], v[2], v[3]);
-    d[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-  }
-}
 
 // Scalar epilogue for the transposed (operand-swapped) orientation.
 __device__ __forceinline__ void epi_store1(const GemmParams& P, float v, void* out, void* aux,
@@ -553,8 +514,11 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
                                            uint8_t* stg) {
   constexpr int HALF = BN / 2;
   constexpr int CW = HALF < 32 ? HALF : 32;
-  if constexpr (!OUT_T && HALF == 128) {
-    if (P.n_split == 1 && stg != nullptr) {
+  // non-swapped tiles are 256 wide and always drain through the staging
+  // buffer (or, with split-K, into the dense partials below)
+  static_assert(OUT_T || HALF == 128, "non-swapped tiles are 128 x 256");
+  if constexpr (!OUT_T) {
+    if (P.n_split == 1) {
       const int lane = threadIdx.x & 31;
       const int32_t gi0 = gi - lane;
       if (P.out_f32) {
@@ -610,7 +574,7 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
       }
       continue;
     }
-    if (OUT_T) {
+    if constexpr (OUT_T) {
       // operand-swapped: GEMM row gi is the output column, so one bias value
       const float bsc = P.bias[g] != nullptr
                             ? bf16_bits_to_f(static_cast<const uint16_t*>(P.bias[g])[gi])
@@ -623,29 +587,6 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
           const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
           for (int rep = 0; rep < P.n_rep; ++rep)
             epi_store1(P, __uint_as_float(r[i]) + bsc, P.out[g + rep], P.aux[g], off_o, off_a);
-        }
-      }
-    } else {
-      const size_t esz = P.out_f32 ? 4 : 2;
-#pragma unroll
-      for (int i = 0; i < CW; i += 8) {
-        const int32_t gj = gj0 + i;
-        if (gj >= P.cols_g) continue;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[i + e]);
-        if (P.bias[g] != nullptr) add_bias8(v, static_cast<const uint16_t*>(P.bias[g]) + gj);
-        void* auxp = nullptr;
-        if (P.epi != EPI_NONE && P.aux[g] != nullptr) {
-          const size_t aesz = (P.epi == EPI_DGELU) ? 2 : esz;
-          auxp = static_cast<uint8_t*>(P.aux[g]) +
-                 (static_cast<int64_t>(gi) * P.ld_aux + gj) * static_cast<int64_t>(aesz);
-        }
-        epi8(P, v, auxp);
-        for (int rep = 0; rep < P.n_rep; ++rep) {
-          uint8_t* dst = static_cast<uint8_t*>(P.out[g + rep]) +
-                         (static_cast<int64_t>(gi) * P.ld_out + gj) * static_cast<int64_t>(esz);
-          store8(dst, P.out_f32 != 0, v);
         }
       }
     }
