@@ -58,8 +58,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=100,
-                    help="steps of the end-to-end run (host buffers, copies overlapped with compute)")
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the end-to-end run (host buffers, copies overlapped with compute); "
+                         "0: as many as --steps, so both runs see the same sustained clocks")
     ap.add_argument("--sweep", action="store_true",
                     help="chunk_m sweep of the GPT-3-scale FC pair: fused time vs the timeline model")
     ap.add_argument("--configs", action="store_true",
@@ -424,7 +425,7 @@ def run_ours(args):
     # (uploaded once, before timing); every step uploads its data (X, dY)
     # from pinned host memory and downloads its results (Y, dX).  Context:
     # the same with W1, W2 uploaded and dW1, dW2 downloaded every step too.
-    E = max(1, args.e2e_steps)
+    E = max(1, args.e2e_steps if args.e2e_steps > 0 else args.steps)
     steps = [step, MLPStep(tp, torch, host)]
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     comp = torch.cuda.current_stream()
