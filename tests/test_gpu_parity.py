@@ -584,6 +584,38 @@ def test_timeline_trace_records_every_unit(tp):
     assert not np.any(rec[len(used):, 0])                  # units are numbered from 0, densely
 
 
+# ------------------------------------------------------------------ concurrent streams
+
+def test_two_streams_with_their_own_workspaces(tp):
+    """Calls enqueued on two streams with no ordering between them, each with
+    its own workspace (one a sliced CTA-pair launch, one a split-K skinny
+    launch), both exact."""
+    import torch
+    p, M, N, K = 2, 2048, 2560, 512
+    xa = [ints((M, K), 790 + r) for r in range(p)]
+    wa = [ints((K, N), 792 + r) for r in range(p)]
+    pb, Mb, Nb, Kb = 8, 16, 2048, 512
+    xb = [ints((Mb, Kb), 794 + r) for r in range(pb)]
+    wb = [ints((Kb, Nb), 803 + r) for r in range(pb)]
+    XA, WA = [dev(a) for a in xa], [dev(b) for b in wa]
+    XB, WB = [dev(a) for a in xb], [dev(b) for b in wb]
+    ya = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    yb = torch.empty((Mb, Nb), dtype=torch.float32, device="cuda")
+    wsa = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0)
+    wsb = ws_for(tp, tp.TP_OP_ROW_AR, pb, Mb, Nb, Kb, 16)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            tp.tp_row_linear_fwd_allreduce(XA, WA, [ya], wsa)
+        with torch.cuda.stream(s2):
+            tp.tp_row_linear_fwd_allreduce(XB, WB, [yb], wsb, chunk_m=16)
+    torch.cuda.synchronize()
+    assert tp.tp_get_device_status(wsa) == tp.TP_OK and tp.tp_get_device_status(wsb) == tp.TP_OK
+    assert np.array_equal(host_f64(ya), oracle.row_fwd_allreduce(xa, wa))
+    assert np.array_equal(host_f64(yb), oracle.row_fwd_allreduce(xb, wb))
+
+
 # ------------------------------------------------------------------ calls from other threads
 
 def test_call_from_a_fresh_thread(tp):
