@@ -46,6 +46,10 @@
  *    workspace that still holds the plan without last-wave slices is
  *    accepted, and the call then runs without them.
  *    Calls that share a workspace must be ordered on the same stream.
+ *  - Any host thread may call; a call runs on that thread's current CUDA
+ *    device (the library makes the device's primary context current).
+ *  - Biases (forward) and bias gradients (backward) are optional bf16 /
+ *    out_dtype vectors over the output columns; NULL leaves them out.
  *  - Errors: argument checks run on the host before anything is enqueued
  *    and return a tp_status; on error nothing is launched.  A device-side
  *    wait that runs out of time latches TP_ERR_DEVICE_TIMEOUT into the
