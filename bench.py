@@ -70,6 +70,8 @@ def parse():
                     help="0: planner chooses 128x256 or CTA-pair 256x256 tiles; 1: 128x256 only; 2: pairs")
     ap.add_argument("--profile-case", action="store_true",
                     help="run each GEMM variant of the step twice at the step's shapes (for ncu)")
+    ap.add_argument("--profile-workload", default="", metavar="NAME",
+                    help="set up one workload of --configs and run its calls twice (for ncu)")
     ap.add_argument("--trace", action="store_true",
                     help="per-chunk timeline of single fused launches (the two-engine timeline, measured)")
     ap.add_argument("--precision-report", action="store_true",
@@ -545,6 +547,23 @@ def profile_case():
     print("profile case done")
 
 
+def profile_workload(name):
+    """One workload of --configs, set up once and its calls run twice: a
+    bounded case for ncu (at most about 3 GB resident, a few launches)."""
+    import torch
+    torch.cuda.set_device(0)
+    import gemm_reduce_fusion_gb300 as tp
+    table = dict(workloads(torch, tp))
+    if name not in table:
+        raise SystemExit(f"unknown workload {name!r}; one of {sorted(table)}")
+    w = table[name]()
+    for _ in range(2):
+        for _, fn in w["calls"]:
+            fn()
+    torch.cuda.synchronize()
+    print(f"profile workload {name} done: {[n for n, _ in w['calls']]} x 2")
+
+
 # ------------------------------------------------------------------ all workloads / chunk sweep
 
 def _dev_all(torch, tree):
@@ -1013,6 +1032,9 @@ def main():
         tp.tp_debug_set(tp.TP_DEBUG_TILE_MODE, args.tile_mode)
     if args.profile_case:
         profile_case()
+        return
+    if args.profile_workload:
+        profile_workload(args.profile_workload)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -79,10 +79,10 @@ def test_bench_modes_present():
     sys.path.insert(0, ROOT)
     import bench
     for name in ("run_ours", "run_reference", "run_configs", "run_sweep", "profile_case", "workloads",
-                 "cpu_baseline", "aggregate_value", "run_precision_report", "run_trace"):
+                 "cpu_baseline", "aggregate_value", "run_precision_report", "run_trace", "profile_workload"):
         assert callable(getattr(bench, name)), name
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True,
                          text=True, timeout=120)
     for flag in ("--configs", "--sweep", "--profile-case", "--tile-mode", "--impl", "--gpus", "--steps", "--warmup",
-                 "--precision-report", "--trace"):
+                 "--precision-report", "--trace", "--profile-workload"):
         assert flag in out.stdout, flag
