@@ -593,6 +593,7 @@ def workloads(torch, tp):
                             lambda: tp.tp_row_linear_fwd_reducescatter(d["x"], d["w"], ys, ws, 32))],
                     flops=2 * 2.0 * M * N * K * p, bytes=2 * (2 * (p * M * K + p * K * N) + 2 * M * N),
                     bound="hbm", flush=True,
+                    row_reduce=dict(call="row_fwd_allreduce", x=d["x"], w=d["w"], y=y, chunk=32),
                     desc="row-parallel p=2, X_r[128,1024], W_r[1024,2048], AllReduce + ReduceScatter, chunk_m=32")
 
     def w2():
@@ -615,6 +616,7 @@ def workloads(torch, tp):
             ("col_bwd_dx", lambda: tp.tp_col_linear_bwd(None, d["w1"], DZ, DX, None, ws)),
             ("col_bwd_dw", lambda: tp.tp_col_linear_bwd(d["x"], d["w1"], DZ, None, DW1, ws))],
             flops=6 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
+            row_reduce=dict(call="row_fwd_allreduce", x=Z, w=d["w2"], y=Y, chunk=0),
             desc="Megatron MLP block fwd+bwd p=4, 4096 tokens, h=4096, ffn=16384")
 
     def w3():
@@ -634,6 +636,7 @@ def workloads(torch, tp):
             ("wo_row_bwd", lambda: tp.tp_row_linear_bwd(d["o"], d["wo"], d["dy"], DO, DWO, ws)),
             ("qkv_col_bwd", lambda: tp.tp_col_linear_bwd(d["x"], d["wqkv"], d["dqkv"], DX, DWQ, ws))],
             flops=3 * (2.0 * M * h * nq * p + 2.0 * M * no * h * p), bytes=None, bound="tensor", flush=False,
+            row_reduce=dict(call="wo_row_fwd_allreduce", x=d["o"], w=d["wo"], y=Y, chunk=0),
             desc="MHA projections fwd+bwd p=4, 4096 tokens, h=4096, QKV [4096,3072]/shard, W_O [1024,4096]/shard")
 
     def w4():
@@ -648,6 +651,7 @@ def workloads(torch, tp):
             ("ag_matmul_gelu", lambda: tp.tp_ag_matmul(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
             ("row_fwd_reducescatter", lambda: tp.tp_row_linear_fwd_reducescatter(Z, d["w2"], YS, ws))],
             flops=2 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
+            row_reduce=dict(call="row_fwd_reducescatter", x=Z, w=d["w2"], y=None, chunk=0, op=tp.TP_OP_ROW_RS),
             desc="sequence-parallel pair fwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672")
 
     def w4b():
@@ -688,6 +692,7 @@ def workloads(torch, tp):
                 flops=2 * 2.0 * M * h * nk * p,
                 bytes=wbytes + 4.0 * M * h + 6.0 * M * nk * p,
                 bound="hbm" if M <= 64 else "tensor", flush=M <= 64,
+                row_reduce=dict(call="row_fwd_allreduce", x=Z, w=d["w2"], y=Y, chunk=0),
                 desc=f"GPT-3-scale MLP fwd p=8, h=12288, ffn=49152, M={M}")
         return setup
 
@@ -750,6 +755,34 @@ def _time_unsharded(torch, gemms, steps, warmup, flush_buf):
     return ms
 
 
+def _row_timeline(torch, tp, rr, fused_ms, steps, warmup, flush_buf):
+    """The two-engine timeline of a workload's row-parallel reduction
+    ([M027] §03): c = one chunk's per-rank partial GEMMs and m = its
+    rank-order reduce, both timed on the unfused baseline on chunk_m rows;
+    the modelled T = c + (n-1) max(c, m) + m beside the fused call and the
+    whole unfused call.  A ReduceScatter is modelled by the AllReduce of the
+    same partials: it sums the same terms and routes row slices."""
+    x, w = rr["x"], rr["w"]
+    p = len(x)
+    M, K = x[0].shape
+    N = w[0].shape[1]
+    y = rr["y"] if rr["y"] is not None else torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    chunk = min(rr["chunk"] or tp.tp_choose_chunk_m(rr.get("op", tp.TP_OP_ROW_AR), p, M, N, K), M)
+    n = tp.tp_num_chunks(M, chunk)
+    ws = _ws_for(torch, tp, [(tp.TP_OP_ROW_AR_UNFUSED, p, M, N, K, chunk)])
+    xc, yc = [a[:chunk] for a in x], y[:chunk]
+    c, _, _, _ = _time_calls(torch, [("c", lambda: tp.tp_row_linear_fwd_unfused(xc, w, yc, ws, chunk, phases=1))],
+                             steps, warmup, flush_buf)
+    m, _, _, _ = _time_calls(torch, [("m", lambda: tp.tp_row_linear_fwd_unfused(xc, w, yc, ws, chunk, phases=2))],
+                             steps, warmup, flush_buf)
+    u, _, _, _ = _time_calls(torch, [("u", lambda: tp.tp_row_linear_fwd_unfused(x, w, y, ws, chunk, phases=3))],
+                             steps, warmup, flush_buf)
+    del ws
+    return {"call": rr["call"], "chunk_m": chunk, "n_chunks": n, "c_ms": c, "m_ms": m,
+            "model_pipelined_ms": tp.tp_pipeline_time(c, m, n), "model_serial_ms": n * (c + m),
+            "fused_ms": fused_ms, "unfused_ms": u}
+
+
 def run_configs(args):
     import torch
     torch.cuda.set_device(0)
@@ -758,8 +791,8 @@ def run_configs(args):
     flush = torch.empty(256 << 20, dtype=torch.float32, device="cuda")   # 1 GiB > 2 x L2
     for name, setup in workloads(torch, tp):
         w = setup()
-        ms, per, mn, p90 = _time_calls(torch, w["calls"], max(10, args.steps), max(3, args.warmup),
-                                       flush if w["flush"] else None)
+        steps, warmup = max(50, args.steps), max(10, args.warmup)
+        ms, per, mn, p90 = _time_calls(torch, w["calls"], steps, warmup, flush if w["flush"] else None)
         tflops = w["flops"] / (ms / 1e3) / 1e12
         line = {"workload": name, "desc": w["desc"], "ms_per_step": ms, "ms_min": mn, "ms_p90": p90,
                 "tflops": tflops, "frac_of_bf16_sustained": tflops / pk["bf16_tflops_sustained"],
@@ -768,10 +801,14 @@ def run_configs(args):
         if w["bytes"]:
             gbs = w["bytes"] / (ms / 1e3) / 1e9
             line.update({"hbm_gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"], "bytes_per_step": w["bytes"]})
+        if w.get("row_reduce"):
+            rr = w["row_reduce"]
+            line["timeline"] = _row_timeline(torch, tp, rr, per[rr["call"]], steps, warmup,
+                                             flush if w["flush"] else None)
         del w
         torch.cuda.empty_cache()
         if name in UNSHARDED_GEMMS:
-            cms = _time_unsharded(torch, UNSHARDED_GEMMS[name], max(10, args.steps), max(3, args.warmup),
+            cms = _time_unsharded(torch, UNSHARDED_GEMMS[name], steps, warmup,
                                   flush if line["l2"].startswith("flushed") else None)
             line.update({"unsharded_torch_matmul_ms": cms,
                          "fused_speed_vs_unsharded_torch_matmul": cms / ms,

@@ -50,6 +50,7 @@ TP_DEBUG_TIMEOUT_MS = 0
 TP_DEBUG_DROP_LOAD = 1
 TP_DEBUG_TILE_MODE = 2
 TP_DEBUG_NO_TAIL_SLICES = 3
+TP_DEBUG_SPLIT_K = 4
 # tp_row_linear_fwd_unfused flags
 TP_UNFUSED_BF16_COLLECTIVE = 1
 

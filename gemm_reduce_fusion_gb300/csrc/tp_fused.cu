@@ -47,6 +47,7 @@ std::atomic<uint64_t> g_timeout_override_ns{0};
 std::atomic<int64_t> g_debug_drop_q{-1};
 std::atomic<int64_t> g_debug_tile_mode{0};  // 0 auto, 1 single-CTA tiles only, 2 CTA pairs whenever possible
 std::atomic<int64_t> g_debug_no_tail{0};    // 1: no k-slices in the last wave of pair launches
+std::atomic<int64_t> g_debug_split_k{0};    // n > 0: split-K factor of launches below one wave
 std::atomic<unsigned long long*> g_trace{nullptr};  // timeline trace buffer of the next launches
 std::atomic<int64_t> g_trace_cap{0};
 std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (slice counters)
@@ -330,19 +331,36 @@ void finish_shape(Shape* s) {
     }
   }
   if (s->units0 < kPlanSMs) {
-    // Deterministic split-K: choose the split that fills the SMs best, with
-    // at least 4 k-blocks per split and at most 16 splits.
-    double best_eff = 0.0;
+    // Deterministic split-K, at least 4 k-blocks per split and at most 16
+    // splits.  Every split adds an fp32 partial of the whole output to the
+    // second stage's reads, and the second stage is a launch of its own: the
+    // split is the largest that still runs all units in one wave.  A GEMM too
+    // small to repay the second stage is not split.  Where one wave leaves
+    // a quarter of the SMs idle on units of 256 k-blocks or more (skinny
+    // calls over long contractions, bound by HBM), the split that fills the
+    // SMs best over several waves keeps every SM streaming.
     int best = 1;
-    for (int ns = 1; ns <= 16; ++ns) {
-      if (ns > 1 && s->kb_total / ns < 4) break;
-      const int64_t u = s->units0 * ns;
-      const double eff = static_cast<double>(u) / (cdiv(u, kPlanSMs) * kPlanSMs);
-      if (eff > best_eff + 0.02) {
-        best_eff = eff;
-        best = ns;
+    for (int ns = 2; ns <= 16; ++ns) {
+      if (s->kb_total / ns < 4 || s->units0 * ns > kPlanSMs) break;
+      best = ns;
+    }
+    if (s->units0 * s->kb_total <= 256) {
+      best = 1;
+    } else if (s->kb_total / best >= 256 && 4 * s->units0 * best < 3 * kPlanSMs) {
+      double best_eff = 0.0;
+      best = 1;
+      for (int ns = 1; ns <= 16; ++ns) {
+        if (ns > 1 && s->kb_total / ns < 4) break;
+        const int64_t u = s->units0 * ns;
+        const double eff = static_cast<double>(u) / (cdiv(u, kPlanSMs) * kPlanSMs);
+        if (eff > best_eff + 0.02) {
+          best_eff = eff;
+          best = ns;
+        }
       }
     }
+    const int64_t forced = g_debug_split_k.load();
+    if (forced > 0) best = static_cast<int>(std::min<int64_t>(forced, s->kb_total));
     if (best > 1) {
       s->kb_per_split = cdiv(s->kb_total, best);
       s->n_split = static_cast<int>(cdiv(s->kb_total, s->kb_per_split));
@@ -742,6 +760,10 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_NO_TAIL_SLICES:
       if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
       g_debug_no_tail.store(value);
+      return TP_OK;
+    case TP_DEBUG_SPLIT_K:
+      if (value < 0 || value > 16) return TP_ERR_INVALID_ARG;
+      g_debug_split_k.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;

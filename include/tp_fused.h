@@ -325,12 +325,19 @@ tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* 
  *   TP_DEBUG_NO_TAIL_SLICES: 1 runs the last partial wave of a CTA-pair
  *     launch as whole tiles instead of k-slices; 0 (default) lets the
  *     planner slice it.
+ *   TP_DEBUG_SPLIT_K: 0 (default) lets the planner choose the split-K
+ *     factor of single-CTA launches with fewer tiles than SMs; n in 1..16
+ *     splits their contraction n ways instead (clamped to one k-block per
+ *     split; fp32 outputs still split further where they need it).  Changes
+ *     the workspace size of those calls; for parity testing of the split-K
+ *     path on shapes the planner would not split.
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
 typedef enum {
   TP_DEBUG_TIMEOUT_MS = 0,
   TP_DEBUG_DROP_LOAD = 1,
   TP_DEBUG_TILE_MODE = 2,
-  TP_DEBUG_NO_TAIL_SLICES = 3
+  TP_DEBUG_NO_TAIL_SLICES = 3,
+  TP_DEBUG_SPLIT_K = 4
 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 

@@ -108,6 +108,39 @@ def test_workspace_size(tp):
     assert tp.tp_workspace_size(tp.TP_OP_ROW_AR, 0, 16, 16, 16, 0) == 256
 
 
+def test_split_plan_and_forced_split(tp):
+    """The split-K factor of launches below one wave: the largest that keeps
+    every unit in one wave, none for a GEMM too small to repay the second
+    stage, the SM-filling split for HBM-bound skinny calls over long
+    contractions; TP_DEBUG_SPLIT_K overrides it (fp32 partials: one copy of
+    the output per split)."""
+    def splits(op, p, M, N, K, chunk):
+        return (tp.tp_workspace_size(op, p, M, N, K, chunk) - 256) / (M * N * 4)
+    AR = tp.TP_OP_ROW_AR
+    # [128, 2048] output in 64 swapped tiles of 32 tokens, 32 k-blocks: 2 splits fill one wave
+    assert splits(AR, 2, 128, 2048, 1024, 32) == 2
+    # 32 tiles of 128 x 256, 64 k-blocks: 4 splits
+    assert splits(AR, 4, 1024, 1024, 1024, 0) == 4
+    # 9 tiles x 8 k-blocks: not split
+    assert splits(AR, 2, 300, 520, 200, 0) == 0
+    # decode: 96 swapped tiles of 16 tokens over 768 k-blocks fill the SMs over several waves
+    assert splits(AR, 8, 16, 12288, 6144, 0) == 11
+    try:
+        assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 3) == tp.TP_OK
+        assert splits(AR, 2, 300, 520, 200, 0) == 3
+        assert splits(AR, 2, 128, 2048, 1024, 32) == 3
+        # clamped to one k-block per split: 1 x [64, 64] per rank, p = 2
+        assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 16) == tp.TP_OK
+        assert splits(AR, 2, 64, 64, 64, 0) == 2
+        # launches of a wave or more are not split
+        assert tp.tp_workspace_size(AR, 2, 4864, 2048, 1024, 0, tp.TP_BF16) == 256
+        assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 17) == tp.TP_ERR_INVALID_ARG
+        assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, -1) == tp.TP_ERR_INVALID_ARG
+    finally:
+        tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 0)
+    assert splits(AR, 2, 300, 520, 200, 0) == 0
+
+
 def test_workspace_holds_the_last_wave_slices(tp):
     """bf16 outputs on CTA pairs: 4096 x 4096 is 256 pair tiles, 3 full waves
     of 76 clusters and 28 tiles cut into 2 k-slices: one fp32 256 x 256 tile

@@ -94,3 +94,4 @@ def test_debug_hook_argument_checks(tp):
     assert tp.tp_debug_set(tp.TP_DEBUG_TIMEOUT_MS, -5) == tp.TP_ERR_INVALID_ARG
     assert tp.tp_debug_set(tp.TP_DEBUG_DROP_LOAD, -2) == tp.TP_ERR_INVALID_ARG
     assert tp.tp_debug_set(tp.TP_DEBUG_NO_TAIL_SLICES, 2) == tp.TP_ERR_INVALID_ARG
+    assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 17) == tp.TP_ERR_INVALID_ARG

@@ -72,6 +72,16 @@ def ws_for(tp, op, p, M, N, K, chunk):
     return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
+@pytest.fixture(params=[0, 3], ids=["planned_split", "split3"])
+def split_k(tp, request):
+    """The planner's split-K factor (0), or every single-CTA launch below one
+    wave split 3 ways: the split-K partials and the second stage's epilogues
+    then run on the small shapes the planner leaves whole."""
+    assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, request.param) == tp.TP_OK
+    yield request.param
+    tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 0)
+
+
 ROW_CASES = [  # p, M, N, K, chunk_m
     (1, 128, 256, 64, 0),
     (2, 300, 520, 200, 0),
@@ -87,7 +97,7 @@ ROW_CASES = [  # p, M, N, K, chunk_m
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", ROW_CASES)
-def test_row_allreduce_exact(tp, p, M, N, K, chunk, f32):
+def test_row_allreduce_exact(tp, split_k, p, M, N, K, chunk, f32):
     xs = [ints((M, K), 100 + r) for r in range(p)]
     ws = [ints((K, N), 200 + r) for r in range(p)]
     ref = oracle.row_fwd_allreduce(xs, ws)
@@ -99,7 +109,7 @@ def test_row_allreduce_exact(tp, p, M, N, K, chunk, f32):
 
 
 @pytest.mark.parametrize("p,M,N,K,chunk", [(2, 300, 520, 200, 0), (4, 130, 136, 72, 32)])
-def test_row_allreduce_replicas_identical(tp, p, M, N, K, chunk):
+def test_row_allreduce_replicas_identical(tp, split_k, p, M, N, K, chunk):
     xs = [ints((M, K), 110 + r) for r in range(p)]
     ws = [ints((K, N), 210 + r) for r in range(p)]
     y = outs([(M, N)] * p, False)
@@ -118,7 +128,7 @@ RS_CASES = [(2, 128, 2048, 1024, 32), (2, 300, 520, 200, 0), (4, 520, 264, 136, 
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", RS_CASES)
-def test_row_reducescatter_exact(tp, p, M, N, K, chunk, f32):
+def test_row_reducescatter_exact(tp, split_k, p, M, N, K, chunk, f32):
     xs = [ints((M, K), 120 + r) for r in range(p)]
     ws = [ints((K, N), 220 + r) for r in range(p)]
     refs = oracle.row_fwd_reducescatter(xs, ws)
@@ -141,7 +151,7 @@ COL_CASES = [(1, 128, 256, 64, 0), (3, 300, 264, 136, 0), (4, 257, 520, 200, 128
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", COL_CASES)
-def test_col_fwd_exact(tp, p, M, N, K, chunk, f32):
+def test_col_fwd_exact(tp, split_k, p, M, N, K, chunk, f32):
     x = ints((M, K), 130)
     ws = [ints((K, N), 230 + k) for k in range(p)]
     refs, _ = oracle.col_fwd(x, ws)
@@ -154,7 +164,7 @@ def test_col_fwd_exact(tp, p, M, N, K, chunk, f32):
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", [(3, 300, 264, 136, 0), (2, 100, 136, 200, 16), (4, 260, 520, 72, 64)])
-def test_col_fwd_gelu(tp, p, M, N, K, chunk, f32):
+def test_col_fwd_gelu(tp, split_k, p, M, N, K, chunk, f32):
     # H ~ N(0, 1): the GeLU curve itself is exercised
     x = synth.normal_bf16((M, K), 131, sigma=1.0 / np.sqrt(K))
     ws = [synth.normal_bf16((K, N), 231 + k) for k in range(p)]
@@ -181,7 +191,7 @@ COLB_CASES = [(1, 128, 256, 64, 0), (3, 300, 136, 264, 0), (4, 257, 72, 520, 128
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", COLB_CASES)
-def test_col_bwd_exact(tp, p, M, N, K, chunk, f32):
+def test_col_bwd_exact(tp, split_k, p, M, N, K, chunk, f32):
     x = ints((M, K), 140)
     ws = [ints((K, N), 240 + k) for k in range(p)]
     dys = [ints((M, N), 340 + k) for k in range(p)]
@@ -203,7 +213,7 @@ ROWB_CASES = [(1, 128, 256, 64, 0), (3, 300, 136, 264, 0), (4, 257, 520, 72, 128
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", ROWB_CASES)
-def test_row_bwd_exact(tp, p, M, N, K, chunk, f32):
+def test_row_bwd_exact(tp, split_k, p, M, N, K, chunk, f32):
     xs = [ints((M, K), 150 + k) for k in range(p)]
     ws = [ints((K, N), 250 + k) for k in range(p)]
     dy = ints((M, N), 350)
@@ -222,7 +232,7 @@ def test_row_bwd_exact(tp, p, M, N, K, chunk, f32):
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", [(3, 300, 136, 264, 0), (2, 100, 136, 200, 16), (4, 130, 64, 72, 64)])
-def test_row_bwd_dgelu(tp, p, M, N, K, chunk, f32):
+def test_row_bwd_dgelu(tp, split_k, p, M, N, K, chunk, f32):
     ws = [synth.normal_bf16((K, N), 251 + k, sigma=1.0 / np.sqrt(N)) for k in range(p)]
     dy = synth.normal_bf16((M, N), 351)
     hs = [synth.normal_bf16((M, K), 451 + k) for k in range(p)]
@@ -242,7 +252,7 @@ AG_CASES = [(2, 256, 264, 136, 0), (4, 512, 136, 200, 128), (4, 400, 72, 72, 0),
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", AG_CASES)
-def test_ag_matmul_exact(tp, p, M, N, K, chunk, f32):
+def test_ag_matmul_exact(tp, split_k, p, M, N, K, chunk, f32):
     Mp = M // p
     xs = [ints((Mp, K), 160 + s) for s in range(p)]
     ws = [ints((K, N), 260 + k) for k in range(p)]
@@ -258,7 +268,7 @@ def test_ag_matmul_exact(tp, p, M, N, K, chunk, f32):
 
 
 @pytest.mark.parametrize("p,M,N,K,chunk", [(4, 512, 264, 136, 0), (2, 100, 136, 64, 16)])
-def test_ag_matmul_gelu(tp, p, M, N, K, chunk):
+def test_ag_matmul_gelu(tp, split_k, p, M, N, K, chunk):
     Mp = M // p
     xs = [synth.normal_bf16((Mp, K), 161 + s, sigma=1.0 / np.sqrt(K)) for s in range(p)]
     ws = [synth.normal_bf16((K, N), 261 + k) for k in range(p)]
@@ -318,13 +328,13 @@ def ibias(n, seed):
     return ints((1, n), seed)[0]
 
 
-BIAS_ROW_CASES = [  # p, M, N, K, chunk_m: split-K (second-stage bias), operand-swapped, K == 0
+BIAS_ROW_CASES = [  # p, M, N, K, chunk_m: 128x256 tiles, operand-swapped, K == 0
     (2, 300, 520, 200, 0), (3, 130, 136, 72, 32), (4, 64, 264, 64, 16), (2, 40, 72, 0, 0)]
 
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K,chunk", BIAS_ROW_CASES)
-def test_row_bias_exact(tp, p, M, N, K, chunk, f32):
+def test_row_bias_exact(tp, split_k, p, M, N, K, chunk, f32):
     """Y = sum_r X_r W_r + b (b once, after the reduction), AllReduce with
     replicas and ReduceScatter."""
     xs = [ints((M, K), 600 + r) for r in range(p)]
@@ -362,7 +372,7 @@ def test_row_bias_direct_epilogue_both_tile_paths(tp, tile_mode):
 
 @pytest.mark.parametrize("p,M,N,K,chunk", [(2, 300, 264, 136, 0), (3, 77, 136, 72, 64), (2, 2048, 1280, 64, 0),
                                            (2, 24, 72, 0, 0)])
-def test_column_and_allgather_bias(tp, p, M, N, K, chunk):
+def test_column_and_allgather_bias(tp, split_k, p, M, N, K, chunk):
     """H_k = X A_k + b_k before the GeLU: H exact on integers, GeLU(H) within
     the fp32 tolerance; the AllGather+MatMul form routes b_k by shard k."""
     x = ints((M, K), 640)
@@ -399,7 +409,7 @@ def test_column_and_allgather_bias(tp, p, M, N, K, chunk):
 
 @pytest.mark.parametrize("f32", [True, False])
 @pytest.mark.parametrize("p,M,N,K", [(2, 300, 72, 64), (4, 1024, 264, 136), (3, 96, 520, 72), (2, 0, 136, 64)])
-def test_bias_gradients_exact(tp, p, M, N, K, f32):
+def test_bias_gradients_exact(tp, split_k, p, M, N, K, f32):
     """db = the row sums of dY on integer inputs (exact in fp32): column
     backward (one per shard), row backward, AllGather+MatMul backward (with
     dW in the same call) and the ReduceScatter backward (summed over the
@@ -922,7 +932,7 @@ SP_BWD_CASES = [  # p, M, N, K, chunk_m
 
 @pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
 @pytest.mark.parametrize("p,M,N,K,chunk", SP_BWD_CASES)
-def test_ag_matmul_bwd_exact(tp, tile_mode, p, M, N, K, chunk):
+def test_ag_matmul_bwd_exact(tp, tile_mode, split_k, p, M, N, K, chunk):
     Mp = M // p
     xs = [ints((Mp, K), 600 + s) for s in range(p)]
     ws = [ints((K, N), 610 + k) for k in range(p)]
@@ -939,7 +949,7 @@ def test_ag_matmul_bwd_exact(tp, tile_mode, p, M, N, K, chunk):
 
 @pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
 @pytest.mark.parametrize("p,M,N,K,chunk", SP_BWD_CASES)
-def test_row_bwd_reducescatter_exact(tp, tile_mode, p, M, N, K, chunk):
+def test_row_bwd_reducescatter_exact(tp, tile_mode, split_k, p, M, N, K, chunk):
     Mp = M // p
     xs = [ints((M, K), 630 + r) for r in range(p)]
     ws = [ints((K, N), 640 + r) for r in range(p)]
@@ -957,7 +967,7 @@ def test_row_bwd_reducescatter_exact(tp, tile_mode, p, M, N, K, chunk):
 
 
 @pytest.mark.parametrize("p,M,N,K,chunk", [(4, 512, 256, 192, 0), (2, 128, 136, 64, 32)])
-def test_row_bwd_reducescatter_dgelu(tp, p, M, N, K, chunk):
+def test_row_bwd_reducescatter_dgelu(tp, split_k, p, M, N, K, chunk):
     Mp = M // p
     ws = [synth.normal_bf16((K, N), 660 + r, sigma=1.0 / np.sqrt(N)) for r in range(p)]
     dys = [synth.normal_bf16((Mp, N), 670 + s) for s in range(p)]
