@@ -659,6 +659,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up above touches no global memory: it overlaps the previous kernel
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -909,6 +912,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync_all();  // both CTAs' barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up above touches no global memory: it overlaps the previous kernel
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {

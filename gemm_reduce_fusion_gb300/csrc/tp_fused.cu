@@ -197,6 +197,11 @@ cudaError_t launch_pair_t(const GemmParams& P, int clusters, cudaStream_t s) {
       cfg.gridDim = dim3(2 * clusters, 1, 1);
     }
   }
+  cudaLaunchAttribute attr2[2] = {attr[0], {}};
+  attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr2[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr2;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, P);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -215,7 +220,18 @@ cudaError_t launch_t(const GemmParams& P, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  k<<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(P);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, P);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -46,6 +46,10 @@
  *    workspace that still holds the plan without last-wave slices is
  *    accepted, and the call then runs without them.
  *    Calls that share a workspace must be ordered on the same stream.
+ *    The GEMM kernels use programmatic dependent launch: a kernel's set-up
+ *    (barriers, tensor memory) may overlap the end of the previous kernel in
+ *    the stream, but it reads and writes global memory only after that
+ *    kernel has completed, so stream order is kept as for plain launches.
  *  - Any host thread may call; a call runs on that thread's current CUDA
  *    device (the library makes the device's primary context current).
  *  - Biases (forward) and bias gradients (backward) are optional bf16 /
