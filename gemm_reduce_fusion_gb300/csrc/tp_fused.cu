@@ -185,15 +185,20 @@ cudaError_t launch_pair_t(const GemmParams& P, int clusters, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // no more clusters than can be resident at once (persistent tiles)
-  static int max_active[64] = {};  // per device and instantiation
+  // (per device and instantiation; threads that race to fill it store the same value)
+  static std::atomic<int> max_active[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
-    if (max_active[dev] == 0) {
+    int m = max_active[dev].load(std::memory_order_relaxed);
+    if (m == 0) {
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0) max_active[dev] = n;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0) {
+        m = n;
+        max_active[dev].store(n, std::memory_order_relaxed);
+      }
     }
-    if (max_active[dev] > 0 && clusters > max_active[dev]) {
-      clusters = max_active[dev];
+    if (m > 0 && clusters > m) {
+      clusters = m;
       cfg.gridDim = dim3(2 * clusters, 1, 1);
     }
   }
