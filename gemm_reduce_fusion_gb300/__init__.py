@@ -2,8 +2,11 @@
 
 Every function here has the name of the C entry point it calls
 (``include/tp_fused.h``).  It reads shapes from the torch tensors it is
-given, passes their device pointers and the current CUDA stream to the
-shared library, and raises :class:`TPError` on a non-zero status.  All
+given and checks that every shard, output and bias has the shape, dtype,
+layout and device the call implies (the C ABI sees only pointers, so a
+wrong-sized buffer would otherwise be read or written out of bounds on the
+device); it then passes the device pointers and the current CUDA stream to
+the shared library and raises :class:`TPError` on a non-zero status.  All
 arithmetic runs in the library's CUDA kernels; there is no fallback: if the
 library is missing the import fails.
 
@@ -157,6 +160,52 @@ def _check(status: int, where: str) -> None:
         raise TPError(status, where)
 
 
+# ------------------------------------------------------------------ argument checks
+#
+# The C ABI takes one M, N, K for all shards and plain pointers: it cannot see
+# how large a buffer is, so a shard of the wrong shape would be read or
+# written out of bounds on the device.  The binding knows every tensor's
+# shape and checks them on the host before anything is enqueued: shape,
+# bfloat16 for inputs, row-major layout, and the calling thread's current
+# CUDA device (the device the library runs the call on).  None stands for a
+# NULL pointer; the library decides where NULL is allowed.
+
+def _current_device() -> int:
+    import torch
+    return torch.cuda.current_device()
+
+
+def _need(where: str, name: str, t, shape, bf16: bool, dev: int) -> None:
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{where}: {name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if bf16:
+        import torch
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{where}: {name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{where}: {name} must be contiguous (row-major)")
+    if t.get_device() != dev:
+        raise TypeError(f"{where}: {name} is on {t.device}; the call runs on cuda:{dev}, "
+                        "the calling thread's current device")
+
+
+def _need_all(where: str, name: str, ts, counts, shape, bf16: bool, dev: int) -> None:
+    if ts is None:
+        return
+    if len(ts) not in counts:
+        raise ValueError(f"{where}: {name} holds {len(ts)} tensors, expected "
+                         + " or ".join(str(c) for c in counts))
+    for i, t in enumerate(ts):
+        _need(where, f"{name}[{i}]", t, shape, bf16, dev)
+
+
+def _need_ws(where: str, ws, dev: int) -> None:
+    if ws.get_device() != dev:
+        raise TypeError(f"{where}: the workspace is on {ws.device}; the call runs on cuda:{dev}")
+
+
 # ------------------------------------------------------------------ host-only calls
 
 def tp_status_string(status: int) -> str:
@@ -221,6 +270,12 @@ def tp_row_linear_fwd_allreduce(x: Sequence, w: Sequence, y: Sequence, ws, chunk
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
+    W, dev = "tp_row_linear_fwd_allreduce", _current_device()
+    _need_all(W, "x", x, (p,), (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "y", y, (1, p), (M, N), False, dev)
+    _need(W, "bias", bias, (N,), True, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_fwd_allreduce(_arr(x), _arr(w), _ptr(bias), _arr(y), len(y), p, M, N, K, chunk_m,
                                             _dtype_code(y[0]), wp, wb, _stream(stream)),
@@ -233,6 +288,12 @@ def tp_row_linear_fwd_reducescatter(x: Sequence, w: Sequence, y: Sequence, ws, c
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
+    W, dev = "tp_row_linear_fwd_reducescatter", _current_device()
+    _need_all(W, "x", x, (p,), (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "y", y, (p,), (M // p, N), False, dev)
+    _need(W, "bias", bias, (N,), True, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_fwd_reducescatter(_arr(x), _arr(w), _ptr(bias), _arr(y), p, M, N, K, chunk_m,
                                                 _dtype_code(y[0]), wp, wb, _stream(stream)),
@@ -245,6 +306,13 @@ def tp_col_linear_fwd(x, w: Sequence, y: Sequence, ws, epi: int = TP_EPI_NONE, p
     p = len(w)
     M, K = x.shape
     N = w[0].shape[1]
+    W, dev = "tp_col_linear_fwd", _current_device()
+    _need(W, "x", x, (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "y", y, (p,), (M, N), False, dev)
+    _need_all(W, "preact", preact, (p,), (M, N), False, dev)
+    _need_all(W, "bias", bias, (p,), (N,), True, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_col_linear_fwd(_ptr(x), _arr(w), _arr(bias), _arr(y), _arr(preact), epi, p, M, N, K, chunk_m,
                                   _out_dtype(y, preact), wp, wb, _stream(stream)), "tp_col_linear_fwd")
@@ -256,6 +324,14 @@ def tp_col_linear_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0]
+    W, dev = "tp_col_linear_bwd", _current_device()
+    _need(W, "x", x, (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "dy", dy, (p,), (M, N), True, dev)
+    _need(W, "dx", dx, (M, K), False, dev)
+    _need_all(W, "dw", dw, (p,), (K, N), False, dev)
+    _need_all(W, "db", db, (p,), (N,), False, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_col_linear_bwd(_ptr(x), _arr(w), _arr(dy), _ptr(dx), _arr(dw), _arr(db), p, M, N, K,
                                   chunk_m, _out_dtype(dx, dw, db), wp, wb, _stream(stream)), "tp_col_linear_bwd")
@@ -267,6 +343,15 @@ def tp_row_linear_bwd(x, w: Sequence, dy, dx, dw, ws, preact=None, chunk_m: int 
     p = len(w)
     K, N = w[0].shape
     M = dy.shape[0]
+    W, dev = "tp_row_linear_bwd", _current_device()
+    _need_all(W, "x", x, (p,), (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need(W, "dy", dy, (M, N), True, dev)
+    _need_all(W, "dx", dx, (p,), (M, K), False, dev)
+    _need_all(W, "dw", dw, (p,), (K, N), False, dev)
+    _need(W, "db", db, (N,), False, dev)
+    _need_all(W, "preact", preact, (p,), (M, K), True, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_bwd(_arr(x), _arr(w), _ptr(dy), _arr(dx), _arr(dw), _ptr(db), _arr(preact), p,
                                   M, N, K, chunk_m, _out_dtype(dx, dw, db), wp, wb, _stream(stream)),
@@ -279,6 +364,14 @@ def tp_ag_matmul(x: Sequence, w: Sequence, y: Sequence, ws, x_gathered=None,
     p = len(x)
     Mp, K = x[0].shape
     N = w[0].shape[1]
+    W, dev = "tp_ag_matmul", _current_device()
+    _need_all(W, "x", x, (p,), (Mp, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "y", y, (p,), (Mp * p, N), False, dev)
+    _need(W, "x_gathered", x_gathered, (Mp * p, K), True, dev)
+    _need_all(W, "preact", preact, (p,), (Mp * p, N), False, dev)
+    _need_all(W, "bias", bias, (p,), (N,), True, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_ag_matmul(_arr(x), _arr(w), _arr(bias), _arr(y), _ptr(x_gathered), epi, _arr(preact), p,
                              Mp * p, N, K, chunk_m, _out_dtype(y, preact), wp, wb, _stream(stream)),
@@ -291,6 +384,14 @@ def tp_ag_matmul_bwd(x, w: Sequence, dy: Sequence, dx, dw, ws, chunk_m: int = 0,
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0]
+    W, dev = "tp_ag_matmul_bwd", _current_device()
+    _need_all(W, "x", x, (p,), (M // p, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "dy", dy, (p,), (M, N), True, dev)
+    _need_all(W, "dx", dx, (p,), (M // p, K), False, dev)
+    _need_all(W, "dw", dw, (p,), (K, N), False, dev)
+    _need_all(W, "db", db, (p,), (N,), False, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_ag_matmul_bwd(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), _arr(db), p, M, N, K, chunk_m,
                                  _out_dtype(dx, dw, db), wp, wb, _stream(stream)), "tp_ag_matmul_bwd")
@@ -303,6 +404,15 @@ def tp_row_linear_bwd_reducescatter(x, w: Sequence, dy: Sequence, dx, dw, ws, pr
     p = len(w)
     K, N = w[0].shape
     M = dy[0].shape[0] * p
+    W, dev = "tp_row_linear_bwd_reducescatter", _current_device()
+    _need_all(W, "x", x, (p,), (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "dy", dy, (p,), (M // p, N), True, dev)
+    _need_all(W, "dx", dx, (p,), (M, K), False, dev)
+    _need_all(W, "dw", dw, (p,), (K, N), False, dev)
+    _need(W, "db", db, (N,), False, dev)
+    _need_all(W, "preact", preact, (p,), (M, K), True, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_bwd_reducescatter(_arr(x), _arr(w), _arr(dy), _arr(dx), _arr(dw), _ptr(db),
                                                 _arr(preact), p, M, N, K, chunk_m, _out_dtype(dx, dw, db), wp, wb,
@@ -316,6 +426,11 @@ def tp_row_linear_fwd_unfused(x: Sequence, w: Sequence, y, ws, chunk_m: int = 0,
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
+    W, dev = "tp_row_linear_fwd_unfused", _current_device()
+    _need_all(W, "x", x, (p,), (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need(W, "y", y, (M, N), False, dev)
+    _need_ws(W, ws, dev)
     wp, wb = _ws(ws)
     _check(_lib.tp_row_linear_fwd_unfused(_arr(x), _arr(w), _ptr(y), p, M, N, K, chunk_m, _dtype_code(y),
                                           phases, flags, wp, wb, _stream(stream)), "tp_row_linear_fwd_unfused")
@@ -333,5 +448,9 @@ def tp_row_linear_fwd_allreduce_noalloc(x: Sequence, w: Sequence, y: Sequence, c
     p = len(x)
     M, K = x[0].shape
     N = w[0].shape[1]
+    W, dev = "tp_row_linear_fwd_allreduce_noalloc", _current_device()
+    _need_all(W, "x", x, (p,), (M, K), True, dev)
+    _need_all(W, "w", w, (p,), (K, N), True, dev)
+    _need_all(W, "y", y, (1, p), (M, N), False, dev)
     _check(fn(_arr(x), _arr(w), _arr(y), len(y), p, M, N, K, chunk_m, _dtype_code(y[0]), _stream(stream)),
            "tp_row_linear_fwd_allreduce_noalloc")
