@@ -583,7 +583,7 @@ def workloads(torch, tp):
     bf = dict(dtype=torch.bfloat16, device="cuda")
 
     def w1():
-        d = _dev_all(torch, synth.config1_inputs())
+        d = _dev_all(torch, synth.worked_example_inputs())
         p, M, K, N = 2, 128, 1024, 2048
         y = torch.empty((M, N), **bf)
         ys = [torch.empty((M // p, N), **bf) for _ in range(p)]
@@ -597,7 +597,7 @@ def workloads(torch, tp):
                     desc="row-parallel p=2, X_r[128,1024], W_r[1024,2048], AllReduce + ReduceScatter, chunk_m=32")
 
     def w2():
-        d = _dev_all(torch, synth.config2_inputs())
+        d = _dev_all(torch, synth.mlp_block_inputs())
         p, M, h, nk = 4, 4096, 4096, 4096
         Z = [torch.empty((M, nk), **bf) for _ in range(p)]
         Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
@@ -620,7 +620,7 @@ def workloads(torch, tp):
             desc="Megatron MLP block fwd+bwd p=4, 4096 tokens, h=4096, ffn=16384")
 
     def w3():
-        d = _dev_all(torch, synth.config3_inputs())
+        d = _dev_all(torch, synth.mha_projection_inputs())
         p, M, h, nq, no = 4, 4096, 4096, 3072, 1024
         QKV = [torch.empty((M, nq), **bf) for _ in range(p)]
         Y = torch.empty((M, h), **bf)
@@ -640,7 +640,7 @@ def workloads(torch, tp):
             desc="MHA projections fwd+bwd p=4, 4096 tokens, h=4096, QKV [4096,3072]/shard, W_O [1024,4096]/shard")
 
     def w4():
-        d = _dev_all(torch, synth.config4_inputs())
+        d = _dev_all(torch, synth.sequence_parallel_pair_inputs())
         p, Mp, h, nk = 8, 1024, 8192, 3584
         M = p * Mp
         Z = [torch.empty((M, nk), **bf) for _ in range(p)]
@@ -655,7 +655,7 @@ def workloads(torch, tp):
             desc="sequence-parallel pair fwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672")
 
     def w4b():
-        d = _dev_all(torch, synth.config4_inputs())
+        d = _dev_all(torch, synth.sequence_parallel_pair_inputs())
         p, Mp, h, nk = 8, 1024, 8192, 3584
         M = p * Mp
         dys = _dev_all(torch, {"dy": [synth.normal_bf16((Mp, h), synth.seed_for(43, s)) for s in range(p)]})["dy"]
@@ -679,7 +679,7 @@ def workloads(torch, tp):
 
     def w5(M):
         def setup():
-            d = _dev_all(torch, synth.config5_inputs(M))
+            d = _dev_all(torch, synth.gpt3_mlp_inputs(M))
             p, h, nk = 8, 12288, 6144
             Z = [torch.empty((M, nk), **bf) for _ in range(p)]
             Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
@@ -696,8 +696,8 @@ def workloads(torch, tp):
                 desc=f"GPT-3-scale MLP fwd p=8, h=12288, ffn=49152, M={M}")
         return setup
 
-    return [("config1", w1), ("config2", w2), ("config3", w3), ("config4", w4), ("config4_fwd_bwd", w4b),
-            ("config5_m2048", w5(2048)), ("config5_m16", w5(16))]
+    return [("worked_example_p2", w1), ("mlp_block_p4", w2), ("mha_projections_p4", w3), ("sp_pair_fwd_p8", w4), ("sp_pair_fwd_bwd_p8", w4b),
+            ("gpt3_mlp_p8_m2048", w5(2048)), ("gpt3_mlp_p8_m16", w5(16))]
 
 
 def _time_calls(torch, calls, steps, warmup, flush_buf=None):
@@ -728,16 +728,16 @@ def _time_calls(torch, calls, steps, warmup, flush_buf=None):
 # matmuls: context for each workload (a GEMM library on the concatenated
 # weights, with no reduction or gather to do), not part of the measured path.
 UNSHARDED_GEMMS = {
-    "config1": [(128, 2048, 2048)] * 2,
-    "config2": [(4096, 4096, 16384), (4096, 16384, 4096), (4096, 4096, 16384), (16384, 4096, 4096),
+    "worked_example_p2": [(128, 2048, 2048)] * 2,
+    "mlp_block_p4": [(4096, 4096, 16384), (4096, 16384, 4096), (4096, 4096, 16384), (16384, 4096, 4096),
                 (4096, 16384, 4096), (4096, 4096, 16384)],
-    "config3": [(4096, 4096, 12288), (4096, 4096, 4096), (4096, 4096, 4096), (4096, 4096, 4096),
+    "mha_projections_p4": [(4096, 4096, 12288), (4096, 4096, 4096), (4096, 4096, 4096), (4096, 4096, 4096),
                 (4096, 12288, 4096), (4096, 4096, 12288)],
-    "config4": [(8192, 8192, 28672), (8192, 28672, 8192)],
-    "config4_fwd_bwd": [(8192, 8192, 28672), (8192, 28672, 8192), (8192, 8192, 28672), (28672, 8192, 8192),
+    "sp_pair_fwd_p8": [(8192, 8192, 28672), (8192, 28672, 8192)],
+    "sp_pair_fwd_bwd_p8": [(8192, 8192, 28672), (8192, 28672, 8192), (8192, 8192, 28672), (28672, 8192, 8192),
                         (8192, 28672, 8192), (8192, 8192, 28672)],
-    "config5_m2048": [(2048, 12288, 49152), (2048, 49152, 12288)],
-    "config5_m16": [(16, 12288, 49152), (16, 49152, 12288)],
+    "gpt3_mlp_p8_m2048": [(2048, 12288, 49152), (2048, 49152, 12288)],
+    "gpt3_mlp_p8_m16": [(16, 12288, 49152), (16, 49152, 12288)],
 }
 
 
@@ -827,7 +827,7 @@ def run_sweep(args):
     import gemm_reduce_fusion_gb300 as tp
     import synth
     M, p, h, nk = 2048, 8, 12288, 6144
-    d = _dev_all(torch, synth.config5_inputs(M))
+    d = _dev_all(torch, synth.gpt3_mlp_inputs(M))
     bf = dict(dtype=torch.bfloat16, device="cuda")
     Z = [torch.empty((M, nk), **bf) for _ in range(p)]
     Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
@@ -923,10 +923,10 @@ def run_precision_report(args):
         torch.cuda.empty_cache()
 
     # worked example: p = 2
-    d = _dev_all(torch, synth.config1_inputs())
+    d = _dev_all(torch, synth.worked_example_inputs())
     row_layer("row-parallel worked example (p=2, X_r[128,1024], W_r[1024,2048])", d["x"], d["w"])
     # MLP block: FC2 forward on the GPU's own GeLU output, then the backward's gradients
-    d = _dev_all(torch, synth.config2_inputs())
+    d = _dev_all(torch, synth.mlp_block_inputs())
     p, M, h, nk = 4, 4096, 4096, 4096
     Z = [torch.empty((M, nk), **bf) for _ in range(p)]
     Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
@@ -968,12 +968,12 @@ def run_precision_report(args):
     del w1t, DZ, Z, Hh, d
     torch.cuda.empty_cache()
     # MHA output projection
-    d = _dev_all(torch, synth.config3_inputs())
+    d = _dev_all(torch, synth.mha_projection_inputs())
     row_layer("MHA W_O forward (p=4, 4096 tokens, K_r=1024, h=4096)", d["o"], d["wo"])
     del d
     torch.cuda.empty_cache()
     # GPT-3-scale FC2, p = 8
-    d = _dev_all(torch, synth.config5_inputs(2048))
+    d = _dev_all(torch, synth.gpt3_mlp_inputs(2048))
     p, M, h, nk = 8, 2048, 12288, 6144
     Z = [torch.empty((M, nk), **bf) for _ in range(p)]
     w0 = ws([(tp.TP_OP_COL_FWD, p, M, nk, h, 0)])
@@ -1036,13 +1036,13 @@ def run_trace(args):
     import gemm_reduce_fusion_gb300 as tp
     import synth
     cases = []
-    d1 = _dev_all(torch, synth.config1_inputs())
+    d1 = _dev_all(torch, synth.worked_example_inputs())
     y1 = torch.empty((128, 2048), dtype=torch.bfloat16, device="cuda")
     ws1 = _ws_for(torch, tp, [(tp.TP_OP_ROW_AR, 2, 128, 2048, 1024, 32)])
     cases.append(("worked example: row AllReduce p=2, M=128, chunk_m=32",
                   lambda: tp.tp_row_linear_fwd_allreduce(d1["x"], d1["w"], [y1], ws1, 32)))
     M, p, h, nk = 2048, 8, 12288, 6144
-    d5 = _dev_all(torch, synth.config5_inputs(M))
+    d5 = _dev_all(torch, synth.gpt3_mlp_inputs(M))
     z5 = [torch.empty((M, nk), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     y5 = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
     for c in (256, 1024, 2048):

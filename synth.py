@@ -138,21 +138,22 @@ def ramp_bf16(rows: int, cols: int, scale: float = 1.0) -> np.ndarray:
 # --------------------------------------------------------------- workload recipes
 # Shapes, value distributions and seeds of the five sharded-Linear workloads.
 # Each recipe only names tensors and draws them; what is computed from them
-# lives in the library (GPU) and in the oracle (CPU).  Tensor group g of
-# workload c draws from seed_for(10 * c + g, shard).
+# lives in the library (GPU) and in the oracle (CPU).  Each recipe has its
+# own seed namespace c (1 to 5, in the order below): tensor group g draws
+# from seed_for(10 * c + g, shard).
 
 def _sd(c, g, k=0):
     return seed_for(10 * c + g, k)
 
 
-def config1_inputs():
+def worked_example_inputs():
     """Row-parallel Linear, p = 2: X_r [128, 1024], W_r [1024, 2048], N(0,1)/sqrt(2048)."""
     s = 1.0 / np.sqrt(2048.0)
     return {"x": [normal_bf16((128, 1024), _sd(1, 0, r), s) for r in range(2)],
             "w": [normal_bf16((1024, 2048), _sd(1, 1, r), s) for r in range(2)]}
 
 
-def config2_inputs():
+def mlp_block_inputs():
     """MLP block, p = 4, 4096 tokens, h = 4096, ffn = 16384: X, dY N(0,1); W N(0, 0.02)."""
     p, m, h, nk = 4, 4096, 4096, 4096
     return {"x": normal_bf16((m, h), _sd(2, 0)),
@@ -161,7 +162,7 @@ def config2_inputs():
             "dy": normal_bf16((m, h), _sd(2, 3))}
 
 
-def config3_inputs():
+def mha_projection_inputs():
     """MHA projections, p = 4, 2 x 2048 tokens, h = 4096, 8 heads x 128 per shard:
     X, attention output O_k, dY, dQKV_k N(0,1); W_qkv_k [4096, 3072], W_O_k [1024, 4096] N(0, 0.02)."""
     p, m, h = 4, 4096, 4096
@@ -173,7 +174,7 @@ def config3_inputs():
             "dqkv": [normal_bf16((m, 3 * 1024), _sd(3, 5, k)) for k in range(p)]}
 
 
-def config4_inputs():
+def sequence_parallel_pair_inputs():
     """Sequence-parallel pair, p = 8: X_r [1024, 8192] N(0,1); W1_k [8192, 3584], W2_k [3584, 8192] N(0, 0.02)."""
     p = 8
     return {"x": [normal_bf16((1024, 8192), _sd(4, 0, r)) for r in range(p)],
@@ -181,7 +182,7 @@ def config4_inputs():
             "w2": [normal_bf16((3584, 8192), _sd(4, 2, k), 0.02) for k in range(p)]}
 
 
-def config5_inputs(m: int):
+def gpt3_mlp_inputs(m: int):
     """GPT-3-scale MLP, p = 8, h = 12288, ffn = 49152: X [m, 12288] N(0,1); W N(0, 0.02)."""
     p = 8
     return {"x": normal_bf16((m, 12288), _sd(5, 0, 0 if m == 2048 else 1)),

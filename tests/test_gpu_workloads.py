@@ -50,9 +50,9 @@ def rows_of(t, rows):
 
 # ------------------------------------------------------------------ 1: row-parallel worked example
 
-def test_config1_row_parallel_p2_chunk32(tp):
+def test_worked_example_row_parallel_p2_chunk32(tp):
     import torch
-    inp = synth.config1_inputs()
+    inp = synth.worked_example_inputs()
     p, M, K, N, chunk = 2, 128, 1024, 2048, 32
     assert tp.tp_num_chunks(M, chunk) == 4
     xs, ws = [dev(a) for a in inp["x"]], [dev(b) for b in inp["w"]]
@@ -75,8 +75,8 @@ def test_config1_row_parallel_p2_chunk32(tp):
 
 # ------------------------------------------------------------------ 2: MLP block fwd + bwd
 
-def test_config2_mlp_block_fwd_bwd(tp):
-    inp = synth.config2_inputs()
+def test_mlp_block_fwd_bwd(tp):
+    inp = synth.mlp_block_inputs()
     p, M, h, nk = 4, 4096, 4096, 4096
     X, W1, W2, DY = dev(inp["x"]), [dev(a) for a in inp["w1"]], [dev(a) for a in inp["w2"]], dev(inp["dy"])
     Z = [bf((M, nk)) for _ in range(p)]
@@ -129,8 +129,8 @@ def test_config2_mlp_block_fwd_bwd(tp):
 
 # ------------------------------------------------------------------ 3: MHA projections
 
-def test_config3_mha_projections_fwd_bwd(tp):
-    inp = synth.config3_inputs()
+def test_mha_projections_fwd_bwd(tp):
+    inp = synth.mha_projection_inputs()
     p, M, h, nq, no = 4, 4096, 4096, 3072, 1024
     X, WQ = dev(inp["x"]), [dev(a) for a in inp["wqkv"]]
     O, WO = [dev(a) for a in inp["o"]], [dev(a) for a in inp["wo"]]
@@ -170,9 +170,9 @@ def test_config3_mha_projections_fwd_bwd(tp):
 
 # ------------------------------------------------------------------ 4: sequence-parallel pair
 
-def test_config4_sequence_parallel_pair(tp):
+def test_sequence_parallel_pair(tp):
     import torch
-    inp = synth.config4_inputs()
+    inp = synth.sequence_parallel_pair_inputs()
     p, Mp, h, nk = 8, 1024, 8192, 3584
     M = p * Mp
     XS, W1, W2 = [dev(a) for a in inp["x"]], [dev(a) for a in inp["w1"]], [dev(a) for a in inp["w2"]]
@@ -198,10 +198,10 @@ def test_config4_sequence_parallel_pair(tp):
     assert_close(y_gpu, yr, False, "MatMul+ReduceScatter")
 
 
-def test_config4_sequence_parallel_pair_backward(tp):
+def test_sequence_parallel_pair_backward(tp):
     """The dual of the SP pair: FC2's MatMul+ReduceScatter backward gathers dY
     (with GeLU'), FC1's AllGather+MatMul backward reduce-scatters dX."""
-    inp = synth.config4_inputs()
+    inp = synth.sequence_parallel_pair_inputs()
     p, Mp, h, nk = 8, 1024, 8192, 3584
     M = p * Mp
     dys = [synth.normal_bf16((Mp, h), synth.seed_for(43, s)) for s in range(p)]
@@ -248,8 +248,8 @@ def torch_cat(ts):
 # ------------------------------------------------------------------ 5: GPT-3-scale MLP, chunk sweep
 
 @pytest.mark.parametrize("M,chunks", [(2048, (0, 16, 64, 256, 1024, 2048)), (16, (0, 16))])
-def test_config5_gpt3_mlp_chunk_sweep(tp, M, chunks):
-    inp = synth.config5_inputs(M)
+def test_gpt3_mlp_chunk_sweep(tp, M, chunks):
+    inp = synth.gpt3_mlp_inputs(M)
     p, h, nk = 8, 12288, 6144
     X, W1, W2 = dev(inp["x"]), [dev(a) for a in inp["w1"]], [dev(a) for a in inp["w2"]]
     rows = sample_idx(M, extra=range(0, M, 16)) if M > 64 else np.arange(M)
