@@ -66,6 +66,10 @@ def parse():
     ap.add_argument("--configs", action="store_true",
                     help="one JSON line per workload (all five), TFLOP/s and roofline fraction")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="leave out the per-workload table of the headline line")
+    ap.add_argument("--workload-steps", type=int, default=20,
+                    help="timed steps per workload in the headline line's workload table")
     ap.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2],
                     help="0: planner chooses 128x256 or CTA-pair 256x256 tiles; 1: 128x256 only; 2: pairs")
     ap.add_argument("--profile-case", action="store_true",
@@ -358,6 +362,25 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU leg
 
+def _dist(v):
+    """median, min and p90 of a list of per-step times."""
+    s = sorted(v)
+    return s[len(s) // 2], s[0], s[int(0.9 * (len(s) - 1))]
+
+
+def choose_peak(pk, src, clocks):
+    """The bf16 roofline denominator for what the timed region saw: the
+    measured burst peak while no sample showed the power cap (the SM clock at
+    its maximum), the measured sustained peak once sw_power_cap was seen."""
+    burst = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    sust = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    if capped:
+        return sust, f"{src} bf16 dense, sustained: sw_power_cap was active during the timed region"
+    return burst, (f"{src} bf16 dense, burst: no sw_power_cap sample during the timed region "
+                   f"(SM clock median {clocks.get('sm_mhz')} of max {clocks.get('sm_max_mhz')} MHz)")
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_init(args.gpus)
@@ -377,24 +400,40 @@ def run_ours(args):
     if st != tp.TP_OK:
         raise RuntimeError(f"device status after warm-up: {tp.tp_status_string(st)}")
 
+    # Headline: K steps back to back, events at step boundaries only (no
+    # event between the launches of a step, which keeps the programmatic
+    # dependent launch overlap of consecutive kernels intact).
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        ev[0].record(stream)
         for k in range(K):
-            ev[k][0].record(stream)
-            for i, (_, fn) in enumerate(calls):
+            for _, fn in calls:
                 fn()
-                ev[k][i + 1].record(stream)
+            ev[k + 1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
     clocks = clk.summary()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][len(calls)])
+    total_ms = ev[0].elapsed_time(ev[K])
+    step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+    med, mn, p90 = _dist(step_ms)
+
+    # Per-call durations, in a separate pass of K steps with an event around
+    # every launch (used for the dominant kernel's roofline only).
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for k in range(K):
+        evc[k][0].record(stream)
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            evc[k][i + 1].record(stream)
+    torch.cuda.synchronize()
     per_call = {name: 0.0 for name, _ in calls}
     for k in range(K):
         for i, (name, _) in enumerate(calls):
-            per_call[name] += ev[k][i].elapsed_time(ev[k][i + 1])
+            per_call[name] += evc[k][i].elapsed_time(evc[k][i + 1])
     st = tp.tp_get_device_status(step.ws)
     if st != tp.TP_OK:
         raise RuntimeError(f"device status after timing: {tp.tp_status_string(st)}")
@@ -412,13 +451,21 @@ def run_ours(args):
     dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
     dom_avg_s = per_kernel[dom]["ms"] / per_kernel[dom]["launches"] / 1e3
     pk, src = peaks()
-    peak = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    peak, peak_why = choose_peak(pk, src, clocks)
+    burst = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    sust = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     achieved = GEMM_FLOPS / dom_avg_s / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"{src} bf16 dense, sustained (timed inside a long step)",
+                "frac": achieved / peak, "peak_source": peak_why,
+                "frac_of_burst": achieved / burst, "frac_of_sustained": achieved / sust,
                 "traffic": dram_traffic(dom),
                 "per_call_ms": {n: per_call[n] / K for n in per_call},
-                "value_frac_of_peak": value / world / peak}
+                "per_call_pass": f"a separate pass of {K} steps with an event around every launch",
+                "dominant_launches_per_step": per_kernel[dom]["launches"] // K,
+                "algorithmic_flops_per_launch": GEMM_FLOPS,
+                "value_frac_of_peak": value / world / peak,
+                "value_frac_of_burst": value / world / burst,
+                "value_frac_of_sustained": value / world / sust}
 
     # End to end through the ABI with host buffers, double-buffered: two
     # device buffer sets alternate, so step i+1's upload (copy stream) and
@@ -503,9 +550,143 @@ def run_ours(args):
                        "parallelism": f"{world} independent replica(s), all {P} ranks on each GPU"},
             "roofline": roofline, "clocks": clocks, "e2e": e2e, "e2e_streamed_weights": e2e_streamed,
             "gpu_launches": len(calls) * K}
+    line.update({"ms_per_step_median": med, "ms_per_step_min": mn, "ms_per_step_p90": p90,
+                 "timing": "CUDA events at step boundaries on the launching stream; value = work of all "
+                           "K steps / their total time; median, min and p90 over the K steps"})
+    if world == 1 and not args.no_workloads:
+        del step, calls
+        torch.cuda.empty_cache()
+        headline = {"ms_median": med, "ms_min": mn, "ms_p90": p90, "steps": K,
+                    "tflops": STEP_FLOPS / (med / 1e3) / 1e12, "peak": peak, "clocks": clocks}
+        line["workloads"] = workload_table(torch, tp, args, pk, src, headline)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"]["per_core"] = cpu_rate_one_core()
     print(json.dumps(line), flush=True)
+
+
+# Targets per workload: fraction of the dense bf16 peak for the tensor-bound
+# ones, of the measured HBM copy bandwidth for the decode-like one; the
+# worked example is a parity and latency case, reported as % of HBM.
+WORKLOAD_TABLE = [
+    ("worked_example_p2", "hbm", None),
+    ("mlp_block_p4", "tensor", 0.70),
+    ("mha_projections_p4", "tensor", 0.70),
+    ("sp_pair_fwd_p8", "tensor", 0.70),
+    ("gpt3_mlp_p8_m2048", "tensor", 0.70),
+    ("gpt3_mlp_p8_m16", "hbm", 0.60),
+]
+
+
+def _time_steps(torch, calls, steps, warmup, flush_buf=None):
+    """Per-step ms of the calls: back to back with events at step boundaries,
+    or, with flush_buf, each step timed alone after the L2 is overwritten."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    if flush_buf is None:
+        ev[0].record(stream)
+        for k in range(steps):
+            for _, fn in calls:
+                fn()
+            ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+        return [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    for k in range(steps):
+        flush_buf.fill_(float(k))
+        ev[2 * k].record(stream)
+        for _, fn in calls:
+            fn()
+        ev[2 * k + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(steps)]
+
+
+def workload_table(torch, tp, args, pk, src, headline):
+    """Every workload at full size, timed like the headline (median, min and
+    p90 over --workload-steps steps), each against its roofline: TFLOP/s as
+    a fraction of the bf16 peak chosen from the clocks seen during this pass,
+    or GB/s as a fraction of the measured HBM copy bandwidth (L2 flushed
+    before each step)."""
+    table = dict(workloads(torch, tp))
+    flush = torch.empty(256 << 20, dtype=torch.float32, device="cuda")   # 1 GiB > 2 x L2
+    hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    out, raw = {}, {}
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for name, bound, target in WORKLOAD_TABLE:
+            if name == "mlp_block_p4":
+                continue
+            w = table[name]()
+            ms = _time_steps(torch, w["calls"], args.workload_steps, 3, flush if w["flush"] else None)
+            st = tp.tp_get_device_status(w["ws"])
+            if st != tp.TP_OK:
+                raise RuntimeError(f"{name}: device status {tp.tp_status_string(st)}")
+            raw[name] = ({k: w.get(k) for k in ("desc", "flops", "bytes", "flush")}, ms)
+            del w
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+    clocks = clk.summary()
+    peak, why = choose_peak(pk, src, clocks)
+    for name, bound, target in WORKLOAD_TABLE:
+        if name == "mlp_block_p4":
+            h = headline
+            e = {"desc": WORKLOAD, "bound": "tensor", "ms_median": h["ms_median"], "ms_min": h["ms_min"],
+                 "ms_p90": h["ms_p90"], "steps": h["steps"], "tflops": h["tflops"],
+                 "peak_tflops": h["peak"], "frac_of_peak": h["tflops"] / h["peak"],
+                 "l2": "inputs larger than L2", "timed_in": "the headline run above"}
+            e["target"] = f">= {target} of the dense bf16 peak"
+            e["meets_target"] = e["frac_of_peak"] >= target
+            out[name] = e
+            continue
+        w, ms = raw[name]
+        med, mn, p90 = _dist(ms)
+        e = {"desc": w["desc"], "bound": bound, "ms_median": med, "ms_min": mn, "ms_p90": p90,
+             "steps": len(ms), "flops_per_step": w["flops"], "tflops": w["flops"] / (med / 1e3) / 1e12,
+             "l2": "flushed before each step" if w["flush"] else "inputs larger than L2"}
+        e["peak_tflops"] = peak
+        e["frac_of_peak"] = e["tflops"] / peak
+        if w.get("bytes"):
+            e["bytes_per_step"] = w["bytes"]
+            e["hbm_gbs"] = w["bytes"] / (med / 1e3) / 1e9
+            e["frac_of_hbm"] = e["hbm_gbs"] / hbm
+        if target is not None:
+            frac = e["frac_of_hbm"] if bound == "hbm" else e["frac_of_peak"]
+            e["target"] = f">= {target} of {'HBM bandwidth' if bound == 'hbm' else 'the dense bf16 peak'}"
+            e["meets_target"] = frac >= target
+        out[name] = e
+    del raw, flush
+    torch.cuda.empty_cache()
+    return {"entries": out, "peak_tflops": peak, "peak_source": why, "hbm_gbs_peak": hbm,
+            "clocks": clocks, "steps_each": args.workload_steps,
+            "how": "each workload set up once (seeded inputs), 3 warm-up steps, then --workload-steps "
+                   "steps timed with CUDA events at step boundaries; the MLP block is the headline run"}
+
+
+def cpu_rate_one_core(tokens=64):
+    """The oracle's rate on one host core: the same MLP step on a token
+    sample in a child process whose BLAS and OpenMP pools have one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    code = ("import time, bench\n"
+            f"x, w1, w2, dy = bench.cpu_inputs({tokens})\n"
+            "bench.oracle_step(x[:8], w1, w2, dy[:8])\n"
+            "t0 = time.perf_counter()\n"
+            "bench.oracle_step(x, w1, w2, dy)\n"
+            "print(time.perf_counter() - t0)\n")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=600)
+        dt = float(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, never fatal
+        return {"error": f"one-core run failed: {e}"}
+    flops = STEP_FLOPS * tokens / M
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "gflops_per_core": flops / dt / 1e9,
+            "sample": f"one MLP fwd+bwd step over {tokens} of the {M} tokens with the full weights, "
+                      f"fp64 numpy oracle with one BLAS/OpenMP thread ({dt:.1f} s, {flops / 1e9:.0f} GFLOP)"}
 
 
 def profile_case():
@@ -594,7 +775,7 @@ def workloads(torch, tp):
                     flops=2 * 2.0 * M * N * K * p, bytes=2 * (2 * (p * M * K + p * K * N) + 2 * M * N),
                     bound="hbm", flush=True,
                     row_reduce=dict(call="row_fwd_allreduce", x=d["x"], w=d["w"], y=y, chunk=32),
-                    desc="row-parallel p=2, X_r[128,1024], W_r[1024,2048], AllReduce + ReduceScatter, chunk_m=32")
+                    desc="row-parallel p=2, X_r[128,1024], W_r[1024,2048], AllReduce + ReduceScatter, chunk_m=32", ws=ws)
 
     def w2():
         d = _dev_all(torch, synth.mlp_block_inputs())
@@ -617,7 +798,7 @@ def workloads(torch, tp):
             ("col_bwd_dw", lambda: tp.tp_col_linear_bwd(d["x"], d["w1"], DZ, None, DW1, ws))],
             flops=6 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
             row_reduce=dict(call="row_fwd_allreduce", x=Z, w=d["w2"], y=Y, chunk=0),
-            desc="Megatron MLP block fwd+bwd p=4, 4096 tokens, h=4096, ffn=16384")
+            desc="Megatron MLP block fwd+bwd p=4, 4096 tokens, h=4096, ffn=16384", ws=ws)
 
     def w3():
         d = _dev_all(torch, synth.mha_projection_inputs())
@@ -637,7 +818,7 @@ def workloads(torch, tp):
             ("qkv_col_bwd", lambda: tp.tp_col_linear_bwd(d["x"], d["wqkv"], d["dqkv"], DX, DWQ, ws))],
             flops=3 * (2.0 * M * h * nq * p + 2.0 * M * no * h * p), bytes=None, bound="tensor", flush=False,
             row_reduce=dict(call="wo_row_fwd_allreduce", x=d["o"], w=d["wo"], y=Y, chunk=0),
-            desc="MHA projections fwd+bwd p=4, 4096 tokens, h=4096, QKV [4096,3072]/shard, W_O [1024,4096]/shard")
+            desc="MHA projections fwd+bwd p=4, 4096 tokens, h=4096, QKV [4096,3072]/shard, W_O [1024,4096]/shard", ws=ws)
 
     def w4():
         d = _dev_all(torch, synth.sequence_parallel_pair_inputs())
@@ -652,7 +833,7 @@ def workloads(torch, tp):
             ("row_fwd_reducescatter", lambda: tp.tp_row_linear_fwd_reducescatter(Z, d["w2"], YS, ws))],
             flops=2 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
             row_reduce=dict(call="row_fwd_reducescatter", x=Z, w=d["w2"], y=None, chunk=0, op=tp.TP_OP_ROW_RS),
-            desc="sequence-parallel pair fwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672")
+            desc="sequence-parallel pair fwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672", ws=ws)
 
     def w4b():
         d = _dev_all(torch, synth.sequence_parallel_pair_inputs())
@@ -675,11 +856,16 @@ def workloads(torch, tp):
                                                                              preact=Hh)),
             ("ag_matmul_bwd", lambda: tp.tp_ag_matmul_bwd(d["x"], d["w1"], DZ, DXS, DW1, ws))],
             flops=6 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,
-            desc="sequence-parallel pair fwd+bwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672")
+            desc="sequence-parallel pair fwd+bwd p=8, 8192 tokens (1024/rank), h=8192, ffn=28672", ws=ws)
+
+    gpt3_weights = {}
 
     def w5(M):
         def setup():
-            d = _dev_all(torch, synth.gpt3_mlp_inputs(M))
+            # the weights are shared by both token counts: drawn and uploaded once
+            if not gpt3_weights:
+                gpt3_weights.update(_dev_all(torch, synth.gpt3_mlp_weights()))
+            d = dict(gpt3_weights, **_dev_all(torch, {"x": synth.gpt3_mlp_activations(M)}))
             p, h, nk = 8, 12288, 6144
             Z = [torch.empty((M, nk), **bf) for _ in range(p)]
             Hh = [torch.empty((M, nk), **bf) for _ in range(p)]
@@ -693,7 +879,7 @@ def workloads(torch, tp):
                 bytes=wbytes + 4.0 * M * h + 6.0 * M * nk * p,
                 bound="hbm" if M <= 64 else "tensor", flush=M <= 64,
                 row_reduce=dict(call="row_fwd_allreduce", x=Z, w=d["w2"], y=Y, chunk=0),
-                desc=f"GPT-3-scale MLP fwd p=8, h=12288, ffn=49152, M={M}")
+                desc=f"GPT-3-scale MLP fwd p=8, h=12288, ffn=49152, M={M}", ws=ws)
         return setup
 
     return [("worked_example_p2", w1), ("mlp_block_p4", w2), ("mha_projections_p4", w3), ("sp_pair_fwd_p8", w4), ("sp_pair_fwd_bwd_p8", w4b),

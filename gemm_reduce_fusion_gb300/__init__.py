@@ -454,3 +454,12 @@ def tp_row_linear_fwd_allreduce_noalloc(x: Sequence, w: Sequence, y: Sequence, c
     _need_all(W, "y", y, (1, p), (M, N), False, dev)
     _check(fn(_arr(x), _arr(w), _arr(y), len(y), p, M, N, K, chunk_m, _dtype_code(y[0]), _stream(stream)),
            "tp_row_linear_fwd_allreduce_noalloc")
+
+
+def tp_noalloc_device_status(stream=None) -> int:
+    """Read and clear the status word of the allocation-free entry point's
+    static scratch (synchronises the stream): TP_OK or TP_ERR_DEVICE_TIMEOUT."""
+    fn = _lib.tp_noalloc_device_status
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p]
+    return fn(_stream(stream))

@@ -1560,19 +1560,51 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device with that device current.
+// The current context's driver-assigned ID (unique over the process's
+// lifetime, unlike the context handle, which may be reused), or 0.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(a);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(b);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current device's primary
+// context.  Looked up with that device current on the first call, and again
+// whenever the context has changed since (after a cudaDeviceReset the module
+// is loaded anew and the array may sit elsewhere).
 tp_status noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = 0;
   if (bind_device(&dev) != TP_OK) return TP_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return TP_ERR_CUDA;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return TP_ERR_CUDA;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return TP_OK;
@@ -1594,4 +1626,10 @@ extern "C" tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, c
   TP_TRY(noalloc_scratch(&scratch));
   return row_fwd_impl(false, x, w, nullptr, y, n_out, p, M, N, K, chunk_m, out_dtype, scratch,
                       TP_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" tp_status tp_noalloc_device_status(cudaStream_t stream) {
+  void* scratch = nullptr;
+  TP_TRY(noalloc_scratch(&scratch));
+  return tp_get_device_status(scratch, stream);
 }

@@ -305,13 +305,26 @@ tp_status tp_get_device_status(void* ws, cudaStream_t stream);
  *    every partial a call reads was written earlier by that same call, and
  *    slice counters carry the number of the launch that wrote them, so
  *    stale ones read as zero.
- *  - Device-side timeouts are latched in the array but not reported; use
- *    tp_row_linear_fwd_allreduce with a workspace to read them.            */
+ *  - A device-side wait that runs out of time latches
+ *    TP_ERR_DEVICE_TIMEOUT into the array's status word, as it would into a
+ *    workspace; tp_noalloc_device_status() reads and clears it.
+ *  - The array's address is looked up again when the device's context has
+ *    changed (for instance after cudaDeviceReset), so a reset does not
+ *    leave a stale address behind; the first call after it then repeats
+ *    the look-up and must also come before any stream capture.           */
 #define TP_NOALLOC_SCRATCH_BYTES (16u << 20)
 tp_status tp_row_linear_fwd_allreduce_noalloc(const void* const* x, const void* const* w,
                                               void* const* y, int n_out, int p,
                                               int64_t M, int64_t N, int64_t K, int64_t chunk_m,
                                               tp_dtype out_dtype, cudaStream_t stream);
+
+/* Status word of the allocation-free entry point's static scratch on the
+ * calling thread's current device (no counterpart in the paper either).
+ * Synchronises `stream`, then returns TP_ERR_DEVICE_TIMEOUT (and clears the
+ * word) if a device wait of an earlier tp_row_linear_fwd_allreduce_noalloc
+ * call ran out of time, TP_OK if none did, TP_ERR_CUDA if the CUDA calls
+ * fail.  Like the entry point itself it allocates nothing.                */
+tp_status tp_noalloc_device_status(cudaStream_t stream);
 
 /* Test hooks of the failure-detection path (process-wide, read when a call
  * is planned).  Not for production use.

@@ -182,9 +182,18 @@ def sequence_parallel_pair_inputs():
             "w2": [normal_bf16((3584, 8192), _sd(4, 2, k), 0.02) for k in range(p)]}
 
 
+def gpt3_mlp_activations(m: int):
+    """GPT-3-scale MLP input X [m, 12288] N(0,1)."""
+    return normal_bf16((m, 12288), _sd(5, 0, 0 if m == 2048 else 1))
+
+
+def gpt3_mlp_weights():
+    """GPT-3-scale MLP weights, p = 8: W1_k [12288, 6144], W2_k [6144, 12288] N(0, 0.02)."""
+    p = 8
+    return {"w1": [normal_bf16((12288, 6144), _sd(5, 1, k), 0.02) for k in range(p)],
+            "w2": [normal_bf16((6144, 12288), _sd(5, 2, k), 0.02) for k in range(p)]}
+
+
 def gpt3_mlp_inputs(m: int):
     """GPT-3-scale MLP, p = 8, h = 12288, ffn = 49152: X [m, 12288] N(0,1); W N(0, 0.02)."""
-    p = 8
-    return {"x": normal_bf16((m, 12288), _sd(5, 0, 0 if m == 2048 else 1)),
-            "w1": [normal_bf16((12288, 6144), _sd(5, 1, k), 0.02) for k in range(p)],
-            "w2": [normal_bf16((6144, 12288), _sd(5, 2, k), 0.02) for k in range(p)]}
+    return dict(gpt3_mlp_weights(), x=gpt3_mlp_activations(m))

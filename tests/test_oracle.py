@@ -323,6 +323,23 @@ def test_round_bf16_values():
     assert synth.f32_to_bf16_bits(vals.astype(np.float32)).tolist() == [0x3F80, 0x3EAB, 0x3F80, 0x3F82, 0xC000, 0]
 
 
+def test_round_bf16_rounds_through_fp32():
+    """The oracle rounds a float64 value to bf16 the way the library rounds
+    its accumulator: first to fp32 (the accumulator's type), then to bf16,
+    nearest even.  1 + 2^-8 + 2^-30 lies just above the bf16 midpoint
+    between 1 and 1 + 2^-7, so rounding float64 -> bf16 directly would give
+    1 + 2^-7 (0x3F81); through fp32 the 2^-30 is lost (below half an fp32
+    ulp), the value becomes the exact midpoint and ties to even: 1.0."""
+    x = np.array([1 + 2 ** -8 + 2 ** -30, -(1 + 2 ** -8 + 2 ** -30), 3 * 2 ** -9 + 2 ** -40])
+    assert oracle.round_bf16(x).tolist() == [0x3F80, 0xBF80, 0x3BC0]
+    # a value that only the direct route rounds up, checked against exact
+    # rational arithmetic: the direct nearest-bf16 is the upper neighbour
+    from fractions import Fraction
+    v = Fraction(1) + Fraction(1, 2 ** 8) + Fraction(1, 2 ** 30)
+    lo, hi = Fraction(1), Fraction(1) + Fraction(1, 2 ** 7)
+    assert v - lo > hi - v
+
+
 def test_splitmix64_published_vectors():
     # Vigna's reference splitmix64 outputs for seeds 0 and 1234567
     assert [int(v) for v in synth.splitmix64(0, 0, 3)] == [
