@@ -208,14 +208,35 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-__device__ __forceinline__ float gelu_f(float h) {
-  return 0.5f * h * (1.0f + erff(h * 0.70710678118654752f));
+// Normal tail Phi(-|h|) and the Gaussian factor e = exp(-h^2 / 2), from
+// Abramowitz & Stegun, Handbook of Mathematical Functions (1964), formula
+// 7.1.26: for z >= 0, erfc(z) = (a1 t + a2 t^2 + ... + a5 t^5) exp(-z^2) with
+// t = 1 / (1 + p z) and an absolute error of at most 1.5e-7.  With
+// z = |h| / sqrt(2) the tail is erfc(z) / 2, and exp(-z^2) is e, which the
+// GeLU derivative's density term reuses.
+__device__ __forceinline__ float normal_tail(float h, float& e) {
+  constexpr float p = 0.3275911f * 0.70710678118654752f;  // p / sqrt(2): t from |h| directly
+  constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
+                  a5 = 1.061405429f;
+  const float t = rcp_approx(fmaf(p, fabsf(h), 1.0f));
+  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
+  e = ex2_approx(h * h * -0.72134752044448170f);  // exp(-h^2/2) = 2^(-h^2 log2(e) / 2)
+  return 0.5f * poly * e;
 }
 
+// GeLU(h) = h Phi(h) ([TP] §7.1, exact erf form; Phi from the tail above,
+// within 3e-7 of the exact value in fp32).
+__device__ __forceinline__ float gelu_f(float h) {
+  float e;
+  const float c = normal_tail(h, e);
+  return h * (h >= 0.0f ? 1.0f - c : c);
+}
+
+// GeLU'(h) = Phi(h) + h phi(h), phi(h) = e / sqrt(2 pi).
 __device__ __forceinline__ float gelu_prime_f(float h) {
-  const float cdf = 0.5f * (1.0f + erff(h * 0.70710678118654752f));
-  const float pdf = 0.39894228040143268f * expf(-0.5f * h * h);
-  return cdf + h * pdf;
+  float e;
+  const float c = normal_tail(h, e);
+  return fmaf(h * e, 0.39894228040143268f, h >= 0.0f ? 1.0f - c : c);
 }
 
 __device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {

@@ -185,6 +185,51 @@ def test_col_fwd_gelu(tp, split_k, p, M, N, K, chunk, f32):
             assert_close(host_f64(y[k].t), oracle.gelu(host_f64(h[k].t)), True, "gelu(H)")
 
 
+def _bf16_grid(lo_exp=-20, hi=16.0):
+    """Every bf16 value v with 2^lo_exp <= |v| <= hi, both signs, and 0."""
+    b = np.arange(0, 0x8000, dtype=np.uint32)
+    v = (b << 16).view(np.float32)
+    keep = (v >= 2.0 ** lo_exp) & (v <= hi)
+    pos = b[keep].astype(np.uint16)
+    return np.concatenate([[0], pos, pos | 0x8000]).astype(np.uint16)
+
+
+@pytest.mark.parametrize("chunk", [0, 32])
+def test_gelu_epilogues_within_their_error_bound(tp, chunk):
+    """The GeLU and GeLU' epilogues on every bf16 pre-activation in
+    [-16, 16] (magnitudes down to 2^-20), fp32 outputs, against the exact
+    functions.  The epilogue's normal CDF follows Abramowitz & Stegun 7.1.26
+    (|error| <= 1.5e-7 on erf), so in fp32 |GeLU error| <= 4e-7 |h| and
+    |GeLU' error| <= 4e-7.  H reaches the epilogue exactly: the column
+    forward multiplies an identity by H, the row backward's product is all
+    ones (dY's first column and A's first column are ones)."""
+    import torch
+    vals = _bf16_grid()
+    M, N = 256, 256     # every value about ten times, on 128-row tiles (chunk 0) or 32-token tiles (chunk 32)
+    hv = np.resize(vals, M * N).reshape(M, N)
+    h = oracle.widen(hv)
+    # column forward with GeLU: X = I [M, M], W = H
+    eye = synth.f32_to_bf16_bits(np.eye(M, dtype=np.float32))
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    pre = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tp.tp_col_linear_fwd(dev(eye), [dev(hv)], [y], ws_for(tp, tp.TP_OP_COL_FWD, 1, M, N, M, chunk),
+                         epi=tp.TP_EPI_GELU, preact=[pre], chunk_m=chunk)
+    assert np.array_equal(host_f64(pre), h)
+    err = np.abs(host_f64(y) - oracle.gelu(h))
+    assert np.all(err <= 4e-7 * np.abs(h)), f"GeLU: worst |d|/|h| = {np.max(err / np.maximum(np.abs(h), 1e-30)):.3e}"
+    # row backward with GeLU': dX = (dY A^T) * GeLU'(H) with dY A^T = 1
+    K, Nb = N, 16
+    dy = np.zeros((M, Nb), dtype=np.float32)
+    dy[:, 0] = 1.0
+    a = np.zeros((K, Nb), dtype=np.float32)
+    a[:, 0] = 1.0
+    dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    tp.tp_row_linear_bwd(None, [dev(synth.f32_to_bf16_bits(a))], dev(synth.f32_to_bf16_bits(dy)), [dx], None,
+                         ws_for(tp, tp.TP_OP_ROW_BWD, 1, M, Nb, K, chunk), preact=[dev(hv)], chunk_m=chunk)
+    err = np.abs(host_f64(dx) - oracle.gelu_prime(h))
+    assert np.all(err <= 4e-7), f"GeLU': max |d| = {err.max():.3e}"
+
+
 COLB_CASES = [(1, 128, 256, 64, 0), (3, 300, 136, 264, 0), (4, 257, 72, 520, 128), (2, 100, 200, 136, 16),
               (3, 77, 72, 72, 64), (2, 64, 64, 256, 32)]
 
