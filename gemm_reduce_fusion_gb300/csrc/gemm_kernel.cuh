@@ -105,6 +105,18 @@ struct GemmParams {
   // this launch's number (never 0): slice counters left by an earlier launch,
   // finished or stopped, read as zero
   unsigned long long epoch;
+  // L2 policies (see l2_policy): of the A and B operand loads (3-D maps) and
+  // of the final output stores
+  int32_t a_hint, b_hint, out_hint;
+  // Staged epilogue by TMA store (out_tma = 1): group g (replica r) writes
+  // its 32-row x 128-byte chunks through tmO[omap[g] + r] at row orow[g] + i,
+  // and its GeLU pre-activation through tmH[hmap[g]] at row hrow[g] + i.
+  // Boxes are 32 rows x 128 bytes with the staging buffer's 128-byte swizzle.
+  int32_t out_tma;
+  CUtensorMap tmO[MAX_MAPS];
+  CUtensorMap tmH[MAX_MAPS];
+  int32_t omap[MAX_GROUPS], orow[MAX_GROUPS];
+  int32_t hmap[MAX_GROUPS], hrow[MAX_GROUPS];
 };
 
 struct Unit {
@@ -287,15 +299,14 @@ __device__ __forceinline__ uint32_t stg_off(int r, int u) {
 // rows [0, rows_valid) x units [0, units_valid) of the staged chunk -> global
 template <int U>
 __device__ __forceinline__ void stage_store(const uint8_t* stg, uint8_t* dst, int64_t ld_bytes,
-                                            int rows_valid, int units_valid, int lane) {
+                                            int rows_valid, int units_valid, int lane, uint64_t policy) {
   constexpr int RPI = 32 / U;  // rows per instruction
 #pragma unroll
   for (int k = 0; k < U; ++k) {
     const int r = k * RPI + lane / U;
     const int u = lane % U;
     if (r < rows_valid && u < units_valid)
-      *reinterpret_cast<uint4*>(dst + r * ld_bytes + u * 16) =
-          *reinterpret_cast<const uint4*>(stg + stg_off(r, u));
+      st_global_v4_hint(dst + r * ld_bytes + u * 16, *reinterpret_cast<const uint4*>(stg + stg_off(r, u)), policy);
   }
 }
 
@@ -358,6 +369,27 @@ __device__ __forceinline__ void load_chunk_tmem(uint32_t taddr, float (&v)[NV]) 
 // One chunk of NV columns (128 bytes of output per row) of the warp's 32
 // rows, starting at group column gj0, values v (this lane's row): bias ->
 // (H out) -> GeLU / GeLU' -> staged stores.
+// The staging buffer may be rewritten: the bulk stores of it this warp
+// issued (lane 0) have read it.
+__device__ __forceinline__ void stage_free(const GemmParams& P, int lane) {
+  if (P.out_tma) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+  }
+}
+
+// The staged chunk (rows gi0.., columns gj0.. of the group) -> global through
+// one bulk tensor store issued by lane 0.
+__device__ __forceinline__ void stage_store_tma(const CUtensorMap* m, const uint8_t* stg, int32_t x, int32_t y,
+                                                bool valid, int lane) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && valid) {
+    tma_store_2d(m, smem_u32(stg), x, y);
+    bulk_commit();
+  }
+}
+
 template <bool F32>
 __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t g, int32_t gi0, int32_t gj0,
                                                     float (&v)[F32 ? 32 : 64], uint8_t* stg, int lane) {
@@ -366,6 +398,7 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
   const int rows_valid = min(32, P.rows_g - gi0);
   const int cols_valid = min(NV, P.cols_g - gj0);     // a multiple of 8 (or <= 0)
   const int units_valid = cols_valid * ESZ / 16;
+  const bool any = rows_valid > 0 && cols_valid > 0;
   if (P.bias[g] != nullptr) {
     const uint16_t* b = static_cast<const uint16_t*>(P.bias[g]) + gj0;
 #pragma unroll
@@ -383,11 +416,16 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
   }
   if (P.epi == EPI_GELU) {
     if (P.aux[g] != nullptr) {
+      stage_free(P, lane);
       stage_row<F32>(stg, lane, v);
-      __syncwarp();
-      uint8_t* dst = static_cast<uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * ESZ;
-      stage_store<8>(stg, dst, P.ld_aux * ESZ, rows_valid, units_valid, lane);
-      __syncwarp();
+      if (P.out_tma) {
+        stage_store_tma(&P.tmH[P.hmap[g]], stg, gj0, P.hrow[g] + gi0, any, lane);
+      } else {
+        __syncwarp();
+        uint8_t* dst = static_cast<uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * ESZ;
+        stage_store<8>(stg, dst, P.ld_aux * ESZ, rows_valid, units_valid, lane, l2_policy(P.out_hint));
+        __syncwarp();
+      }
     }
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = gelu_f(v[i]);
@@ -395,6 +433,7 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
     // H is bf16: NV * 2 bytes per row
     constexpr int UH = NV * 2 / 16;
     const uint8_t* src = static_cast<const uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * 2;
+    stage_free(P, lane);
     stage_load<UH>(stg, src, P.ld_aux * 2, rows_valid, cols_valid * 2 / 16, lane);
     __syncwarp();
 #pragma unroll
@@ -409,11 +448,21 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
     }
     __syncwarp();
   }
+  stage_free(P, lane);
   stage_row<F32>(stg, lane, v);
+  if (P.out_tma) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && any) {
+      for (int rep = 0; rep < P.n_rep; ++rep) tma_store_2d(&P.tmO[P.omap[g] + rep], smem_u32(stg), gj0, P.orow[g] + gi0);
+      bulk_commit();
+    }
+    return;
+  }
   __syncwarp();
   for (int rep = 0; rep < P.n_rep; ++rep) {
     uint8_t* dst = static_cast<uint8_t*>(P.out[g + rep]) + (static_cast<int64_t>(gi0) * P.ld_out + gj0) * ESZ;
-    stage_store<8>(stg, dst, P.ld_out * ESZ, rows_valid, units_valid, lane);
+    stage_store<8>(stg, dst, P.ld_out * ESZ, rows_valid, units_valid, lane, l2_policy(P.out_hint));
   }
   __syncwarp();
 }
@@ -626,7 +675,8 @@ struct GemmCfg {
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
   static_assert(NUM_BARS * 8 + 16 <= 256, "barriers and the TMEM slot fit in 256 bytes");
   // epilogue staging (non-transposed outputs): 4 KiB per epilogue warp
-  static constexpr uint32_t STG_OFF = STAGES * STAGE_BYTES + 256;
+  // 1024-byte aligned: the staging buffers are 128-byte-swizzled TMA store sources
+  static constexpr uint32_t STG_OFF = (STAGES * STAGE_BYTES + 256 + 1023) / 1024 * 1024;
   static constexpr uint32_t STG_BYTES = OUT_T ? 0u : NUM_EPI_WARPS * STAGE_BYTES_PER_WARP;
   // +1024 so the ring can be aligned to 1024 bytes inside dynamic smem
   static constexpr uint32_t SMEM_BYTES = 1024 + STG_OFF + STG_BYTES;
@@ -692,6 +742,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t armed = 0, armed_parity = 0;
       int32_t n_issued = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy(P.a_hint);
+      const uint64_t pol_b = l2_policy(P.b_hint);
       for (int32_t t = blockIdx.x; t < P.num_units && ok; t += gridDim.x) {
         const Unit u = decode_unit(P, t);
         const int32_t arow = P.a_row_gm * u.gm + u.mt * BM;
@@ -720,10 +772,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
           const uint32_t sb = sB0 + stage * Cfg::B_BYTES;
           if (P.map3d) {
-            if (A_MN) tma_load_3d(sa, am, fb, 0, kca, arow / 64);
-            else tma_load_3d(sa, am, fb, 0, arow, kca / 64);
-            if (B_MN) tma_load_3d(sb, bm, fb, 0, kcb, bcol / 64);
-            else tma_load_3d(sb, bm, fb, 0, bcol, kcb / 64);
+            if (A_MN) tma_load_3d(sa, am, fb, 0, kca, arow / 64, pol_a);
+            else tma_load_3d(sa, am, fb, 0, arow, kca / 64, pol_a);
+            if (B_MN) tma_load_3d(sb, bm, fb, 0, kcb, bcol / 64, pol_b);
+            else tma_load_3d(sb, bm, fb, 0, bcol, kcb / 64, pol_b);
           } else {
             if (A_MN) {
 #pragma unroll
@@ -831,6 +883,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    // this warp's bulk stores complete before the CTA exits
+    if (P.out_tma && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -873,7 +927,7 @@ struct PairCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
   static_assert(NUM_BARS * 8 + 16 <= 256, "barriers and the TMEM slot fit in 256 bytes");
-  static constexpr uint32_t STG_OFF = STAGES * STAGE_BYTES + 256;
+  static constexpr uint32_t STG_OFF = (STAGES * STAGE_BYTES + 256 + 1023) / 1024 * 1024;
   static constexpr uint32_t SMEM_BYTES = 1024 + STG_OFF + NUM_EPI_WARPS * STAGE_BYTES_PER_WARP;
   static_assert(SMEM_BYTES <= 232448, "227 KiB of dynamic shared memory per CTA");
 };
@@ -945,6 +999,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t armed = 0, armed_parity = 0;
       int32_t n_issued = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy(P.a_hint);
+      const uint64_t pol_b = l2_policy(P.b_hint);
       for (int32_t t = first; t < P.num_units && ok; t += stride) {
         int32_t tj = -1, tk = 0;
         const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
@@ -976,10 +1032,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // sub-tiles (one per 64-wide K chunk), MN-major operands as
           // consecutive [BKP K-rows][64] sub-tiles (one per 64-wide MN block).
           if (P.map3d) {
-            if (A_MN) tma_load_3d_pair(sa, am, fb, 0, kca, arow / 64);
-            else tma_load_3d_pair(sa, am, fb, 0, arow, kca / 64);
-            if (B_MN) tma_load_3d_pair(sb, bm, fb, 0, kcb, bcol / 64);
-            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kcb / 64);
+            if (A_MN) tma_load_3d_pair(sa, am, fb, 0, kca, arow / 64, pol_a);
+            else tma_load_3d_pair(sa, am, fb, 0, arow, kca / 64, pol_a);
+            if (B_MN) tma_load_3d_pair(sb, bm, fb, 0, kcb, bcol / 64, pol_b);
+            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kcb / 64, pol_b);
           } else {
             if (A_MN) {
 #pragma unroll
@@ -1099,6 +1155,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    // this warp's bulk stores complete before the CTA exits
+    if (P.out_tma && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();

@@ -34,6 +34,9 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // accumulator's own rounding grows with the number of k-steps it takes, and
 // over K = 16384 it alone passes 1e-5 of max|Y|.
 constexpr int64_t kPreciseKb = 32;
+// An operand that every group of a launch reads through the same maps is
+// loaded evict_last when it takes at most this much of the 129 MB L2.
+constexpr int64_t kKeepBytes = 64ll << 20;
 
 // ------------------------------------------------------------------ small helpers
 
@@ -51,6 +54,8 @@ std::atomic<int64_t> g_debug_split_k{0};    // n > 0: split-K factor of launches
 std::atomic<unsigned long long*> g_trace{nullptr};  // timeline trace buffer of the next launches
 std::atomic<int64_t> g_trace_cap{0};
 std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (slice counters)
+std::atomic<int64_t> g_l2_hints{1};         // 1: L2 cache policies on operand loads and output stores
+std::atomic<int64_t> g_tma_store{1};        // 1: staged epilogues leave shared memory by TMA store
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -141,6 +146,21 @@ bool encode_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, 
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output map of the TMA-store epilogue: `cols` x `rows` of a row-major
+// matrix with a pitch of `ld` elements; boxes of 32 rows x 128 bytes with
+// the 128-byte swizzle the staging buffer is written in.
+bool encode_out_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld, bool f32) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (f32 ? 4u : 2u)};
+  cuuint32_t box[2] = {f32 ? 32u : 64u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D maps are used for a launch when every operand's contiguous extent is
@@ -564,6 +584,42 @@ void fill_common(GemmParams* P, const Shape& s) {
 
 size_t esize(tp_dtype d) { return d == TP_FP32 ? 4 : 2; }
 
+// Output maps of the TMA-store epilogue for the group outputs `ptrs` (pitch
+// `ld`): one map per group output (and replica) when there are at most
+// MAX_MAPS of them, each clipped to the group's rows and columns; otherwise,
+// when the groups are row blocks gm of p column buffers gn (the AllGather
+// layouts: ptrs[gm * Gn + gn] = ptrs[gn] + gm * rows_g rows) and rows_g is a
+// multiple of the 32-row box, one map per buffer with row offsets.  False
+// when neither applies (the epilogue then stores with plain instructions).
+bool plan_out_maps(const Shape& s, void* const* ptrs, int n_rep, int64_t ld, bool f32, CUtensorMap* maps,
+                   int32_t* mapidx, int32_t* row0) {
+  const int G = s.Gm * s.Gn;
+  if (G * n_rep <= MAX_MAPS) {
+    for (int g = 0; g < G; ++g) {
+      mapidx[g] = g * n_rep;
+      row0[g] = 0;
+      for (int r = 0; r < n_rep; ++r)
+        if (!encode_out_map(&maps[g * n_rep + r], ptrs[g + r], s.cols_g, s.rows_g, ld, f32)) return false;
+    }
+    return true;
+  }
+  if (n_rep != 1 || s.Gn > MAX_MAPS || s.rows_g % 32 != 0) return false;
+  const size_t es = f32 ? 4 : 2;
+  for (int gm = 0; gm < s.Gm; ++gm)
+    for (int gn = 0; gn < s.Gn; ++gn)
+      if (static_cast<const uint8_t*>(ptrs[gm * s.Gn + gn]) !=
+          static_cast<const uint8_t*>(ptrs[gn]) + static_cast<size_t>(gm) * s.rows_g * ld * es)
+        return false;
+  for (int gn = 0; gn < s.Gn; ++gn)
+    if (!encode_out_map(&maps[gn], ptrs[gn], s.cols_g, s.Gm * s.rows_g, ld, f32)) return false;
+  for (int gm = 0; gm < s.Gm; ++gm)
+    for (int gn = 0; gn < s.Gn; ++gn) {
+      mapidx[gm * s.Gn + gn] = gn;
+      row0[gm * s.Gn + gn] = static_cast<int32_t>(gm * s.rows_g);
+    }
+  return true;
+}
+
 tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
                             const DevInfo& di, int phases);
 
@@ -665,6 +721,29 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     uint8_t* base = static_cast<uint8_t*>(ws) + kStatusBytes;
     P.tail_cnt = reinterpret_cast<unsigned long long*>(base);
     P.tail_part = reinterpret_cast<float*>(base + s.tail_cnt_bytes());
+  }
+  // L2 policies: an operand shared by every group (one set of maps for all
+  // of them, re-read by every group's tiles) is kept while the other
+  // streams past it, if it fits in half the L2; final outputs, which nothing
+  // in the launch reads back, are written evict_first.
+  P.a_hint = P.b_hint = P.out_hint = 0;
+  if (g_l2_hints.load() != 0) {
+    const int64_t a_maps = (P.a_idx_gm ? s.Gm : 1) * (P.a_idx_gn ? s.Gn : 1) * (P.a_idx_s ? s.S : 1);
+    const int64_t b_maps = (P.b_idx_gm ? s.Gm : 1) * (P.b_idx_gn ? s.Gn : 1) * (P.b_idx_s ? s.S : 1);
+    const bool a_shared = (P.a_idx_gm == 0 && s.Gm > 1) || (P.a_idx_gn == 0 && s.Gn > 1);
+    const bool b_shared = (P.b_idx_gm == 0 && s.Gm > 1) || (P.b_idx_gn == 0 && s.Gn > 1);
+    P.a_hint = a_shared && a_maps * s.rows_g * s.kseg * 2 <= kKeepBytes ? 1 : 0;
+    P.b_hint = b_shared && b_maps * s.cols_g * s.kseg * 2 <= kKeepBytes ? 1 : 0;
+    P.out_hint = 2;
+  }
+  // staged epilogues (non-swapped tiles, no split-K partials) store through TMA
+  P.out_tma = 0;
+  if (g_tma_store.load() != 0 && !s.swap && s.n_split == 1) {
+    const bool f32 = out_dtype == TP_FP32;
+    bool ok = plan_out_maps(s, P.out, P.n_rep, P.ld_out, f32, P.tmO, P.omap, P.orow);
+    if (ok && P.epi == EPI_GELU && P.aux[0] != nullptr)
+      ok = plan_out_maps(s, P.aux, 1, P.ld_aux, f32, P.tmH, P.hmap, P.hrow);
+    P.out_tma = ok ? 1 : 0;
   }
   const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
                          : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
@@ -785,6 +864,14 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_SPLIT_K:
       if (value < 0 || value > 16) return TP_ERR_INVALID_ARG;
       g_debug_split_k.store(value);
+      return TP_OK;
+    case TP_DEBUG_L2_HINTS:
+      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
+      g_l2_hints.store(value);
+      return TP_OK;
+    case TP_DEBUG_TMA_STORE:
+      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
+      g_tma_store.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;

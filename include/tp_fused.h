@@ -354,7 +354,9 @@ typedef enum {
   TP_DEBUG_DROP_LOAD = 1,
   TP_DEBUG_TILE_MODE = 2,
   TP_DEBUG_NO_TAIL_SLICES = 3,
-  TP_DEBUG_SPLIT_K = 4
+  TP_DEBUG_SPLIT_K = 4,
+  TP_DEBUG_L2_HINTS = 5,
+  TP_DEBUG_TMA_STORE = 6
 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 

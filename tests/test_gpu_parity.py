@@ -1024,3 +1024,46 @@ def test_row_bwd_reducescatter_dgelu(tp, split_k, p, M, N, K, chunk):
     for g, r in zip(dx, oracle.row_rs_bwd_dx(ws, dys, preacts=hs)):
         g.check_bands()
         assert_close(host_f64(g.t), r, False, "SP bwd dgelu")
+
+
+@pytest.mark.parametrize("tile_mode", [1, 2], indirect=True)
+@pytest.mark.parametrize("p,M,N,K", [(2, 300, 520, 200), (4, 512, 264, 136), (3, 257, 136, 72)])
+def test_store_paths_bitwise_identical(tp, tile_mode, p, M, N, K):
+    """The staged epilogue leaves shared memory either by TMA store (the
+    default wherever the groups' outputs allow it) or by plain 16-byte
+    stores; both must write the same bits, including GeLU's H, ragged edges,
+    replicas and the AllGather layout's row blocks."""
+    import torch
+    x = synth.normal_bf16((M, K), 560, 1.0 / np.sqrt(K))
+    xs = [synth.normal_bf16((M, K), 561 + r, 1.0 / np.sqrt(K)) for r in range(p)]
+    ws = [synth.normal_bf16((K, N), 570 + r) for r in range(p)]
+    Mg = M // p * p
+    X, XS, W = dev(x), [dev(a) for a in xs], [dev(b) for b in ws]
+    XG = [dev(a[:Mg // p]) for a in xs]
+
+    def run():
+        bf = dict(dtype=torch.bfloat16, device="cuda")
+        y = [torch.empty((M, N), **bf) for _ in range(p)]
+        z = [torch.empty((M, N), **bf) for _ in range(p)]
+        h = [torch.empty((M, N), **bf) for _ in range(p)]
+        g = [torch.empty((Mg, N), **bf) for _ in range(p)]
+        gh = [torch.empty((Mg, N), **bf) for _ in range(p)]
+        f = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        wsp = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0)
+        tp.tp_row_linear_fwd_allreduce(XS, W, y, wsp)                      # p replicas
+        tp.tp_row_linear_fwd_allreduce(XS, W, [f], ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0))
+        tp.tp_col_linear_fwd(X, W, z, ws_for(tp, tp.TP_OP_COL_FWD, p, M, N, K, 0), epi=tp.TP_EPI_GELU, preact=h)
+        tp.tp_ag_matmul(XG, W, g, ws_for(tp, tp.TP_OP_AG_MM, p, Mg, N, K, 0), epi=tp.TP_EPI_GELU, preact=gh)
+        torch.cuda.synchronize()
+        return [t.clone() for t in y + z + h + g + gh + [f]]
+
+    a = run()
+    assert tp.tp_debug_set(tp.TP_DEBUG_TMA_STORE, 0) == tp.TP_OK
+    try:
+        b = run()
+    finally:
+        tp.tp_debug_set(tp.TP_DEBUG_TMA_STORE, 1)
+    for i, (u, v) in enumerate(zip(a, b)):
+        iv = torch.int32 if u.dtype == torch.float32 else torch.int16
+        assert torch.equal(u.view(iv), v.view(iv)), f"output {i} differs between the store paths"
+    assert_close(host_f64(a[-1]), oracle.row_fwd_allreduce(xs, ws), True, "fp32 AllReduce")
