@@ -348,6 +348,13 @@ tp_status tp_noalloc_device_status(cudaStream_t stream);
  *     split; fp32 outputs still split further where they need it).  Changes
  *     the workspace size of those calls; for parity testing of the split-K
  *     path on shapes the planner would not split.
+ *   TP_DEBUG_L2_HINTS: 1 (default) loads an operand that every output group
+ *     of a launch re-reads (and that fits in half the L2) with an
+ *     evict_last policy and writes final outputs evict_first; 0 leaves
+ *     every access at the normal policy.  Results are identical either way.
+ *   TP_DEBUG_TMA_STORE: 1 (default) lets the staged epilogue leave shared
+ *     memory by TMA tensor stores wherever the outputs allow it; 0 forces
+ *     plain 16-byte stores (bit-identical results; for testing both paths).
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
 typedef enum {
   TP_DEBUG_TIMEOUT_MS = 0,
