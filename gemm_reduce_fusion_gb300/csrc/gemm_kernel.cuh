@@ -675,18 +675,29 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
 template <int NV>
 __device__ __forceinline__ void sum_partial_row(const float* base, int64_t sstride, int n, int32_t gi, int32_t gj0,
                                                 const GemmParams& P, float (&v)[NV]) {
+  // every load of one split is issued before any of them is used: n round
+  // trips to L2 per chunk, not n per float4
+  const float* e = base + static_cast<int64_t>(gi) * P.cols_g + gj0;
+  const bool row = gi < P.rows_g;
+  float4 a[NV / 4];
+#pragma unroll
+  for (int m = 0; m < NV / 4; ++m)
+    a[m] = row && gj0 + 4 * m < P.cols_g ? __ldcg(reinterpret_cast<const float4*>(e + 4 * m))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 1; k < n; ++k) {
+    float4 b[NV / 4];
+#pragma unroll
+    for (int m = 0; m < NV / 4; ++m)
+      b[m] = row && gj0 + 4 * m < P.cols_g ? __ldcg(reinterpret_cast<const float4*>(e + k * sstride + 4 * m))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < NV / 4; ++m) {
+      a[m].x += b[m].x; a[m].y += b[m].y; a[m].z += b[m].z; a[m].w += b[m].w;
+    }
+  }
 #pragma unroll
   for (int m = 0; m < NV / 4; ++m) {
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (gi < P.rows_g && gj0 + 4 * m < P.cols_g) {
-      const float* e = base + static_cast<int64_t>(gi) * P.cols_g + gj0 + 4 * m;
-      a = __ldcg(reinterpret_cast<const float4*>(e));
-      for (int k = 1; k < n; ++k) {
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(e + k * sstride));
-        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-      }
-    }
-    v[4 * m] = a.x; v[4 * m + 1] = a.y; v[4 * m + 2] = a.z; v[4 * m + 3] = a.w;
+    v[4 * m] = a[m].x; v[4 * m + 1] = a[m].y; v[4 * m + 2] = a[m].z; v[4 * m + 3] = a[m].w;
   }
 }
 
@@ -724,16 +735,27 @@ __device__ __forceinline__ void fixup_tile(const GemmParams& P, const Unit& u, i
     // operand-swapped: GEMM row gi is the output column, partials [token][gi]
     if (gi >= P.rows_g) return;
     const float bsc = P.bias[g] != nullptr ? bf16_bits_to_f(static_cast<const uint16_t*>(P.bias[g])[gi]) : 0.0f;
-#pragma unroll 1
-    for (int c = half * HALF; c < (half + 1) * HALF; ++c) {
-      const int32_t gj = u.nt * BN + c;
-      if (gj >= P.cols_g) break;
-      const float* e = base + static_cast<int64_t>(gj) * P.rows_g + gi;
-      float a = __ldcg(e);
-      for (int k = 1; k < P.n_split; ++k) a += __ldcg(e + k * sstride);
-      const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
-      const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
-      for (int rep = 0; rep < P.n_rep; ++rep) epi_store1(P, a + bsc, P.out[g + rep], P.aux[g], off_o, off_a);
+    const int32_t gj0 = u.nt * BN + half * HALF;
+    const float* e = base + static_cast<int64_t>(gj0) * P.rows_g + gi;
+    float a[HALF];
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) a[c] = gj0 + c < P.cols_g ? __ldcg(e + static_cast<int64_t>(c) * P.rows_g) : 0.f;
+    for (int k = 1; k < P.n_split; ++k) {
+      float b[HALF];
+#pragma unroll
+      for (int c = 0; c < HALF; ++c)
+        b[c] = gj0 + c < P.cols_g ? __ldcg(e + k * sstride + static_cast<int64_t>(c) * P.rows_g) : 0.f;
+#pragma unroll
+      for (int c = 0; c < HALF; ++c) a[c] += b[c];
+    }
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) {
+      const int32_t gj = gj0 + c;
+      if (gj < P.cols_g) {
+        const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
+        const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
+        for (int rep = 0; rep < P.n_rep; ++rep) epi_store1(P, a[c] + bsc, P.out[g + rep], P.aux[g], off_o, off_a);
+      }
     }
   }
 }
