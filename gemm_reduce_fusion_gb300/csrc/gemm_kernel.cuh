@@ -117,11 +117,6 @@ struct GemmParams {
   CUtensorMap tmH[MAX_MAPS];
   int32_t omap[MAX_GROUPS], orow[MAX_GROUPS];
   int32_t hmap[MAX_GROUPS], hrow[MAX_GROUPS];
-  // Single-CTA split-K reduced in the kernel (fixup = 1): per (tile, epilogue
-  // warp) a counter as in finish_slice; the warp that writes a region's last
-  // split partial sums the n_split partials in split order and runs the epilogue.
-  int32_t fixup;
-  unsigned long long* fixup_cnt;
 };
 
 struct Unit {
@@ -668,98 +663,6 @@ __device__ __forceinline__ void drain_tile(const GemmParams& P, const Unit& u, i
   }
 }
 
-// Sum, in split order, of the n split-K partials of NV columns of row gi
-// starting at column gj0 (dense [rows_g][cols_g] per split and group, split
-// stride `sstride` floats); zeros outside the group.  The first partial is
-// the starting value, as in the second-stage kernel, so both give the same bits.
-template <int NV>
-__device__ __forceinline__ void sum_partial_row(const float* base, int64_t sstride, int n, int32_t gi, int32_t gj0,
-                                                const GemmParams& P, float (&v)[NV]) {
-  // every load of one split is issued before any of them is used: n round
-  // trips to L2 per chunk, not n per float4
-  const float* e = base + static_cast<int64_t>(gi) * P.cols_g + gj0;
-  const bool row = gi < P.rows_g;
-  float4 a[NV / 4];
-#pragma unroll
-  for (int m = 0; m < NV / 4; ++m)
-    a[m] = row && gj0 + 4 * m < P.cols_g ? __ldcg(reinterpret_cast<const float4*>(e + 4 * m))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 1; k < n; ++k) {
-    float4 b[NV / 4];
-#pragma unroll
-    for (int m = 0; m < NV / 4; ++m)
-      b[m] = row && gj0 + 4 * m < P.cols_g ? __ldcg(reinterpret_cast<const float4*>(e + k * sstride + 4 * m))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < NV / 4; ++m) {
-      a[m].x += b[m].x; a[m].y += b[m].y; a[m].z += b[m].z; a[m].w += b[m].w;
-    }
-  }
-#pragma unroll
-  for (int m = 0; m < NV / 4; ++m) {
-    v[4 * m] = a[m].x; v[4 * m + 1] = a[m].y; v[4 * m + 2] = a[m].z; v[4 * m + 3] = a[m].w;
-  }
-}
-
-// In-kernel split-K reduction (GemmParams::fixup) for one epilogue warp's
-// half of a tile whose split partial it has just written: the warp that
-// completes the region's n_split partials sums them and runs the epilogue;
-// the others return.  No warp waits for another.
-template <int BN, bool OUT_T>
-__device__ __forceinline__ void fixup_tile(const GemmParams& P, const Unit& u, int32_t tile, int32_t g, int32_t gi,
-                                           int half, int wslot, uint8_t* stg) {
-  const int lane = threadIdx.x & 31;
-  if (!finish_slice(P, P.fixup_cnt + static_cast<size_t>(tile) * NUM_EPI_WARPS + wslot, P.n_split)) return;
-  constexpr int HALF = BN / 2;
-  const int64_t per = static_cast<int64_t>(P.rows_g) * P.cols_g;
-  const int64_t sstride = static_cast<int64_t>(P.Gm) * P.Gn * per;
-  const float* base = P.partial + static_cast<int64_t>(g) * per;
-  if constexpr (!OUT_T) {
-    const int32_t gi0 = gi - lane;
-    if (P.out_f32) {
-#pragma unroll 1
-      for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 32) {
-        float v[32];
-        sum_partial_row<32>(base, sstride, P.n_split, gi, u.nt * BN + c0, P, v);
-        finish_chunk_staged<true>(P, g, gi0, u.nt * BN + c0, v, stg, lane);
-      }
-    } else {
-#pragma unroll 1
-      for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += 64) {
-        float v[64];
-        sum_partial_row<64>(base, sstride, P.n_split, gi, u.nt * BN + c0, P, v);
-        finish_chunk_staged<false>(P, g, gi0, u.nt * BN + c0, v, stg, lane);
-      }
-    }
-  } else {
-    // operand-swapped: GEMM row gi is the output column, partials [token][gi]
-    if (gi >= P.rows_g) return;
-    const float bsc = P.bias[g] != nullptr ? bf16_bits_to_f(static_cast<const uint16_t*>(P.bias[g])[gi]) : 0.0f;
-    const int32_t gj0 = u.nt * BN + half * HALF;
-    const float* e = base + static_cast<int64_t>(gj0) * P.rows_g + gi;
-    float a[HALF];
-#pragma unroll
-    for (int c = 0; c < HALF; ++c) a[c] = gj0 + c < P.cols_g ? __ldcg(e + static_cast<int64_t>(c) * P.rows_g) : 0.f;
-    for (int k = 1; k < P.n_split; ++k) {
-      float b[HALF];
-#pragma unroll
-      for (int c = 0; c < HALF; ++c)
-        b[c] = gj0 + c < P.cols_g ? __ldcg(e + k * sstride + static_cast<int64_t>(c) * P.rows_g) : 0.f;
-#pragma unroll
-      for (int c = 0; c < HALF; ++c) a[c] += b[c];
-    }
-#pragma unroll
-    for (int c = 0; c < HALF; ++c) {
-      const int32_t gj = gj0 + c;
-      if (gj < P.cols_g) {
-        const int64_t off_o = static_cast<int64_t>(gj) * P.ld_out + gi;
-        const int64_t off_a = static_cast<int64_t>(gj) * P.ld_aux + gi;
-        for (int rep = 0; rep < P.n_rep; ++rep) epi_store1(P, a[c] + bsc, P.out[g + rep], P.aux[g], off_o, off_a);
-      }
-    }
-  }
-}
-
 template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
@@ -979,8 +882,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
-      // the accumulator is released: the next tile's MMAs run while this sums
-      if (P.fixup) fixup_tile<BN, OUT_T>(P, u, t / P.n_split, g, gi, half, warp - 2, stg);
     }
     // this warp's bulk stores complete before the CTA exits
     if (P.out_tma && lane == 0) bulk_wait_all();

@@ -56,7 +56,6 @@ std::atomic<int64_t> g_trace_cap{0};
 std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (slice counters)
 std::atomic<int64_t> g_l2_hints{1};         // 1: L2 cache policies on operand loads and output stores
 std::atomic<int64_t> g_tma_store{1};        // 1: staged epilogues leave shared memory by TMA store
-std::atomic<int64_t> g_debug_split_stage{0};  // 1: split-K always summed by the second-stage kernel
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -300,23 +299,15 @@ struct Shape {
   // CTA pairs: the tiles of a last partial wave run as tail_split k-slices
   int64_t tail_start = 0;
   int tail_split = 1;
-  // single-CTA split-K summed inside the GEMM launch (no second stage)
-  bool fixup = false;
   bool empty() const { return rows_g == 0 || cols_g == 0; }
   int64_t tail_tiles() const { return tail_split > 1 ? units0 - tail_start : 0; }
   size_t tail_cnt_bytes() const {
     return static_cast<size_t>((tail_tiles() * 2 * NUM_EPI_WARPS * 8 + 255) / 256 * 256);
   }
-  size_t split_bytes() const {  // split-K fp32 partials, padded to 256 bytes
-    return n_split > 1 ? (static_cast<size_t>(n_split) * Gm * Gn * rows_g * cols_g * 4u + 255) / 256 * 256 : 0;
-  }
-  size_t fixup_cnt_bytes() const {  // one 8-byte counter per (tile, epilogue warp)
-    return fixup ? static_cast<size_t>(units0) * NUM_EPI_WARPS * 8u : 0;
-  }
   size_t partial_bytes() const {
     if (tail_split > 1)  // counters, then one fp32 256 x 256 tile per slice
       return tail_cnt_bytes() + static_cast<size_t>(tail_tiles()) * tail_split * 256 * 256 * 4u;
-    return split_bytes() + fixup_cnt_bytes();
+    return n_split > 1 ? static_cast<size_t>(n_split) * Gm * Gn * rows_g * cols_g * 4u : 0;
   }
 };
 
@@ -362,7 +353,6 @@ void finish_shape(Shape* s) {
   s->pair = false;
   s->tail_start = 0;
   s->tail_split = 1;
-  s->fixup = false;
   if (s->units0 == 0 || s->kb_total == 0) return;
   // 256x256 tiles on CTA pairs when a group has at least 256 rows and the
   // pair tiles still fill the clusters; otherwise 128x256 tiles (with split-K
@@ -421,12 +411,6 @@ void finish_shape(Shape* s) {
     s->kb_per_split = kPreciseKb;
     s->n_split = static_cast<int>(cdiv(s->kb_total, kPreciseKb));
   }
-  // A split launch of one wave with few splits sums its partials inside the
-  // kernel (the warp that writes a tile region's last partial adds them up),
-  // which saves the second-stage launch; more splits or several waves keep
-  // the second stage, which spreads the summing over every SM.
-  s->fixup = s->n_split > 1 && s->n_split <= 4 && s->units0 * s->n_split <= kPlanSMs && !s->no_pair &&
-             g_debug_split_stage.load() == 0;
 }
 
 // Chunk used by a call: 0 -> scheduler; clamp to M.
@@ -731,9 +715,6 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     return TP_OK;
   }
   if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  P.fixup = s.fixup ? 1 : 0;
-  if (s.fixup)
-    P.fixup_cnt = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + kStatusBytes + s.split_bytes());
   // slice counters tagged with another launch's number read as zero
   P.epoch = g_launch_epoch.fetch_add(1) + 1;
   if (s.tail_split > 1) {
@@ -767,7 +748,7 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
   const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
                          : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
   if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
-  if (s.n_split > 1 && !s.fixup && (phases & 2)) return launch_reduce(L, s, s.n_split, stream, di);
+  if (s.n_split > 1 && (phases & 2)) return launch_reduce(L, s, s.n_split, stream, di);
   return TP_OK;
 }
 
@@ -891,10 +872,6 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_TMA_STORE:
       if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
       g_tma_store.store(value);
-      return TP_OK;
-    case TP_DEBUG_SPLIT_STAGE:
-      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
-      g_debug_split_stage.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;

@@ -115,10 +115,8 @@ def test_split_plan_and_forced_split(tp):
     contractions; TP_DEBUG_SPLIT_K overrides it (fp32 partials: one copy of
     the output per split)."""
     def splits(op, p, M, N, K, chunk):
-        return (tp.tp_workspace_size(op, p, M, N, K, chunk) - 256) // (M * N * 4)  # partials padded to 256 B
+        return (tp.tp_workspace_size(op, p, M, N, K, chunk) - 256) / (M * N * 4)
     AR = tp.TP_OP_ROW_AR
-    # partials summed by the second-stage kernel: the workspace is status + partials only
-    assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_STAGE, 1) == tp.TP_OK
     # [128, 2048] output in 64 swapped tiles of 32 tokens, 32 k-blocks: 2 splits fill one wave
     assert splits(AR, 2, 128, 2048, 1024, 32) == 2
     # 32 tiles of 128 x 256, 64 k-blocks: 4 splits
@@ -140,19 +138,7 @@ def test_split_plan_and_forced_split(tp):
         assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, -1) == tp.TP_ERR_INVALID_ARG
     finally:
         tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 0)
-        tp.tp_debug_set(tp.TP_DEBUG_SPLIT_STAGE, 0)
     assert splits(AR, 2, 300, 520, 200, 0) == 0
-
-
-def test_in_kernel_split_sum_workspace(tp):
-    """A split launch of one wave with at most 4 splits sums its partials in
-    the GEMM kernel: the workspace adds one 8-byte counter per (tile,
-    epilogue warp) after the partials.  The worked example: 64 swapped tiles,
-    2 splits of [128, 2048] fp32 partials."""
-    AR = tp.TP_OP_ROW_AR
-    assert tp.tp_workspace_size(AR, 2, 128, 2048, 1024, 32) == 256 + 2 * 128 * 2048 * 4 + 64 * 8 * 8
-    # several waves (the decode-like FC2 with 11 splits) keep the second stage: no counters
-    assert tp.tp_workspace_size(AR, 8, 16, 12288, 6144, 0) == 256 + 11 * 16 * 12288 * 4
 
 
 def test_workspace_holds_the_last_wave_slices(tp):

@@ -72,19 +72,14 @@ def ws_for(tp, op, p, M, N, K, chunk):
     return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
-@pytest.fixture(params=[(0, 0), (3, 0), (3, 1)], ids=["planned_split", "split3", "split3_stage2"])
+@pytest.fixture(params=[0, 3], ids=["planned_split", "split3"])
 def split_k(tp, request):
-    """The planner's split-K factor, or every single-CTA launch below one
-    wave split 3 ways: the split-K partials and their sums then run on the
-    small shapes the planner leaves whole -- summed inside the GEMM kernel
-    where the launch qualifies (split3), or always by the second-stage
-    kernel (split3_stage2)."""
-    n, stage2 = request.param
-    assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, n) == tp.TP_OK
-    assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_STAGE, stage2) == tp.TP_OK
-    yield n
+    """The planner's split-K factor (0), or every single-CTA launch below one
+    wave split 3 ways: the split-K partials and the second stage's epilogues
+    then run on the small shapes the planner leaves whole."""
+    assert tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, request.param) == tp.TP_OK
+    yield request.param
     tp.tp_debug_set(tp.TP_DEBUG_SPLIT_K, 0)
-    tp.tp_debug_set(tp.TP_DEBUG_SPLIT_STAGE, 0)
 
 
 ROW_CASES = [  # p, M, N, K, chunk_m
