@@ -932,15 +932,26 @@ struct PairCfg {
   static_assert(SMEM_BYTES <= 232448, "227 KiB of dynamic shared memory per CTA");
 };
 
-// TAIL: the launch runs its last partial wave as k-slices (P.tail_split >
-// 1).  A separate instantiation, so that launches without slices carry none
-// of that code.
-template <bool A_MN, bool B_MN, int BKP, bool TAIL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    tp_gemm_pair_kernel(const __grid_constant__ GemmParams P) {
-  using Cfg = PairCfg<A_MN, B_MN, BKP>;
+// One launch of the pair kernel may carry two independent GEMM problems
+// (the dX and dW products of one backward call): units [0, split) are problem
+// 0's, units [split, total) problem 1's, on the same clusters, so the two
+// share one fill, one drain and one partial last wave.
+struct PairLaunch2 {
+  GemmParams P[2];
+  int32_t split;  // units of problem 0
+  int32_t total;  // units of both problems
+};
+
+// Body of the CTA-pair kernel over NPROB problems (1 or 2): problem i has
+// operand majors (A_i, B_i).  Launch-wide state -- the status word, the
+// device wait limit, the trace and the test hook -- comes from problem 0.
+template <bool A0, bool B0, bool A1, bool B1, int BKP, bool TAIL, int NPROB>
+__device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, int32_t total) {
+  using Cfg = PairCfg<A0, B0, BKP>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int KC = BKP / 64;  // 64-wide K chunks per k-block
+  static_assert(NPROB == 1 || !TAIL, "last-wave slices only in single-problem launches");
+  const GemmParams& P = Ps[0];
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -964,6 +975,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool leader = crank == 0;
   const int32_t first = static_cast<int32_t>(blockIdx.x >> 1);
   const int32_t stride = static_cast<int32_t>(gridDim.x >> 1);
+  // problem of unit t, and t's index within it
+  auto prob_of = [&](int32_t t) -> int { return (NPROB == 2 && t >= split) ? 1 : 0; };
+  auto local = [&](int32_t t, int pi) -> int32_t { return pi ? t - split : t; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -999,18 +1013,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t armed = 0, armed_parity = 0;
       int32_t n_issued = 0;
       bool ok = true;
-      const uint64_t pol_a = l2_policy(P.a_hint);
-      const uint64_t pol_b = l2_policy(P.b_hint);
-      for (int32_t t = first; t < P.num_units && ok; t += stride) {
+      uint64_t pol_a[NPROB], pol_b[NPROB];
+#pragma unroll
+      for (int i = 0; i < NPROB; ++i) {
+        pol_a[i] = l2_policy(Ps[i].a_hint);
+        pol_b[i] = l2_policy(Ps[i].b_hint);
+      }
+      for (int32_t t = first; t < total && ok; t += stride) {
+        const int pi = prob_of(t);
+        const GemmParams& Q = Ps[pi];
+        const bool a_mn = pi ? A1 : A0;
+        const bool b_mn = pi ? B1 : B0;
         int32_t tj = -1, tk = 0;
-        const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
-        const int32_t arow = P.a_row_gm * u.gm + u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM;
-        const int32_t bcol = P.b_col_gn * u.gn + u.nt * Cfg::BN + static_cast<int32_t>(crank) * Cfg::BNH;
+        const Unit u = TAIL ? decode_pair_unit(Q, t, tj, tk) : decode_unit(Q, local(t, pi));
+        const int32_t arow = Q.a_row_gm * u.gm + u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM;
+        const int32_t bcol = Q.b_col_gn * u.gn + u.nt * Cfg::BN + static_cast<int32_t>(crank) * Cfg::BNH;
         for (int32_t q = u.q0; q < u.q1; ++q) {
-          const int32_t s = q / P.kb_per_seg;
-          const int32_t kc = (q % P.kb_per_seg) * BKP;
-          const int32_t kca = kc + s * P.a_koff_s;
-          const int32_t kcb = kc + s * P.b_koff_s;
+          const int32_t s = q / Q.kb_per_seg;
+          const int32_t kc = (q % Q.kb_per_seg) * BKP;
+          const int32_t kca = kc + s * Q.a_koff_s;
+          const int32_t kcb = kc + s * Q.b_koff_s;
           if (!wait_bar(empty_bar(stage), phase ^ 1u, P, abort_flag, 1u)) {
             ok = false;
             break;
@@ -1022,8 +1044,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             continue;
           }
-          const CUtensorMap* am = &P.tmA[P.a_idx_gm * u.gm + P.a_idx_gn * u.gn + P.a_idx_s * s];
-          const CUtensorMap* bm = &P.tmB[P.b_idx_gm * u.gm + P.b_idx_gn * u.gn + P.b_idx_s * s];
+          const CUtensorMap* am = &Q.tmA[Q.a_idx_gm * u.gm + Q.a_idx_gn * u.gn + Q.a_idx_s * s];
+          const CUtensorMap* bm = &Q.tmB[Q.b_idx_gm * u.gm + Q.b_idx_gn * u.gn + Q.b_idx_s * s];
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
           const uint32_t sa = sA0 + stage * Cfg::A_BYTES;
@@ -1031,13 +1053,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // Shared-memory tiles: K-major operands as KC consecutive [rows][64]
           // sub-tiles (one per 64-wide K chunk), MN-major operands as
           // consecutive [BKP K-rows][64] sub-tiles (one per 64-wide MN block).
-          if (P.map3d) {
-            if (A_MN) tma_load_3d_pair(sa, am, fb, 0, kca, arow / 64, pol_a);
-            else tma_load_3d_pair(sa, am, fb, 0, arow, kca / 64, pol_a);
-            if (B_MN) tma_load_3d_pair(sb, bm, fb, 0, kcb, bcol / 64, pol_b);
-            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kcb / 64, pol_b);
+          if (Q.map3d) {
+            if (a_mn) tma_load_3d_pair(sa, am, fb, 0, kca, arow / 64, pol_a[pi]);
+            else tma_load_3d_pair(sa, am, fb, 0, arow, kca / 64, pol_a[pi]);
+            if (b_mn) tma_load_3d_pair(sb, bm, fb, 0, kcb, bcol / 64, pol_b[pi]);
+            else tma_load_3d_pair(sb, bm, fb, 0, bcol, kcb / 64, pol_b[pi]);
           } else {
-            if (A_MN) {
+            if (a_mn) {
 #pragma unroll
               for (int j = 0; j < BM / 64; ++j)
                 tma_load_2d_pair(sa + j * (64 * BKP * 2), am, fb, arow + 64 * j, kca);
@@ -1045,7 +1067,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int h = 0; h < KC; ++h) tma_load_2d_pair(sa + h * (BM * 128), am, fb, kca + 64 * h, arow);
             }
-            if (B_MN) {
+            if (b_mn) {
 #pragma unroll
               for (int j = 0; j < Cfg::BNH / 64; ++j)
                 tma_load_2d_pair(sb + j * (64 * BKP * 2), bm, fb, bcol + 64 * j, kcb);
@@ -1072,15 +1094,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ pair MMA issuer (CTA 0)
-      constexpr uint32_t idesc = make_idesc_bf16(2 * BM, Cfg::BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int32_t t = first; t < P.num_units && ok; t += stride) {
+      for (int32_t t = first; t < total && ok; t += stride) {
+        const int pi = prob_of(t);
+        const GemmParams& Q = Ps[pi];
+        const bool a_mn = pi ? A1 : A0;
+        const bool b_mn = pi ? B1 : B0;
+        const uint32_t idesc = pi ? make_idesc_bf16(2 * BM, Cfg::BN, A1, B1) : make_idesc_bf16(2 * BM, Cfg::BN, A0, B0);
         int32_t tj = -1, tk = 0;
-        const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
+        const Unit u = TAIL ? decode_pair_unit(Q, t, tj, tk) : decode_unit(Q, local(t, pi));
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, P, abort_flag, 2u)) break;
         tc_fence_after();
         trace_mma_start(P, t, u.ch, blockIdx.x >> 1);
@@ -1099,9 +1125,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // MN-major: 16 K-rows of 128 bytes per step.
             const uint32_t ka = (kk / 4) * (BM * 128) + (kk % 4) * (UMMA_K * 2);
             const uint32_t kb = (kk / 4) * (Cfg::BNH * 128) + (kk % 4) * (UMMA_K * 2);
-            const uint64_t ad = A_MN ? make_sw128_desc(sa + kk * (UMMA_K * 128), 64 * BKP * 2, 1024)
+            const uint64_t ad = a_mn ? make_sw128_desc(sa + kk * (UMMA_K * 128), 64 * BKP * 2, 1024)
                                      : make_sw128_desc(sa + ka, 16, 1024);
-            const uint64_t bd = B_MN ? make_sw128_desc(sb + kk * (UMMA_K * 128), 64 * BKP * 2, 1024)
+            const uint64_t bd = b_mn ? make_sw128_desc(sb + kk * (UMMA_K * 128), 64 * BKP * 2, 1024)
                                      : make_sw128_desc(sb + kb, 16, 1024);
             umma_bf16_pair(d_tmem, ad, bd, idesc, (q > u.q0 || kk > 0) ? 1u : 0u);
           }
@@ -1128,24 +1154,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = 32 * q + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int32_t t = first; t < P.num_units; t += stride) {
+    for (int32_t t = first; t < total; t += stride) {
+      const int pi = prob_of(t);
+      const GemmParams& Q = Ps[pi];
       int32_t tj = -1, tk = 0;
-      const Unit u = TAIL ? decode_pair_unit(P, t, tj, tk) : decode_unit(P, t);
+      const Unit u = TAIL ? decode_pair_unit(Q, t, tj, tk) : decode_unit(Q, local(t, pi));
       bool ok = wait_bar(tfull_bar(acc), acc_phase, P, abort_flag, 4u);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int32_t g = u.gm * P.Gn + u.gn;
+      const int32_t g = u.gm * Q.Gn + u.gn;
       const int32_t gi = u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM + row_in_tile;
-      const bool row_ok = gi < P.rows_g;
+      const bool row_ok = gi < Q.rows_g;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * Cfg::BN);
       uint8_t* stg = base_ptr + Cfg::STG_OFF + (warp - 2) * STAGE_BYTES_PER_WARP;
       if (leader && warp == 2 && lane == 0) trace_acc_full(P, t);
       if (TAIL && tj >= 0)
-        drain_slice_wide(P, u, P.tail_part, P.tail_cnt, tj, tk, P.tail_split, 2, crank, g, gi, t_row, half,
+        drain_slice_wide(Q, u, Q.tail_part, Q.tail_cnt, tj, tk, Q.tail_split, 2, crank, g, gi, t_row, half,
                          warp - 2, stg);
-      else drain_tile<Cfg::BN, false>(P, u, t % P.n_split, g, gi, row_ok, t_row, half, stg);
+      else drain_tile<Cfg::BN, false>(Q, u, 0, g, gi, row_ok, t_row, half, stg);
       if (lane == 0) trace_drained(P, t);
       tc_fence_before();
       __syncwarp();
@@ -1156,7 +1184,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     // this warp's bulk stores complete before the CTA exits
-    if (P.out_tma && lane == 0) bulk_wait_all();
+    bool any_tma = P.out_tma != 0;
+    if (NPROB == 2) any_tma = any_tma || Ps[NPROB - 1].out_tma != 0;
+    if (any_tma && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -1175,6 +1205,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
   }
+}
+
+// TAIL: the launch runs its last partial wave as k-slices (P.tail_split >
+// 1).  A separate instantiation, so that launches without slices carry none
+// of that code.
+template <bool A_MN, bool B_MN, int BKP, bool TAIL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tp_gemm_pair_kernel(const __grid_constant__ GemmParams P) {
+  pair_body<A_MN, B_MN, A_MN, B_MN, BKP, TAIL, 1>(&P, P.num_units, P.num_units);
+}
+
+// Two problems in one launch (PairLaunch2), majors (A0, B0) then (A1, B1).
+template <bool A0, bool B0, bool A1, bool B1, int BKP>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tp_gemm_pair2_kernel(const __grid_constant__ PairLaunch2 L) {
+  pair_body<A0, B0, A1, B1, BKP, false, 2>(L.P, L.split, L.total);
 }
 
 // ------------------------------------------------------------- split-K stage 2

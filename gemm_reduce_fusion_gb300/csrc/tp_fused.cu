@@ -56,6 +56,7 @@ std::atomic<int64_t> g_trace_cap{0};
 std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (slice counters)
 std::atomic<int64_t> g_l2_hints{1};         // 1: L2 cache policies on operand loads and output stores
 std::atomic<int64_t> g_tma_store{1};        // 1: staged epilogues leave shared memory by TMA store
+std::atomic<int64_t> g_debug_no_fuse{0};    // 1: backward dX and dW always as two launches
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -228,6 +229,50 @@ cudaError_t launch_pair_t(const GemmParams& P, int clusters, cudaStream_t s) {
   cfg.attrs = attr2;
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, P);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Two problems in one CTA-pair launch: dY.W^T (K-major A and B) units first,
+// then X^T.dY (MN-major A and B) units.
+cudaError_t launch_pair2(const PairLaunch2& L2, int clusters, cudaStream_t s) {
+  using Cfg = PairCfg<false, false, PAIR_BK>;
+  auto k = tp_gemm_pair2_kernel<false, false, true, true, PAIR_BK>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2] = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static std::atomic<int> max_active[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    int m = max_active[dev].load(std::memory_order_relaxed);
+    if (m == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0) {
+        m = n;
+        max_active[dev].store(n, std::memory_order_relaxed);
+      }
+    }
+    if (m > 0 && clusters > m) {
+      clusters = m;
+      cfg.gridDim = dim3(2 * clusters, 1, 1);
+    }
+  }
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, k, L2);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -622,6 +667,7 @@ bool plan_out_maps(const Shape& s, void* const* ptrs, int n_rep, int64_t ld, boo
 
 tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
                             const DevInfo& di, int phases);
+void prepare_gemm(Launch& L, tp_dtype out_dtype, void* ws);
 
 // Second stage over the launch's groups: out = epilogue(bias + sum of the
 // n_split fp32 partials in split order); n_split == 0 sums nothing.
@@ -676,6 +722,70 @@ tp_status run_launch(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t strea
   return run_launch_phases(L, out_dtype, ws, stream, di, 3);
 }
 
+// Longest per-cluster run, in k-blocks, of a pair launch's units under the
+// kernel's static assignment (unit t on cluster t mod C): n0 units of kb0
+// k-blocks, then n1 units of kb1 (n1 = 0: one problem, whose last partial
+// wave may run as `tail` k-slices of each of its last tiles).
+int64_t pair_makespan(int64_t n0, int64_t kb0, int64_t n1, int64_t kb1, int64_t C, int tail) {
+  if (tail > 1 && n1 == 0) {
+    const int64_t R = n0 % C;
+    return (n0 / C) * kb0 + cdiv(cdiv(R * tail, C) * kb0, tail);
+  }
+  int64_t worst = 0;
+  for (int64_t c = 0; c < std::min<int64_t>(C, n0 + n1); ++c) {
+    const int64_t a = n0 > c ? (n0 - c + C - 1) / C : 0;
+    const int64_t all = (n0 + n1 - c + C - 1) / C;
+    worst = std::max(worst, a * kb0 + (all - a) * kb1);
+  }
+  return worst;
+}
+
+// The dX (dY.W^T) and dW (X^T.dY) launches of one backward call: one CTA-pair
+// launch for both when each is a plain pair launch (no split-K) and the
+// combined static assignment finishes no later than the two launches one
+// after the other; otherwise the two launches.  The two GEMMs are
+// independent: neither reads what the other writes.
+tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype out_dtype, void* ws,
+                       cudaStream_t stream, const DevInfo& di) {
+  const Shape& a = LX.shape;
+  const Shape& b = LW.shape;
+  const bool both = do_x && do_w && !a.empty() && !b.empty() && a.kb_total > 0 && b.kb_total > 0 &&
+                    a.pair && b.pair && !a.swap && LX.variant == V_KK && LW.variant == V_MM &&
+                    g_debug_no_fuse.load() == 0;
+  if (both) {
+    const int64_t C = di.sms / 2;
+    const int64_t kba = a.S * cdiv(a.kseg, PAIR_BK), kbb = b.S * cdiv(b.kseg, PAIR_BK);
+    const int64_t sep = pair_makespan(a.units0, kba, 0, 0, C, a.tail_split) +
+                        pair_makespan(b.units0, kbb, 0, 0, C, b.tail_split);
+    const int64_t fused = pair_makespan(a.units0, kba, b.units0, kbb, C, 1);
+    if (fused <= sep) {
+      // whole tiles only: the fused launch has a single partial last wave
+      Shape sa = a, sb = b;
+      sa.tail_split = sb.tail_split = 1;
+      sa.tail_start = sb.tail_start = 0;
+      fill_common(&LX.P, sa);
+      fill_common(&LW.P, sb);
+      LX.shape = sa;
+      LW.shape = sb;
+      prepare_gemm(LX, out_dtype, ws);
+      prepare_gemm(LW, out_dtype, ws);
+      LW.P.epoch = LX.P.epoch;
+      static thread_local PairLaunch2 L2;   // 14 KB: kept off the stack
+      L2.P[0] = LX.P;
+      L2.P[1] = LW.P;
+      L2.split = LX.P.num_units;
+      L2.total = LX.P.num_units + LW.P.num_units;
+      const int clusters = static_cast<int>(std::min<int64_t>(L2.total, di.sms / 2));
+      return launch_pair2(L2, clusters, stream) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    }
+  }
+  if (do_x) {
+    const tp_status st = run_launch(LX, out_dtype, ws, stream, di);
+    if (st != TP_OK) return st;
+  }
+  return do_w ? run_launch(LW, out_dtype, ws, stream, di) : TP_OK;
+}
+
 // phases: bit 0 = the GEMM launch (or the K == 0 fill), bit 1 = the split-K
 // second stage.
 tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_t stream,
@@ -714,6 +824,21 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     }
     return TP_OK;
   }
+  prepare_gemm(L, out_dtype, ws);
+  const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
+                         : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
+  if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
+  if (s.n_split > 1 && (phases & 2)) return launch_reduce(L, s, s.n_split, stream, di);
+  return TP_OK;
+}
+
+// The launch-time fields of a GEMM launch with work to do (K > 0): workspace
+// regions, the launch number, L2 policies and the TMA-store output maps.
+void prepare_gemm(Launch& L, tp_dtype out_dtype, void* ws) {
+  const Shape& s = L.shape;
+  GemmParams& P = L.P;
+  P.status = static_cast<uint32_t*>(ws);
+  P.out_f32 = out_dtype == TP_FP32 ? 1 : 0;
   if (s.n_split > 1) P.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
   // slice counters tagged with another launch's number read as zero
   P.epoch = g_launch_epoch.fetch_add(1) + 1;
@@ -745,11 +870,6 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
       ok = plan_out_maps(s, P.aux, 1, P.ld_aux, f32, P.tmH, P.hmap, P.hrow);
     P.out_tma = ok ? 1 : 0;
   }
-  const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
-                         : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
-  if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
-  if (s.n_split > 1 && (phases & 2)) return launch_reduce(L, s, s.n_split, stream, di);
-  return TP_OK;
 }
 
 // ------------------------------------------------------------------ validation
@@ -872,6 +992,10 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_TMA_STORE:
       if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
       g_tma_store.store(value);
+      return TP_OK;
+    case TP_DEBUG_NO_BWD_FUSION:
+      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
+      g_debug_no_fuse.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;
@@ -1196,12 +1320,11 @@ tp_status tp_ag_matmul(const void* const* x, const void* const* w, const void* c
 // ---------------------------------------------------------------- backward
 
 // Weight gradient dA_g = Xsrc_g^T . dYsrc_g for g = 0..p-1 ([K, N] each,
-// contraction over the M tokens); both operands MN-major.
-static tp_status weight_grad(const Shape& s, const void* const* xk, const void* x1,
+// contraction over the M tokens); both operands MN-major.  Fills L for
+// run_bwd_pair.
+static tp_status weight_grad(Launch& L, const Shape& s, const void* const* xk, const void* x1,
                              const void* const* dyk, const void* dy1, void* const* dw, int p,
-                             int64_t M, int64_t N, int64_t K, tp_dtype dt, void* ws,
-                             cudaStream_t stream, const DevInfo& di) {
-  Launch L;
+                             int64_t M, int64_t N, int64_t K) {
   L.shape = s;
   init_params(&L.P);
   fill_common(&L.P, s);
@@ -1227,7 +1350,7 @@ static tp_status weight_grad(const Shape& s, const void* const* xk, const void* 
   P.ld_out = N;
   P.epi = EPI_NONE;
   L.variant = V_MM;
-  return run_launch(L, dt, ws, stream, di);
+  return TP_OK;
 }
 
 tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* const* dy, void* dx,
@@ -1260,8 +1383,9 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
   if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
+  Launch LX, LW;
   if (dx_work) {
-    Launch L;
+    Launch& L = LX;
     L.shape = shapes[0];
     init_params(&L.P);
     fill_common(&L.P, L.shape);
@@ -1288,9 +1412,9 @@ tp_status tp_col_linear_bwd(const void* x, const void* const* w, const void* con
     P.ld_out = K;
     P.epi = EPI_NONE;
     L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
-    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
-  if (dw_work) TP_TRY(weight_grad(shapes[1], nullptr, x, dy, nullptr, dw, p, M, N, K, out_dtype, ws, stream, di));
+  if (dw_work) TP_TRY(weight_grad(LW, shapes[1], nullptr, x, dy, nullptr, dw, p, M, N, K));
+  TP_TRY(run_bwd_pair(LX, dx_work, LW, dw_work, out_dtype, ws, stream, di));
   if (db_work) TP_TRY(bias_grad(dy, p, 1, db, M, N, out_dtype, stream));   // db_k = sum of dY_k's rows
   return TP_OK;
 }
@@ -1327,8 +1451,9 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
   if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
+  Launch LX, LW;
   if (dx_work) {
-    Launch L;
+    Launch& L = LX;
     L.shape = shapes[0];
     init_params(&L.P);
     fill_common(&L.P, L.shape);
@@ -1360,9 +1485,9 @@ tp_status tp_row_linear_bwd(const void* const* x, const void* const* w, const vo
     P.ld_aux = K;
     P.epi = preact ? EPI_DGELU : EPI_NONE;
     L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
-    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
-  if (dw_work) TP_TRY(weight_grad(shapes[1], x, nullptr, nullptr, dy, dw, p, M, N, K, out_dtype, ws, stream, di));
+  if (dw_work) TP_TRY(weight_grad(LW, shapes[1], x, nullptr, nullptr, dy, dw, p, M, N, K));
+  TP_TRY(run_bwd_pair(LX, dx_work, LW, dw_work, out_dtype, ws, stream, di));
   if (db_work) TP_TRY(bias_grad(&dy, 1, 1, &db, M, N, out_dtype, stream));   // db = sum of dY's rows
   return TP_OK;
 }
@@ -1405,8 +1530,9 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
   if (!dx_work && !dw_work && !db_work) return TP_OK;
   DevInfo di;
   TP_TRY(device_info(&di));
+  Launch LX, LW;
   if (dx_work) {
-    Launch L;
+    Launch& L = LX;
     L.shape = shapes[0];
     init_params(&L.P);
     fill_common(&L.P, L.shape);
@@ -1435,10 +1561,9 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
     P.ld_out = K;
     P.epi = EPI_NONE;
     L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
-    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
   if (dw_work) {
-    Launch L;
+    Launch& L = LW;
     L.shape = shapes[1];
     init_params(&L.P);
     fill_common(&L.P, L.shape);
@@ -1460,8 +1585,8 @@ extern "C" tp_status tp_ag_matmul_bwd(const void* const* x, const void* const* w
     P.ld_out = N;
     P.epi = EPI_NONE;
     L.variant = V_MM;
-    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
+  TP_TRY(run_bwd_pair(LX, dx_work, LW, dw_work, out_dtype, ws, stream, di));
   if (db_work) TP_TRY(bias_grad(dy, p, 1, db, M, N, out_dtype, stream));   // db_k = sum of dY_k's M rows
   return TP_OK;
 }
@@ -1504,8 +1629,9 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
   DevInfo di;
   TP_TRY(device_info(&di));
   const size_t es = esize(out_dtype);
+  Launch LX, LW;
   if (dx_work) {
-    Launch L;
+    Launch& L = LX;
     L.shape = shapes[0];
     init_params(&L.P);
     fill_common(&L.P, L.shape);
@@ -1544,10 +1670,9 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
     P.ld_aux = K;
     P.epi = preact ? EPI_DGELU : EPI_NONE;
     L.variant = s.swap ? sw_variant_kk(s.bn) : V_KK;
-    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
   if (dw_work) {
-    Launch L;
+    Launch& L = LW;
     L.shape = shapes[1];
     init_params(&L.P);
     fill_common(&L.P, L.shape);
@@ -1570,8 +1695,8 @@ extern "C" tp_status tp_row_linear_bwd_reducescatter(const void* const* x, const
     P.ld_out = N;
     P.epi = EPI_NONE;
     L.variant = V_MM;
-    TP_TRY(run_launch(L, out_dtype, ws, stream, di));
   }
+  TP_TRY(run_bwd_pair(LX, dx_work, LW, dw_work, out_dtype, ws, stream, di));
   // db = sum over the p token shards of dY, in shard order, of their rows
   if (db_work) TP_TRY(bias_grad(dy, p, p, &db, Mp, N, out_dtype, stream));
   return TP_OK;

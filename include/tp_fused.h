@@ -355,6 +355,9 @@ tp_status tp_noalloc_device_status(cudaStream_t stream);
  *   TP_DEBUG_TMA_STORE: 1 (default) lets the staged epilogue leave shared
  *     memory by TMA tensor stores wherever the outputs allow it; 0 forces
  *     plain 16-byte stores (bit-identical results; for testing both paths).
+ *   TP_DEBUG_NO_BWD_FUSION: 0 (default) lets a backward call run its dX and
+ *     dW products as one CTA-pair launch where that is planned to finish
+ *     sooner; 1 always runs them as two launches (bit-identical results).
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
 typedef enum {
   TP_DEBUG_TIMEOUT_MS = 0,
@@ -363,7 +366,8 @@ typedef enum {
   TP_DEBUG_NO_TAIL_SLICES = 3,
   TP_DEBUG_SPLIT_K = 4,
   TP_DEBUG_L2_HINTS = 5,
-  TP_DEBUG_TMA_STORE = 6
+  TP_DEBUG_TMA_STORE = 6,
+  TP_DEBUG_NO_BWD_FUSION = 7
 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 

@@ -1067,3 +1067,68 @@ def test_store_paths_bitwise_identical(tp, tile_mode, p, M, N, K):
         iv = torch.int32 if u.dtype == torch.float32 else torch.int16
         assert torch.equal(u.view(iv), v.view(iv)), f"output {i} differs between the store paths"
     assert_close(host_f64(a[-1]), oracle.row_fwd_allreduce(xs, ws), True, "fp32 AllReduce")
+
+
+@pytest.fixture
+def no_fusion(tp):
+    yield
+    tp.tp_debug_set(tp.TP_DEBUG_NO_BWD_FUSION, 0)
+
+
+@pytest.mark.parametrize("tile_mode", [0, 2], indirect=True)
+@pytest.mark.parametrize("p,M,N,K", [(2, 2048, 2048, 2048), (3, 300, 264, 136), (4, 512, 256, 192)])
+def test_backward_fused_launch_bitwise_and_exact(tp, tile_mode, no_fusion, p, M, N, K):
+    """A backward call's dX and dW products may run as one CTA-pair launch
+    (where the planner expects it to finish sooner than two); the results
+    must equal those of the two separate launches bit for bit, and the
+    oracle exactly on integer inputs, for the row backward (with GeLU'), the
+    column backward and both sequence-parallel backward calls."""
+    import torch
+    x = ints((M, K), 600)
+    xs = [ints((M, K), 601 + r) for r in range(p)]
+    xsh = [ints((M // p, K), 611 + r) for r in range(p)]
+    w = [ints((K, N), 621 + r) for r in range(p)]
+    dy = ints((M, N), 631)
+    dys = [ints((M, N), 641 + r) for r in range(p)]
+    dysh = [ints((M // p, N), 651 + r) for r in range(p)]
+    f32 = dict(dtype=torch.float32, device="cuda")
+    W, DY, DYS, DYSH = [dev(a) for a in w], dev(dy), [dev(a) for a in dys], [dev(a) for a in dysh]
+    X, XS, XSH = dev(x), [dev(a) for a in xs], [dev(a) for a in xsh]
+    H = [dev(synth.normal_bf16((M, K), 661 + r)) for r in range(p)]
+
+    def run():
+        r = {}
+        r["row_dx"] = [torch.empty((M, K), **f32) for _ in range(p)]
+        r["row_dw"] = [torch.empty((K, N), **f32) for _ in range(p)]
+        tp.tp_row_linear_bwd(XS, W, DY, r["row_dx"], r["row_dw"], ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0))
+        r["row_dx_gelu"] = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        r["row_dw_bf16"] = [torch.empty((K, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        tp.tp_row_linear_bwd(XS, W, DY, r["row_dx_gelu"], r["row_dw_bf16"],
+                             ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0), preact=H)
+        r["col_dx"] = [torch.empty((M, K), **f32)]
+        r["col_dw"] = [torch.empty((K, N), **f32) for _ in range(p)]
+        tp.tp_col_linear_bwd(X, W, DYS, r["col_dx"][0], r["col_dw"], ws_for(tp, tp.TP_OP_COL_BWD, p, M, N, K, 0))
+        r["ag_dx"] = [torch.empty((M // p, K), **f32) for _ in range(p)]
+        r["ag_dw"] = [torch.empty((K, N), **f32) for _ in range(p)]
+        tp.tp_ag_matmul_bwd(XSH, W, DYS, r["ag_dx"], r["ag_dw"], ws_for(tp, tp.TP_OP_AG_MM_BWD, p, M, N, K, 0))
+        r["rs_dx"] = [torch.empty((M, K), **f32) for _ in range(p)]
+        r["rs_dw"] = [torch.empty((K, N), **f32) for _ in range(p)]
+        tp.tp_row_linear_bwd_reducescatter(XS, W, DYSH, r["rs_dx"], r["rs_dw"],
+                                           ws_for(tp, tp.TP_OP_ROW_RS_BWD, p, M, N, K, 0))
+        torch.cuda.synchronize()
+        return r
+
+    fused = run()
+    assert tp.tp_debug_set(tp.TP_DEBUG_NO_BWD_FUSION, 1) == tp.TP_OK
+    sep = run()
+    for k in fused:
+        for a, b in zip(fused[k], sep[k]):
+            iv = torch.int32 if a.dtype == torch.float32 else torch.int16
+            assert torch.equal(a.view(iv), b.view(iv)), f"{k}: fused and separate launches differ"
+    refs = {"row_dx": oracle.row_bwd_dx(w, dy), "row_dw": oracle.row_bwd_dw(xs, dy),
+            "col_dx": [oracle.col_bwd_dx(w, dys)], "col_dw": oracle.col_bwd_dw(x, dys),
+            "ag_dx": oracle.ag_matmul_bwd_dx(w, dys), "ag_dw": oracle.ag_matmul_bwd_dw(xsh, dys),
+            "rs_dx": oracle.row_rs_bwd_dx(w, dysh), "rs_dw": oracle.row_rs_bwd_dw(xs, dysh)}
+    for k, ref in refs.items():
+        for a, r in zip(fused[k], ref):
+            assert np.array_equal(host_f64(a), r), f"{k}: not exact"
