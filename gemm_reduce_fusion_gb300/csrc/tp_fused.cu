@@ -37,6 +37,9 @@ constexpr int64_t kPreciseKb = 32;
 // An operand that every group of a launch reads through the same maps is
 // loaded evict_last when it takes at most this much of the 129 MB L2.
 constexpr int64_t kKeepBytes = 64ll << 20;
+// Backward dX and dW share one launch only when neither alone takes more
+// than this many waves of CTA pairs.
+constexpr int64_t kFuseWaves = 6;
 
 // ------------------------------------------------------------------ small helpers
 
@@ -741,10 +744,13 @@ int64_t pair_makespan(int64_t n0, int64_t kb0, int64_t n1, int64_t kb1, int64_t 
 }
 
 // The dX (dY.W^T) and dW (X^T.dY) launches of one backward call: one CTA-pair
-// launch for both when each is a plain pair launch (no split-K) and the
-// combined static assignment finishes no later than the two launches one
-// after the other; otherwise the two launches.  The two GEMMs are
-// independent: neither reads what the other writes.
+// launch for both when each is a short plain pair launch (no split-K, at
+// most kFuseWaves waves) and the combined static assignment finishes no
+// later than the two launches one after the other; otherwise the two
+// launches.  The two GEMMs are independent: neither reads what the other
+// writes.  Short launches gain most (one fill, drain and partial last wave
+// instead of two); on long ones the two problems' operands compete for L2
+// and measured slower, so those stay apart.
 tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype out_dtype, void* ws,
                        cudaStream_t stream, const DevInfo& di) {
   const Shape& a = LX.shape;
@@ -758,7 +764,7 @@ tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype ou
     const int64_t sep = pair_makespan(a.units0, kba, 0, 0, C, a.tail_split) +
                         pair_makespan(b.units0, kbb, 0, 0, C, b.tail_split);
     const int64_t fused = pair_makespan(a.units0, kba, b.units0, kbb, C, 1);
-    if (fused <= sep) {
+    if (fused <= sep && std::max(a.units0, b.units0) <= kFuseWaves * C) {
       // whole tiles only: the fused launch has a single partial last wave
       Shape sa = a, sb = b;
       sa.tail_split = sb.tail_split = 1;
