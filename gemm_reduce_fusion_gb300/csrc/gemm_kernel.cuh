@@ -914,10 +914,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //     accumulator on CTA 0's accumulator-empty barrier;
 //   - both CTAs meet at a cluster barrier before tensor memory is freed.
 
-#ifndef TPF_PAIR_BK
-#define TPF_PAIR_BK 128
-#endif
-constexpr int PAIR_BK = TPF_PAIR_BK;  // k-block depth of the pair kernel: 64 KiB stages, fewer round trips
+constexpr int PAIR_BK = 128;  // k-block depth of the pair kernel: 64 KiB stages, fewer round trips
 
 template <bool A_MN, bool B_MN, int BKP>
 struct PairCfg {

@@ -744,14 +744,13 @@ int64_t pair_makespan(int64_t n0, int64_t kb0, int64_t n1, int64_t kb1, int64_t 
 }
 
 // The dX (dY.W^T) and dW (X^T.dY) launches of one backward call: one CTA-pair
-// launch for both when each is a plain pair launch (no split-K) and the
-// combined static assignment finishes no later than the two launches one
-// after the other -- for short launches (at most kFuseWaves waves each)
-// whenever it is no later, for longer ones only when it saves at least 2 %
-// (their two half-empty last waves); otherwise the two launches.  The two
-// GEMMs are independent: neither reads what the other writes.  On long
-// launches where fusing saves less (a fraction of one wave in 47) the two
-// problems' operands competing for L2 measured slower, so those stay apart.
+// launch for both when each is a short plain pair launch (no split-K, at
+// most kFuseWaves waves) and the combined static assignment finishes no
+// later than the two launches one after the other; otherwise the two
+// launches.  The two GEMMs are independent: neither reads what the other
+// writes.  Short launches gain most (one fill, drain and partial last wave
+// instead of two); on long ones the two problems' operands compete for L2
+// and measured slower, so those stay apart.
 tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype out_dtype, void* ws,
                        cudaStream_t stream, const DevInfo& di) {
   const Shape& a = LX.shape;
@@ -765,8 +764,7 @@ tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype ou
     const int64_t sep = pair_makespan(a.units0, kba, 0, 0, C, a.tail_split) +
                         pair_makespan(b.units0, kbb, 0, 0, C, b.tail_split);
     const int64_t fused = pair_makespan(a.units0, kba, b.units0, kbb, C, 1);
-    const bool short_launches = std::max(a.units0, b.units0) <= kFuseWaves * C;
-    if (fused <= sep && (short_launches || (sep - fused) * 50 >= sep)) {
+    if (fused <= sep && std::max(a.units0, b.units0) <= kFuseWaves * C) {
       // whole tiles only: the fused launch has a single partial last wave
       Shape sa = a, sb = b;
       sa.tail_split = sb.tail_split = 1;
