@@ -110,12 +110,27 @@ tp_status bind_device(int* dev) {
 tp_status device_info(DevInfo* out) {
   int dev = 0;
   if (bind_device(&dev) != TP_OK) return TP_ERR_CUDA;
+  // SM count of each device seen (0: not yet queried; -1: not an sm_103 device)
+  static std::atomic<int> sm_count[64] = {};
+  if (dev >= 0 && dev < 64) {
+    const int c = sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      out->sms = c;
+      out->ok = true;
+      return TP_OK;
+    }
+    if (c < 0) return TP_ERR_ARCH;
+  }
   int major = 0, minor = 0, sms = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return TP_ERR_CUDA;
-  if (major != 10 || minor != 3) return TP_ERR_ARCH;
+  if (major != 10 || minor != 3) {
+    if (dev >= 0 && dev < 64) sm_count[dev].store(-1, std::memory_order_relaxed);
+    return TP_ERR_ARCH;
+  }
+  if (dev >= 0 && dev < 64 && sms > 0) sm_count[dev].store(sms, std::memory_order_relaxed);
   out->sms = sms;
   out->ok = true;
   return TP_OK;
@@ -189,12 +204,25 @@ enum Variant : int {
   V_MM2,       //                           X^T . dY
 };
 
+// cudaFuncSetAttribute(k, MaxDynamicSharedMemorySize, bytes) once per kernel
+// and device (`done` is the kernel's own bitmask of devices already set).
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel k, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 template <bool A_MN, bool B_MN, bool TAIL>
 cudaError_t launch_pair_t(const GemmParams& P, int clusters, cudaStream_t s) {
   using Cfg = PairCfg<A_MN, B_MN, PAIR_BK>;
   auto k = tp_gemm_pair_kernel<A_MN, B_MN, PAIR_BK, TAIL>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Cfg::SMEM_BYTES));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(k, static_cast<int>(Cfg::SMEM_BYTES), smem_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
@@ -241,8 +269,8 @@ cudaError_t launch_pair_t(const GemmParams& P, int clusters, cudaStream_t s) {
 cudaError_t launch_pair2(const PairLaunch2& L2, int clusters, cudaStream_t s) {
   using Cfg = PairCfg<false, false, PAIR_BK>;
   auto k = tp_gemm_pair2_kernel<false, false, true, true, PAIR_BK>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Cfg::SMEM_BYTES));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(k, static_cast<int>(Cfg::SMEM_BYTES), smem_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
@@ -290,8 +318,8 @@ template <bool A_MN, bool B_MN, int BN, bool OUT_T, int STAGES>
 cudaError_t launch_t(const GemmParams& P, int grid, cudaStream_t s) {
   using Cfg = GemmCfg<A_MN, B_MN, BN, OUT_T, STAGES>;
   auto k = tp_gemm_kernel<A_MN, B_MN, BN, OUT_T, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Cfg::SMEM_BYTES));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(k, static_cast<int>(Cfg::SMEM_BYTES), smem_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
