@@ -516,10 +516,13 @@ __device__ __forceinline__ void drain_half_from_parts(const GemmParams& P, int32
 
 // Counts this warp's slice of a (tile, warp) region as finished; true for
 // the warp whose slice is the last of n.  A counter holds (launch epoch <<
-// 16 | slices finished); one left by another launch counts as zero, so no
-// clearing is needed between launches.  Each compare-and-swap that fails
-// means another of the region's n warps succeeded, so at most n attempts
-// are needed; past that bound the status word latches an error.
+// 16 | slices finished); one left by another launch counts as zero, so a
+// launch stopped part-way (a device timeout) leaves nothing the next launch
+// could miscount.  The last warp also sets the counter back to zero, so
+// that a launch replayed with the same number (a CUDA graph) starts from
+// zero too.  Each compare-and-swap that fails means another of the region's
+// n warps succeeded, so at most n attempts are needed; past that bound the
+// status word latches an error.
 __device__ __forceinline__ bool finish_slice(const GemmParams& P, unsigned long long* cnt, int n) {
   __threadfence();
   __syncwarp();
@@ -536,6 +539,7 @@ __device__ __forceinline__ bool finish_slice(const GemmParams& P, unsigned long 
     }
     if (!done) atomicOr(P.status, ST_TIMEOUT | (5u << 4));
     last = done && (next & 0xFFFFull) == static_cast<unsigned long long>(n);
+    if (last) atomicExch(cnt, 0ull);  // every slice of the region has arrived: no other writer is left
   }
   last = __shfl_sync(0xFFFFFFFFu, last, 0);
   if (last) __threadfence();

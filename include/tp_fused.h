@@ -52,6 +52,11 @@
  *    kernel has completed, so stream order is kept as for plain launches.
  *  - Any host thread may call; a call runs on that thread's current CUDA
  *    device (the library makes the device's primary context current).
+ *  - Calls may be captured into a CUDA graph once the same call has run
+ *    eagerly on the device (that first call sets each kernel's attributes).
+ *    A replay re-enqueues the captured launches with the captured pointers
+ *    and shapes and reads the buffers' current contents; the workspace must
+ *    not be shared with work that runs concurrently with the replay.
  *  - Biases (forward) and bias gradients (backward) are optional bf16 /
  *    out_dtype vectors over the output columns; NULL leaves them out.
  *  - Errors: argument checks run on the host before anything is enqueued

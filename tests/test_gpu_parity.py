@@ -1132,3 +1132,66 @@ def test_backward_fused_launch_bitwise_and_exact(tp, tile_mode, no_fusion, p, M,
     for k, ref in refs.items():
         for a, r in zip(fused[k], ref):
             assert np.array_equal(host_f64(a), r), f"{k}: not exact"
+
+
+def test_cuda_graph_capture_replays_bitwise(tp):
+    """Calls can be captured in a CUDA graph (after one eager call, which sets
+    each kernel's attributes) and replayed: each replay reads the inputs'
+    current contents, and gives the eager call's bits.  Covers the split-K
+    second stage (the worked example), ReduceScatter, the CTA-pair kernel with
+    last-wave slices, GeLU and the TMA-store epilogue."""
+    import torch
+    p, M, N, K = 2, 128, 2048, 1024
+    p2, M2, N2, K2 = 2, 2048, 2560, 512
+    x = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    w = [torch.empty((K, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    x2 = [torch.empty((M2, K2), dtype=torch.bfloat16, device="cuda") for _ in range(p2)]
+    w2 = [torch.empty((K2, N2), dtype=torch.bfloat16, device="cuda") for _ in range(p2)]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ys = [torch.empty((M // p, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    z = [torch.empty((M2, N2), dtype=torch.bfloat16, device="cuda") for _ in range(p2)]
+    h = [torch.empty((M2, N2), dtype=torch.bfloat16, device="cuda") for _ in range(p2)]
+    y2 = torch.empty((M2, N2), dtype=torch.float32, device="cuda")
+    ws = max((ws_for(tp, op, pp, mm, nn, kk, c) for op, pp, mm, nn, kk, c in
+              [(tp.TP_OP_ROW_AR, p, M, N, K, 32), (tp.TP_OP_ROW_RS, p, M, N, K, 32),
+               (tp.TP_OP_COL_FWD, p2, M2, N2, K2, 0), (tp.TP_OP_ROW_AR, p2, M2, N2, K2, 0)]), key=lambda t: t.numel())
+
+    def fill(seed):
+        for i, t in enumerate(x + w):
+            t.copy_(dev(synth.normal_bf16(tuple(t.shape), seed + i, 0.05)))
+        for i, t in enumerate(x2 + w2):
+            t.copy_(dev(ints(tuple(t.shape), seed + 50 + i)))
+
+    def calls():
+        tp.tp_row_linear_fwd_allreduce(x, w, [y], ws, 32)
+        tp.tp_row_linear_fwd_reducescatter(x, w, ys, ws, 32)
+        tp.tp_col_linear_fwd(x2[0], w2, z, ws, epi=tp.TP_EPI_GELU, preact=h)
+        tp.tp_row_linear_fwd_allreduce(x2, w2, [y2], ws)
+
+    def outputs():
+        return [t.clone() for t in [y, *ys, *z, *h, y2]]
+
+    fill(700)
+    calls()                      # eager: kernel attributes set, caches filled
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            calls()
+    torch.cuda.current_stream().wait_stream(s)
+    for seed in (710, 720):
+        fill(seed)
+        calls()
+        torch.cuda.synchronize()
+        want = outputs()
+        for t in [y, *ys, *z, *h, y2]:
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(outputs(), want):
+            iv = torch.int32 if a.dtype == torch.float32 else torch.int16
+            assert torch.equal(a.view(iv), b.view(iv)), "graph replay differs from the eager calls"
+    assert tp.tp_get_device_status(ws) == tp.TP_OK
+    assert np.array_equal(host_f64(y2), oracle.row_fwd_allreduce([host_bits(t) for t in x2], [host_bits(t) for t in w2]))
