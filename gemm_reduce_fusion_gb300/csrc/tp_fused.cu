@@ -889,8 +889,11 @@ void prepare_gemm(Launch& L, tp_dtype out_dtype, void* ws) {
   if (g_l2_hints.load() != 0) {
     const int64_t a_maps = (P.a_idx_gm ? s.Gm : 1) * (P.a_idx_gn ? s.Gn : 1) * (P.a_idx_s ? s.S : 1);
     const int64_t b_maps = (P.b_idx_gm ? s.Gm : 1) * (P.b_idx_gn ? s.Gn : 1) * (P.b_idx_s ? s.S : 1);
-    const bool a_shared = (P.a_idx_gm == 0 && s.Gm > 1) || (P.a_idx_gn == 0 && s.Gn > 1);
-    const bool b_shared = (P.b_idx_gm == 0 && s.Gm > 1) || (P.b_idx_gn == 0 && s.Gn > 1);
+    // groups along M that offset their rows within the same A maps (the
+    // ReduceScatter layouts) read different data, as do groups along N that
+    // offset their columns within the same B maps
+    const bool a_shared = (P.a_idx_gm == 0 && P.a_row_gm == 0 && s.Gm > 1) || (P.a_idx_gn == 0 && s.Gn > 1);
+    const bool b_shared = (P.b_idx_gm == 0 && s.Gm > 1) || (P.b_idx_gn == 0 && P.b_col_gn == 0 && s.Gn > 1);
     P.a_hint = a_shared && a_maps * s.rows_g * s.kseg * 2 <= kKeepBytes ? 1 : 0;
     P.b_hint = b_shared && b_maps * s.cols_g * s.kseg * 2 <= kKeepBytes ? 1 : 0;
     P.out_hint = 2;
