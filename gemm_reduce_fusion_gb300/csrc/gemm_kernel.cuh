@@ -117,14 +117,6 @@ struct GemmParams {
   CUtensorMap tmH[MAX_MAPS];
   int32_t omap[MAX_GROUPS], orow[MAX_GROUPS];
   int32_t hmap[MAX_GROUPS], hrow[MAX_GROUPS];
-  // CTA-pair launches: this launch runs units [unit_base, num_units).  A
-  // launch of the last partial wave's k-slices alone (indep_start = 1) reads
-  // nothing the launch before it writes -- that launch holds the same call's
-  // whole tiles -- so it does not wait for it before starting; it waits for
-  // it before exiting, so that its own completion still implies the earlier
-  // launch's.
-  int32_t unit_base;
-  int32_t indep_start;
 };
 
 struct Unit {
@@ -985,7 +977,7 @@ __device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, i
   const int lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
   const bool leader = crank == 0;
-  const int32_t first = P.unit_base + static_cast<int32_t>(blockIdx.x >> 1);
+  const int32_t first = static_cast<int32_t>(blockIdx.x >> 1);
   const int32_t stride = static_cast<int32_t>(gridDim.x >> 1);
   // problem of unit t, and t's index within it
   auto prob_of = [&](int32_t t) -> int { return (NPROB == 2 && t >= split) ? 1 : 0; };
@@ -1014,7 +1006,7 @@ __device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, i
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // set-up above touches no global memory: it overlaps the previous kernel
-  if (!P.indep_start) griddep_wait();
+  griddep_wait();
   griddep_launch_dependents();
 
   if (warp == 0) {
@@ -1217,7 +1209,6 @@ __device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, i
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
   }
-  if (P.indep_start) griddep_wait();  // this launch completes after the one before it
 }
 
 // TAIL: the launch runs its last partial wave as k-slices (P.tail_split >

@@ -60,7 +60,6 @@ std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (sli
 std::atomic<int64_t> g_l2_hints{1};         // 1: L2 cache policies on operand loads and output stores
 std::atomic<int64_t> g_tma_store{1};        // 1: staged epilogues leave shared memory by TMA store
 std::atomic<int64_t> g_debug_no_fuse{0};    // 1: backward dX and dW always as two launches
-std::atomic<int64_t> g_tail_launch{1};      // 1: last-wave k-slices as a launch of their own
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -860,24 +859,6 @@ tp_status run_launch_phases(Launch& L, tp_dtype out_dtype, void* ws, cudaStream_
     return TP_OK;
   }
   prepare_gemm(L, out_dtype, ws);
-  if ((phases & 1) && s.pair && s.tail_split > 1 && g_tail_launch.load() != 0) {
-    // The whole tiles on the plain instantiation, then the last partial
-    // wave's k-slices as a launch of their own that starts on the clusters
-    // the first one frees without waiting for it (it reads none of its
-    // outputs), so the slice code costs the whole tiles nothing.
-    static thread_local GemmParams Pw, Pt;
-    Pw = P;
-    Pw.num_units = static_cast<int32_t>(s.tail_start);
-    Pw.tail_split = 1;
-    Pt = P;
-    Pt.unit_base = static_cast<int32_t>(s.tail_start);
-    Pt.indep_start = 1;
-    const int gw = static_cast<int>(std::min<int64_t>(Pw.num_units, di.sms / 2));
-    const int gt = static_cast<int>(std::min<int64_t>(P.num_units - s.tail_start, di.sms / 2));
-    if (launch_variant(L.variant, Pw, gw, stream) != cudaSuccess) return TP_ERR_CUDA;
-    if (launch_variant(L.variant, Pt, gt, stream) != cudaSuccess) return TP_ERR_CUDA;
-    return TP_OK;
-  }
   const int grid = s.pair ? static_cast<int>(std::min<int64_t>(P.num_units, di.sms / 2))
                          : static_cast<int>(std::min<int64_t>(P.num_units, di.sms));
   if ((phases & 1) && launch_variant(L.variant, P, grid, stream) != cudaSuccess) return TP_ERR_CUDA;
@@ -1052,10 +1033,6 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_NO_BWD_FUSION:
       if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
       g_debug_no_fuse.store(value);
-      return TP_OK;
-    case TP_DEBUG_ONE_LAUNCH_TAIL:
-      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
-      g_tail_launch.store(value ? 0 : 1);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;

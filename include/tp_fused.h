@@ -363,9 +363,6 @@ tp_status tp_noalloc_device_status(cudaStream_t stream);
  *   TP_DEBUG_NO_BWD_FUSION: 0 (default) lets a backward call run its dX and
  *     dW products as one CTA-pair launch where that is planned to finish
  *     sooner; 1 always runs them as two launches (bit-identical results).
- *   TP_DEBUG_ONE_LAUNCH_TAIL: 0 (default) runs a CTA-pair launch whose last
- *     partial wave is cut into k-slices as two launches, the whole tiles and
- *     then the slices; 1 runs both in one launch (bit-identical results).
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
 typedef enum {
   TP_DEBUG_TIMEOUT_MS = 0,
@@ -375,8 +372,7 @@ typedef enum {
   TP_DEBUG_SPLIT_K = 4,
   TP_DEBUG_L2_HINTS = 5,
   TP_DEBUG_TMA_STORE = 6,
-  TP_DEBUG_NO_BWD_FUSION = 7,
-  TP_DEBUG_ONE_LAUNCH_TAIL = 8
+  TP_DEBUG_NO_BWD_FUSION = 7
 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 
