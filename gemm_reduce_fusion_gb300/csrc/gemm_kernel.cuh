@@ -225,15 +225,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 // 7.1.26: for z >= 0, erfc(z) = (a1 t + a2 t^2 + ... + a5 t^5) exp(-z^2) with
 // t = 1 / (1 + p z) and an absolute error of at most 1.5e-7.  With
 // z = |h| / sqrt(2) the tail is erfc(z) / 2, and exp(-z^2) is e, which the
-// GeLU derivative's density term reuses.
+// GeLU derivative's density term reuses.  The halves of a1..a5 (exact in
+// fp32) fold the division by 2 into the polynomial.
+constexpr float kTailP = 0.3275911f * 0.70710678118654752f;  // p / sqrt(2): t from |h| directly
+constexpr float kTailA1 = 0.5f * 0.254829592f, kTailA2 = 0.5f * -0.284496736f, kTailA3 = 0.5f * 1.421413741f,
+                kTailA4 = 0.5f * -1.453152027f, kTailA5 = 0.5f * 1.061405429f;
+constexpr float kTailE = -0.72134752044448170f;  // exp(-h^2/2) = 2^(-h^2 log2(e) / 2)
+constexpr float kPdf = 0.39894228040143268f;     // 1 / sqrt(2 pi)
+
 __device__ __forceinline__ float normal_tail(float h, float& e) {
-  constexpr float p = 0.3275911f * 0.70710678118654752f;  // p / sqrt(2): t from |h| directly
-  constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
-                  a5 = 1.061405429f;
-  const float t = rcp_approx(fmaf(p, fabsf(h), 1.0f));
-  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
-  e = ex2_approx(h * h * -0.72134752044448170f);  // exp(-h^2/2) = 2^(-h^2 log2(e) / 2)
-  return 0.5f * poly * e;
+  const float t = rcp_approx(fmaf(kTailP, fabsf(h), 1.0f));
+  const float q = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kTailA5, kTailA4), kTailA3), kTailA2), kTailA1);
+  e = ex2_approx(h * h * kTailE);
+  return q * e;
 }
 
 // GeLU(h) = h Phi(h) ([TP] §7.1, exact erf form; Phi from the tail above,
@@ -241,14 +245,56 @@ __device__ __forceinline__ float normal_tail(float h, float& e) {
 __device__ __forceinline__ float gelu_f(float h) {
   float e;
   const float c = normal_tail(h, e);
-  return h * (h >= 0.0f ? 1.0f - c : c);
+  return h * (h >= 0.0f ? fmaf(c, -1.0f, 1.0f) : c);
 }
 
 // GeLU'(h) = Phi(h) + h phi(h), phi(h) = e / sqrt(2 pi).
 __device__ __forceinline__ float gelu_prime_f(float h) {
   float e;
   const float c = normal_tail(h, e);
-  return fmaf(h * e, 0.39894228040143268f, h >= 0.0f ? 1.0f - c : c);
+  return fmaf(h * e, kPdf, h >= 0.0f ? fmaf(c, -1.0f, 1.0f) : c);
+}
+
+// The same for two values at once, in packed fp32 arithmetic: every lane
+// performs exactly the operations of the scalar functions above, so the
+// results are bit for bit those of gelu_f / gelu_prime_f.
+__device__ __forceinline__ void normal_tail2(float h0, float h1, uint64_t& hv, uint64_t& c, uint64_t& e) {
+  hv = pk2(h0, h1);
+  uint64_t d = fma2(pk2(kTailP, kTailP), pk2(fabsf(h0), fabsf(h1)), pk2(1.0f, 1.0f));
+  float d0, d1;
+  upk2(d, d0, d1);
+  const uint64_t t = pk2(rcp_approx(d0), rcp_approx(d1));
+  uint64_t q = fma2(t, pk2(kTailA5, kTailA5), pk2(kTailA4, kTailA4));
+  q = fma2(t, q, pk2(kTailA3, kTailA3));
+  q = fma2(t, q, pk2(kTailA2, kTailA2));
+  q = fma2(t, q, pk2(kTailA1, kTailA1));
+  q = mul2(t, q);
+  float g0, g1;
+  upk2(mul2(mul2(hv, hv), pk2(kTailE, kTailE)), g0, g1);
+  e = pk2(ex2_approx(g0), ex2_approx(g1));
+  c = mul2(q, e);
+}
+
+// Phi of the two values from their tails c (packed): 1 - c where h >= 0.
+__device__ __forceinline__ uint64_t phi2(float h0, float h1, uint64_t c) {
+  float c0, c1, o0, o1;
+  upk2(c, c0, c1);
+  upk2(fma2(c, pk2(-1.0f, -1.0f), pk2(1.0f, 1.0f)), o0, o1);
+  return pk2(h0 >= 0.0f ? o0 : c0, h1 >= 0.0f ? o1 : c1);
+}
+
+__device__ __forceinline__ void gelu2(float& x0, float& x1) {
+  uint64_t hv, c, e;
+  normal_tail2(x0, x1, hv, c, e);
+  upk2(mul2(hv, phi2(x0, x1, c)), x0, x1);
+}
+
+// v0, v1 times GeLU'(h0), GeLU'(h1)
+__device__ __forceinline__ void times_gelu_prime2(float& v0, float& v1, float h0, float h1) {
+  uint64_t hv, c, e;
+  normal_tail2(h0, h1, hv, c, e);
+  const uint64_t gp = fma2(mul2(hv, e), pk2(kPdf, kPdf), phi2(h0, h1, c));
+  upk2(mul2(pk2(v0, v1), gp), v0, v1);
 }
 
 __device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
@@ -428,7 +474,7 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
       }
     }
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = gelu_f(v[i]);
+    for (int i = 0; i < NV; i += 2) gelu2(v[i], v[i + 1]);
   } else if (P.epi == EPI_DGELU) {
     // H is bf16: NV * 2 bytes per row
     constexpr int UH = NV * 2 / 16;
@@ -441,10 +487,9 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
       const uint4 h = *reinterpret_cast<const uint4*>(stg + stg_off(lane, u));
       const uint32_t w[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * u + 2 * k] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[k] & 0xFFFFu)));
-        v[8 * u + 2 * k + 1] *= gelu_prime_f(bf16_bits_to_f(static_cast<uint16_t>(w[k] >> 16)));
-      }
+      for (int k = 0; k < 4; ++k)
+        times_gelu_prime2(v[8 * u + 2 * k], v[8 * u + 2 * k + 1], bf16_bits_to_f(static_cast<uint16_t>(w[k] & 0xFFFFu)),
+                          bf16_bits_to_f(static_cast<uint16_t>(w[k] >> 16)));
     }
     __syncwarp();
   }
