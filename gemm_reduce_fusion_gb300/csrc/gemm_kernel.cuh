@@ -3,10 +3,11 @@
 // One launch covers a whole sharded-Linear call.  Its tile space is
 //   groups along M (Gm) x groups along N (Gn) x m-tiles x n-tiles x splits,
 // and its K loop walks S "segments" -- one per rank whose partial product is
-// being reduced -- in rank order, each segment being K/64 k-blocks.  All
-// segments of a tile accumulate into the same fp32 tensor-memory
-// accumulator, so the cross-rank reduction happens in TMEM and the reduced
-// tile is written once.
+// being reduced -- in rank order, each segment being K/64 k-blocks (the
+// pair kernel's whole tiles on a deep contraction walk every other wave in
+// reverse order; see GemmParams::k_alternate).  All segments of a tile
+// accumulate into the same fp32 tensor-memory accumulator, so the
+// cross-rank reduction happens in TMEM and the reduced tile is written once.
 //
 // Roles (320 threads):
 //   warp 0     one thread issues TMA loads of A and B k-blocks into a
@@ -105,9 +106,14 @@ struct GemmParams {
   // this launch's number (never 0): slice counters left by an earlier launch,
   // finished or stopped, read as zero
   unsigned long long epoch;
-  // L2 policies (see l2_policy): of the A and B operand loads (3-D maps) and
-  // of the final output stores
+  // L2 policies (see l2_policy): of the A and B operand loads (3-D maps), and
+  // of the final output stores and the GeLU' epilogue's loads of H
   int32_t a_hint, b_hint, out_hint;
+  // CTA-pair kernel: whole tiles of odd waves (a cluster's 2nd, 4th, ...
+  // unit of this problem) walk their k-blocks from last to first, so a wave
+  // starts on the operand slices the previous wave read last, which are
+  // still in L2 where the two waves share panels.
+  int32_t k_alternate;
   // Staged epilogue by TMA store (out_tma = 1): group g (replica r) writes
   // its 32-row x 128-byte chunks through tmO[omap[g] + r] at row orow[g] + i,
   // and its GeLU pre-activation through tmH[hmap[g]] at row hrow[g] + i.
@@ -360,15 +366,14 @@ __device__ __forceinline__ void stage_store(const uint8_t* stg, uint8_t* dst, in
 // valid range are left unwritten
 template <int U>
 __device__ __forceinline__ void stage_load(uint8_t* stg, const uint8_t* src, int64_t ld_bytes,
-                                           int rows_valid, int units_valid, int lane) {
+                                           int rows_valid, int units_valid, int lane, uint64_t policy) {
   constexpr int RPI = 32 / U;
 #pragma unroll
   for (int k = 0; k < U; ++k) {
     const int r = k * RPI + lane / U;
     const int u = lane % U;
     if (r < rows_valid && u < units_valid)
-      *reinterpret_cast<uint4*>(stg + stg_off(r, u)) =
-          *reinterpret_cast<const uint4*>(src + r * ld_bytes + u * 16);
+      *reinterpret_cast<uint4*>(stg + stg_off(r, u)) = ld_global_v4_hint(src + r * ld_bytes + u * 16, policy);
   }
 }
 
@@ -427,11 +432,11 @@ __device__ __forceinline__ void stage_free(const GemmParams& P, int lane) {
 // The staged chunk (rows gi0.., columns gj0.. of the group) -> global through
 // one bulk tensor store issued by lane 0.
 __device__ __forceinline__ void stage_store_tma(const CUtensorMap* m, const uint8_t* stg, int32_t x, int32_t y,
-                                                bool valid, int lane) {
+                                                bool valid, int lane, uint64_t policy) {
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0 && valid) {
-    tma_store_2d(m, smem_u32(stg), x, y);
+    tma_store_2d(m, smem_u32(stg), x, y, policy);
     bulk_commit();
   }
 }
@@ -465,7 +470,7 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
       stage_free(P, lane);
       stage_row<F32>(stg, lane, v);
       if (P.out_tma) {
-        stage_store_tma(&P.tmH[P.hmap[g]], stg, gj0, P.hrow[g] + gi0, any, lane);
+        stage_store_tma(&P.tmH[P.hmap[g]], stg, gj0, P.hrow[g] + gi0, any, lane, l2_policy(P.out_hint));
       } else {
         __syncwarp();
         uint8_t* dst = static_cast<uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * ESZ;
@@ -480,7 +485,7 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
     constexpr int UH = NV * 2 / 16;
     const uint8_t* src = static_cast<const uint8_t*>(P.aux[g]) + (static_cast<int64_t>(gi0) * P.ld_aux + gj0) * 2;
     stage_free(P, lane);
-    stage_load<UH>(stg, src, P.ld_aux * 2, rows_valid, cols_valid * 2 / 16, lane);
+    stage_load<UH>(stg, src, P.ld_aux * 2, rows_valid, cols_valid * 2 / 16, lane, l2_policy(P.out_hint));
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < UH; ++u) {
@@ -499,7 +504,9 @@ __device__ __forceinline__ void finish_chunk_staged(const GemmParams& P, int32_t
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && any) {
-      for (int rep = 0; rep < P.n_rep; ++rep) tma_store_2d(&P.tmO[P.omap[g] + rep], smem_u32(stg), gj0, P.orow[g] + gi0);
+      const uint64_t pol = l2_policy(P.out_hint);
+      for (int rep = 0; rep < P.n_rep; ++rep)
+        tma_store_2d(&P.tmO[P.omap[g] + rep], smem_u32(stg), gj0, P.orow[g] + gi0, pol);
       bulk_commit();
     }
     return;
@@ -1027,6 +1034,10 @@ __device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, i
   // problem of unit t, and t's index within it
   auto prob_of = [&](int32_t t) -> int { return (NPROB == 2 && t >= split) ? 1 : 0; };
   auto local = [&](int32_t t, int pi) -> int32_t { return pi ? t - split : t; };
+  // whole tiles of a cluster's odd units (within their problem) reverse K
+  auto k_reversed = [&](const GemmParams& Q, int32_t t, int pi, int32_t tj) -> bool {
+    return Q.k_alternate != 0 && tj < 0 && ((local(t, pi) / stride) & 1) != 0;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1077,7 +1088,9 @@ __device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, i
         const Unit u = TAIL ? decode_pair_unit(Q, t, tj, tk) : decode_unit(Q, local(t, pi));
         const int32_t arow = Q.a_row_gm * u.gm + u.mt * (2 * BM) + static_cast<int32_t>(crank) * BM;
         const int32_t bcol = Q.b_col_gn * u.gn + u.nt * Cfg::BN + static_cast<int32_t>(crank) * Cfg::BNH;
-        for (int32_t q = u.q0; q < u.q1; ++q) {
+        const bool rev = k_reversed(Q, t, pi, tj);
+        for (int32_t i = u.q0; i < u.q1; ++i) {
+          const int32_t q = rev ? u.q0 + u.q1 - 1 - i : i;
           const int32_t s = q / Q.kb_per_seg;
           const int32_t kc = (q % Q.kb_per_seg) * BKP;
           const int32_t kca = kc + s * Q.a_koff_s;
@@ -1160,6 +1173,8 @@ __device__ __forceinline__ void pair_body(const GemmParams* Ps, int32_t split, i
         tc_fence_after();
         trace_mma_start(P, t, u.ch, blockIdx.x >> 1);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
+        // the k-blocks arrive in the producer's order (forward or reversed);
+        // only the first one of the unit overwrites the accumulator
         for (int32_t q = u.q0; q < u.q1; ++q) {
           if (!wait_bar(full_bar(stage), phase, P, abort_flag, 3u)) {
             ok = false;

@@ -119,6 +119,15 @@ __device__ __forceinline__ uint64_t l2_policy(int kind) {
   return p;
 }
 
+// 16-byte global load with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_global_v4_hint(const void* ptr, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(policy));
+  return v;
+}
+
 // 16-byte global store with an L2 cache policy.
 __device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
@@ -141,11 +150,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
 
 // 2-D tiled store shared -> global (bulk async group).  Coordinates as for
 // loads; parts of the box outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(x), "r"(y), "r"(src), "l"(policy)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the source shared memory of every committed bulk store of this

@@ -40,6 +40,17 @@ constexpr int64_t kKeepBytes = 64ll << 20;
 // Backward dX and dW share one launch only when neither alone takes more
 // than this many waves of CTA pairs.
 constexpr int64_t kFuseWaves = 6;
+// Pair launches whose contraction is at least this deep alternate its
+// direction wave by wave (GemmParams::k_alternate).  From about 8192 on, the
+// ~18 operand panels (256 rows x K) that a wave of 76 tiles reads outgrow
+// the L2, so a forward-only wave finds none of the previous wave's panels
+// left; running every other wave backwards re-reads the slices that wave
+// touched last.  Measured: DRAM reads of the K = 16384 launches of the MLP
+// step -8 %, of the sequence-parallel pair (K = 8192, 28672) -16 % and -5 %.
+// On shallower contractions the panels a wave shares with the previous one
+// stay in L2 either way, and a reversed wave no longer streams in step with
+// the previous wave's stragglers (reads +2 to +5 %).
+constexpr int64_t kKAlternateDepth = 8192;
 
 // ------------------------------------------------------------------ small helpers
 
@@ -884,7 +895,8 @@ void prepare_gemm(Launch& L, tp_dtype out_dtype, void* ws) {
   // L2 policies: an operand shared by every group (one set of maps for all
   // of them, re-read by every group's tiles) is kept while the other
   // streams past it, if it fits in half the L2; final outputs, which nothing
-  // in the launch reads back, are written evict_first.
+  // in the launch reads back, are written evict_first (plain and TMA
+  // stores), and the GeLU' epilogue reads the saved H, used once, the same way.
   P.a_hint = P.b_hint = P.out_hint = 0;
   if (g_l2_hints.load() != 0) {
     const int64_t a_maps = (P.a_idx_gm ? s.Gm : 1) * (P.a_idx_gn ? s.Gn : 1) * (P.a_idx_s ? s.S : 1);
@@ -898,6 +910,7 @@ void prepare_gemm(Launch& L, tp_dtype out_dtype, void* ws) {
     P.b_hint = b_shared && b_maps * s.cols_g * s.kseg * 2 <= kKeepBytes ? 1 : 0;
     P.out_hint = 2;
   }
+  P.k_alternate = s.pair && s.S * s.kseg >= kKAlternateDepth ? 1 : 0;
   // staged epilogues (non-swapped tiles, no split-K partials) store through TMA
   P.out_tma = 0;
   if (g_tma_store.load() != 0 && !s.swap && s.n_split == 1) {

@@ -5,7 +5,12 @@
  * r's shards are plain device pointers.  Each entry point runs the per-rank
  * partial GEMMs fused with their cross-shard reduction (or gather): the p
  * partials of an output tile are accumulated in one fp32 tensor-memory
- * accumulator in rank order r = 0..p-1 and the tile is written once.  Rows
+ * accumulator in rank order r = 0..p-1 and the tile is written once.  (On
+ * contractions of 8192 and deeper, the CTA-pair kernel runs the tiles of
+ * every other wave in the reverse order, p-1..0 and last k-block first, so
+ * that a wave re-reads from L2 what the previous one read last; the order
+ * of each tile is fixed by the shapes and the GPU's SM count, so results
+ * are reproducible.)  Rows
  * are processed chunk by chunk along M (chunk-major tile order), and a
  * tile's write-out overlaps the next tile's MMAs.
  *
@@ -120,7 +125,7 @@ size_t tp_workspace_size(tp_op op, int p, int64_t M, int64_t N, int64_t K, int64
                          tp_dtype out_dtype);
 
 /* Row-parallel forward, MatMul+AllReduce layout.  [M027 §01; TP §2.4, §四]
- *   Y = sum_{r=0}^{p-1} X_r . W_r (+ b), accumulated in rank order, written once.
+ *   Y = sum_{r=0}^{p-1} X_r . W_r (+ b), accumulated in one accumulator, written once.
  *   x[r]: X_r [M, K] (rank r's column block of the layer input)
  *   w[r]: W_r [K, N] (rank r's row block of the weight)
  *   bias: b [N] bf16 or NULL, added once after the reduction (in fp32,
@@ -158,7 +163,7 @@ tp_status tp_col_linear_fwd(const void* x, const void* const* w, const void* con
 
 /* Column-parallel backward.  [TP §三, §六]
  *   dX = sum_{k=0}^{p-1} dY_k . A_k^T  (the backward AllReduce, fused,
- *        accumulated in rank order, written once) -> dx [M, K] if dx != NULL
+ *        accumulated in one accumulator, written once) -> dx [M, K] if dx != NULL
  *   dA_k = X^T . dY_k (local)                     -> dw[k] [K, N] if dw != NULL
  *   db_k = sum over the M rows of dY_k (the gradient of b_k; summed in a
  *          fixed order, so deterministic)         -> db[k] [N] if db != NULL
