@@ -6,8 +6,9 @@ block, forward and backward, with p = 4 shards held in one GPU's memory,
 4096 tokens, h = 4096, ffn = 16384 -- FC1 column-parallel [4096, 4096] per
 shard with GeLU, FC2 row-parallel [4096, 4096] per shard with the fused
 AllReduce, then FC2's backward (dZ_k = dY W2_k^T * GeLU'(H_k), dW2_k) and
-FC1's backward (the fused dX = sum_k dZ_k W1_k^T, dW1_k).  Six GEMM launches,
-3.30 TFLOP per step.  Inputs: X N(0,1), dY N(0,1), weights N(0, 0.02), bf16,
+FC1's backward (the fused dX = sum_k dZ_k W1_k^T, dW1_k).  Six GEMMs, 3.30
+TFLOP per step, in five ABI calls and five launches: FC2's backward is one
+call whose two products share one launch.  Inputs: X N(0,1), dY N(0,1), weights N(0, 0.02), bf16,
 drawn by the seeded generator.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -207,7 +208,7 @@ class ClockSampler:
 # ------------------------------------------------------------------ the step
 
 class MLPStep:
-    """Device buffers and the six ABI calls of one MLP fwd+bwd step."""
+    """Device buffers and the five ABI calls of one MLP fwd+bwd step."""
 
     def __init__(self, tp, torch, host):
         bf = dict(dtype=torch.bfloat16, device="cuda")
@@ -258,22 +259,23 @@ class MLPStep:
             ("col_fwd_gelu", lambda: tp.tp_col_linear_fwd(self.X, self.W1, self.Z, ws, epi=tp.TP_EPI_GELU,
                                                           preact=self.Hp)),
             ("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(self.Z, self.W2, [self.Y], ws)),
-            ("row_bwd_dx_dgelu", lambda: tp.tp_row_linear_bwd(None, self.W2, self.DY, self.DZ, None, ws,
-                                                              preact=self.Hp)),
-            ("row_bwd_dw", lambda: tp.tp_row_linear_bwd(self.Z, self.W2, self.DY, None, self.DW2, ws)),
+            ("row_bwd", lambda: tp.tp_row_linear_bwd(self.Z, self.W2, self.DY, self.DZ, self.DW2, ws,
+                                                     preact=self.Hp)),
             ("col_bwd_dx", lambda: tp.tp_col_linear_bwd(None, self.W1, self.DZ, self.DX, None, ws)),
             ("col_bwd_dw", lambda: tp.tp_col_linear_bwd(self.X, self.W1, self.DZ, None, self.DW1, ws)),
         ]
 
 
 # which kernel variant each call launches (one launch per call at these
-# sizes; a backward call asked for dX and dW together also runs them as two
-# launches at these sizes) and the GEMMs it computes
+# sizes) and the GEMMs it computes.  The row backward is one call for dZ and
+# dW2, which the library runs as one launch of both products (2 x 13.5 waves
+# as 27); the column backward's two products would run as two launches even
+# from one call (its fused makespan is longer), so the step issues them as two
+# calls and each is timed on its own.
 CALL_KERNEL = {
     "col_fwd_gelu": ("tp_gemm_pair_kernel<0,1,128,0> (X.W, 256x256 tiles on CTA pairs)", 1),
     "row_fwd_allreduce": ("tp_gemm_pair_kernel<0,1,128,1> (X.W, 256x256 tiles on CTA pairs, last wave in k-slices)", 1),
-    "row_bwd_dx_dgelu": ("tp_gemm_pair_kernel<0,0,128,0> (dY.W^T, 256x256 tiles on CTA pairs)", 1),
-    "row_bwd_dw": ("tp_gemm_pair_kernel<1,1,128,0> (X^T.dY, 256x256 tiles on CTA pairs)", 1),
+    "row_bwd": ("tp_gemm_pair2_kernel<0,0,1,1,128> (dY.W^T with GeLU' then X^T.dY, one launch on CTA pairs)", 2),
     "col_bwd_dx": ("tp_gemm_pair_kernel<0,0,128,1> (dY.W^T, 256x256 tiles on CTA pairs, last wave in k-slices)", 1),
     "col_bwd_dw": ("tp_gemm_pair_kernel<1,1,128,0> (X^T.dY, 256x256 tiles on CTA pairs)", 1),
 }
@@ -717,9 +719,9 @@ def profile_case():
     """Each kernel variant of the step at the step's shapes (about 1 GB
     resident), a bounded case for ncu captures.  Launch order:
     [col fwd + GeLU (X.W), row fwd AllReduce (X.W, last wave in k-slices),
-    row bwd dX with GeLU' (dY.W^T), col bwd fused dX (dY.W^T, last wave in
-    k-slices)] x 2,
-    then row bwd dW (X^T.dY) x 2."""
+    row bwd dZ with GeLU' and dW2 in one launch (dY.W^T then X^T.dY), col bwd
+    fused dX (dY.W^T, last wave in k-slices)] x 2,
+    then col bwd dW1 (X^T.dZ) x 2."""
     import torch
     import gemm_reduce_fusion_gb300 as tp
     import synth
@@ -739,14 +741,15 @@ def profile_case():
     ws = _ws_for(torch, tp, [(tp.TP_OP_COL_FWD, P, M, NK, H, 0), (tp.TP_OP_ROW_AR, P, M, H, NK, 0),
                              (tp.TP_OP_ROW_BWD, P, M, H, NK, 0), (tp.TP_OP_COL_BWD, P, M, NK, H, 0)])
     dx = torch.empty((M, H), **bf)
+    wgrad2 = [torch.empty((NK, H), **bf) for _ in range(P)]
     for _ in range(2):
         tp.tp_col_linear_fwd(y, w1, z, ws, epi=tp.TP_EPI_GELU, preact=hh)   # X.W + GeLU
         tp.tp_row_linear_fwd_allreduce(x, w, [y], ws)                         # X.W, fused AllReduce
-        tp.tp_row_linear_bwd(None, w, y, g, None, ws, preact=hh)              # dY.W^T * GeLU'(H)
+        tp.tp_row_linear_bwd(x, w, y, g, wgrad2, ws, preact=hh)               # dY.W^T * GeLU'(H), X^T.dY
         tp.tp_col_linear_bwd(None, w1, g, dx, None, ws)                       # dY.W^T, fused dX
-    wgrad = [torch.empty((NK, H), **bf) for _ in range(P)]
+    wgrad = [torch.empty((H, NK), **bf) for _ in range(P)]
     for _ in range(2):
-        tp.tp_row_linear_bwd(x, w, y, None, wgrad, ws)                        # X^T.dY
+        tp.tp_col_linear_bwd(y, w1, g, None, wgrad, ws)                       # X^T.dZ
     torch.cuda.synchronize()
     assert tp.tp_get_device_status(ws) == tp.TP_OK
     print("profile case done")
@@ -816,8 +819,7 @@ def workloads(torch, tp):
         return dict(calls=[
             ("col_fwd_gelu", lambda: tp.tp_col_linear_fwd(d["x"], d["w1"], Z, ws, epi=tp.TP_EPI_GELU, preact=Hh)),
             ("row_fwd_allreduce", lambda: tp.tp_row_linear_fwd_allreduce(Z, d["w2"], [Y], ws)),
-            ("row_bwd_dx_dgelu", lambda: tp.tp_row_linear_bwd(None, d["w2"], d["dy"], DZ, None, ws, preact=Hh)),
-            ("row_bwd_dw", lambda: tp.tp_row_linear_bwd(Z, d["w2"], d["dy"], None, DW2, ws)),
+            ("row_bwd", lambda: tp.tp_row_linear_bwd(Z, d["w2"], d["dy"], DZ, DW2, ws, preact=Hh)),
             ("col_bwd_dx", lambda: tp.tp_col_linear_bwd(None, d["w1"], DZ, DX, None, ws)),
             ("col_bwd_dw", lambda: tp.tp_col_linear_bwd(d["x"], d["w1"], DZ, None, DW1, ws))],
             flops=6 * 2.0 * M * h * nk * p, bytes=None, bound="tensor", flush=False,

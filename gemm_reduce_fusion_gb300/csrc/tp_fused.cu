@@ -37,8 +37,9 @@ constexpr int64_t kPreciseKb = 32;
 // An operand that every group of a launch reads through the same maps is
 // loaded evict_last when it takes at most this much of the 129 MB L2.
 constexpr int64_t kKeepBytes = 64ll << 20;
-// Backward dX and dW share one launch only when neither alone takes more
-// than this many waves of CTA pairs.
+// Backward dX and dW share one launch whenever that is no slower by the
+// makespan model while neither alone takes more than this many waves of CTA
+// pairs; longer ones only for a predicted gain of at least 3 %.
 constexpr int64_t kFuseWaves = 6;
 // Pair launches whose contraction is at least this deep alternate its
 // direction wave by wave (GemmParams::k_alternate).  From about 8192 on, the
@@ -783,13 +784,15 @@ int64_t pair_makespan(int64_t n0, int64_t kb0, int64_t n1, int64_t kb1, int64_t 
 }
 
 // The dX (dY.W^T) and dW (X^T.dY) launches of one backward call: one CTA-pair
-// launch for both when each is a short plain pair launch (no split-K, at
-// most kFuseWaves waves) and the combined static assignment finishes no
-// later than the two launches one after the other; otherwise the two
-// launches.  The two GEMMs are independent: neither reads what the other
-// writes.  Short launches gain most (one fill, drain and partial last wave
-// instead of two); on long ones the two problems' operands compete for L2
-// and measured slower, so those stay apart.
+// launch for both when both are plain pair launches (no split-K) and the
+// combined static assignment finishes no later than the two launches one
+// after the other -- for launches of more than kFuseWaves waves only when it
+// finishes at least 3 % sooner; otherwise the two launches.  The two GEMMs
+// are independent: neither reads what the other writes.  Short launches gain
+// most (one fill, drain and partial last wave instead of two).  On long ones
+// the saving is at most one wave, and where that is small the fused launch
+// measured slower (sequence-parallel backward, 47 waves each: 1.5-3 %); the
+// MLP block's row backward (2 x 13.5 waves: 27 fused against 28) gained.
 tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype out_dtype, void* ws,
                        cudaStream_t stream, const DevInfo& di) {
   const Shape& a = LX.shape;
@@ -803,7 +806,8 @@ tp_status run_bwd_pair(Launch& LX, bool do_x, Launch& LW, bool do_w, tp_dtype ou
     const int64_t sep = pair_makespan(a.units0, kba, 0, 0, C, a.tail_split) +
                         pair_makespan(b.units0, kbb, 0, 0, C, b.tail_split);
     const int64_t fused = pair_makespan(a.units0, kba, b.units0, kbb, C, 1);
-    if (fused <= sep && std::max(a.units0, b.units0) <= kFuseWaves * C) {
+    const bool short_launches = std::max(a.units0, b.units0) <= kFuseWaves * C;
+    if (fused <= sep && (short_launches || fused * 100 <= sep * 97)) {
       // whole tiles only: the fused launch has a single partial last wave
       Shape sa = a, sb = b;
       sa.tail_split = sb.tail_split = 1;
