@@ -1195,3 +1195,90 @@ def test_cuda_graph_capture_replays_bitwise(tp):
             assert torch.equal(a.view(iv), b.view(iv)), "graph replay differs from the eager calls"
     assert tp.tp_get_device_status(ws) == tp.TP_OK
     assert np.array_equal(host_f64(y2), oracle.row_fwd_allreduce([host_bits(t) for t in x2], [host_bits(t) for t in w2]))
+
+
+def test_alternating_contraction_direction_exact(tp):
+    """A contraction of 8192 or deeper on the CTA-pair kernel runs the whole
+    tiles of every other wave last k-block first (rank p-1's segment first).
+    Here 16 x 11 pair tiles are 2.3 waves over 4 x 2048: on integer inputs
+    every partial sum stays exact, so the bf16 AllReduce and the column
+    backward's fused dX must round exactly the oracle's sums, whichever order
+    a tile took, and the ReduceScatter slices must equal the AllReduce rows."""
+    import torch
+    p, M, N, K = 4, 4096, 2816, 2048
+    xs = [ints((M, K), 700 + r) for r in range(p)]
+    ws = [ints((K, N), 710 + r) for r in range(p)]
+    X, W = [dev(a) for a in xs], [dev(b) for b in ws]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tp.tp_row_linear_fwd_allreduce(X, W, [y], ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0))
+    assert np.array_equal(host_bits(y), oracle.round_bf16(oracle.row_fwd_allreduce(xs, ws)))
+    ys = [torch.empty((M // p, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    tp.tp_row_linear_fwd_reducescatter(X, W, ys, ws_for(tp, tp.TP_OP_ROW_RS, p, M, N, K, 0))
+    assert torch.equal(torch.cat(ys).view(torch.int16), y.view(torch.int16))
+    # column backward: dX = sum_k dY_k . A_k^T over 4 x 2048 = 8192, 16 x 16
+    # pair tiles (3.4 waves; waves 1 and 3 reversed, the last one in slices)
+    N, K = 2048, 4096
+    wc = [ints((K, N), 760 + k) for k in range(p)]
+    dys = [ints((M, N), 720 + k) for k in range(p)]
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    tp.tp_col_linear_bwd(None, [dev(b) for b in wc], [dev(d) for d in dys], dx, None,
+                         ws_for(tp, tp.TP_OP_COL_BWD, p, M, N, K, 0))
+    assert np.array_equal(host_bits(dx), oracle.round_bf16(oracle.col_bwd_dx(wc, dys)))
+
+
+def test_single_band_weight_gradient_exact(tp):
+    """dW_r = X_r^T . dY where the p X_r shards (4 x 2048 x 4608 bf16, 75 MB)
+    exceed the L2 budget and the shared dY (38 MB) does not: the planner
+    rasters all 16 N-tiles as one band instead of two bands of 8, so each
+    X_r panel is streamed once.  The order of the tiles must not change the
+    result: exact against the oracle on integer inputs (sums of 4608
+    products stay below 2**24)."""
+    import torch
+    p, M, N, K = 4, 4608, 4096, 2048
+    xs = [ints((M, K), 730 + r) for r in range(p)]
+    w = [ints((K, N), 740 + r) for r in range(p)]
+    dy = ints((M, N), 750)
+    dw = [torch.empty((K, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    tp.tp_row_linear_bwd([dev(a) for a in xs], [dev(b) for b in w], dev(dy), None, dw,
+                         ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0))
+    for g, r in zip(dw, oracle.row_bwd_dw(xs, dy)):
+        assert np.array_equal(host_bits(g), oracle.round_bf16(r))
+
+
+def test_long_backward_fused_launch_bitwise(tp, no_fusion):
+    """FC2's backward at the MLP block's size (p = 4, M = K = N = 4096): dZ_k
+    = dY . W_k^T * GeLU'(H_k) and dW_k = Z_k^T . dY are 1024 pair tiles each
+    (13.5 waves), which the planner runs as one launch of 27 waves.  That
+    launch must give the bits of the two separate launches, and sampled rows
+    of both products must equal the oracle on integer inputs (sums of 4096
+    products of values in [-4, 4] are exact).  GeLU' uses bf16 H."""
+    import torch
+    p, M, N, K = 4, 4096, 4096, 4096
+    xs = [ints((M, K), 770 + r) for r in range(p)]
+    w = [ints((K, N), 780 + r) for r in range(p)]
+    dy = ints((M, N), 790)
+    X, W, DY = [dev(a) for a in xs], [dev(b) for b in w], dev(dy)
+    ws = ws_for(tp, tp.TP_OP_ROW_BWD, p, M, N, K, 0)
+
+    def run(preact):
+        dx = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        dw = [torch.empty((K, N), dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        tp.tp_row_linear_bwd(X, W, DY, dx, dw, ws, preact=preact)
+        torch.cuda.synchronize()
+        assert tp.tp_get_device_status(ws) == tp.TP_OK
+        return dx, dw
+
+    H = [dev(synth.normal_bf16((M, K), 800 + r)) for r in range(p)]
+    fused = [run(None), run(H)]
+    assert tp.tp_debug_set(tp.TP_DEBUG_NO_BWD_FUSION, 1) == tp.TP_OK
+    sep = [run(None), run(H)]
+    for (fx, fw), (sx, sw) in zip(fused, sep):
+        for a, b in zip(fx + fw, sx + sw):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "fused and separate launches differ"
+    rows = np.array([0, 1, 255, 256, 1023, 2048, 3071, 4095])
+    dx, dw = fused[0]
+    ref_dx = oracle.row_bwd_dx(w, dy[rows])                          # dY . W_r^T on the sampled rows
+    ref_dw = oracle.row_bwd_dw([x[:, rows] for x in xs], dy)          # X_r^T . dY on the sampled rows
+    for r in range(p):
+        assert np.array_equal(host_bits(dx[r])[rows], oracle.round_bf16(ref_dx[r]))
+        assert np.array_equal(host_bits(dw[r])[rows], oracle.round_bf16(ref_dw[r]))

@@ -94,11 +94,11 @@ def test_mlp_block_fwd_bwd(tp):
     DW1 = [bf((h, nk)) for _ in range(p)]
     ws = ws_max(tp, [(tp.TP_OP_COL_FWD, p, M, nk, h, 0), (tp.TP_OP_ROW_AR, p, M, h, nk, 0),
                      (tp.TP_OP_ROW_BWD, p, M, h, nk, 0), (tp.TP_OP_COL_BWD, p, M, nk, h, 0)])
-    # the benchmark's six calls, in its order
+    # the benchmark's five calls, in its order (FC2's backward is one call:
+    # dZ and dW2 run as one launch at this size)
     tp.tp_col_linear_fwd(X, W1, Z, ws, epi=tp.TP_EPI_GELU, preact=H)
     tp.tp_row_linear_fwd_allreduce(Z, W2, [Y], ws)
-    tp.tp_row_linear_bwd(None, W2, DY, DZ, None, ws, preact=H)
-    tp.tp_row_linear_bwd(Z, W2, DY, None, DW2, ws)
+    tp.tp_row_linear_bwd(Z, W2, DY, DZ, DW2, ws, preact=H)
     tp.tp_col_linear_bwd(None, W1, DZ, DX, None, ws)
     tp.tp_col_linear_bwd(X, W1, DZ, None, DW1, ws)
     assert tp.tp_get_device_status(ws) == tp.TP_OK
