@@ -57,6 +57,7 @@ TP_DEBUG_SPLIT_K = 4
 TP_DEBUG_L2_HINTS = 5
 TP_DEBUG_TMA_STORE = 6
 TP_DEBUG_NO_BWD_FUSION = 7
+TP_DEBUG_K_ALTERNATE = 8
 # tp_row_linear_fwd_unfused flags
 TP_UNFUSED_BF16_COLLECTIVE = 1
 

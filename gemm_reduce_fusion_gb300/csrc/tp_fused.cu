@@ -72,6 +72,7 @@ std::atomic<unsigned long long> g_launch_epoch{0};  // numbers every launch (sli
 std::atomic<int64_t> g_l2_hints{1};         // 1: L2 cache policies on operand loads and output stores
 std::atomic<int64_t> g_tma_store{1};        // 1: staged epilogues leave shared memory by TMA store
 std::atomic<int64_t> g_debug_no_fuse{0};    // 1: backward dX and dW always as two launches
+std::atomic<int64_t> g_k_alternate{1};      // 1: deep contractions alternate their direction by wave
 
 uint64_t device_timeout_ns() {
   const uint64_t o = g_timeout_override_ns.load();
@@ -926,7 +927,7 @@ void prepare_gemm(Launch& L, tp_dtype out_dtype, void* ws) {
     P.b_hint = b_shared && b_bytes <= kKeepBytes ? 1 : 0;
     P.out_hint = 2;
   }
-  P.k_alternate = s.pair && s.S * s.kseg >= kKAlternateDepth ? 1 : 0;
+  P.k_alternate = g_k_alternate.load() != 0 && s.pair && s.S * s.kseg >= kKAlternateDepth ? 1 : 0;
   // staged epilogues (non-swapped tiles, no split-K partials) store through TMA
   P.out_tma = 0;
   if (g_tma_store.load() != 0 && !s.swap && s.n_split == 1) {
@@ -1062,6 +1063,10 @@ tp_status tp_debug_set(tp_debug_key key, int64_t value) {
     case TP_DEBUG_NO_BWD_FUSION:
       if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
       g_debug_no_fuse.store(value);
+      return TP_OK;
+    case TP_DEBUG_K_ALTERNATE:
+      if (value < 0 || value > 1) return TP_ERR_INVALID_ARG;
+      g_k_alternate.store(value);
       return TP_OK;
   }
   return TP_ERR_INVALID_ARG;

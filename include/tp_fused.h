@@ -368,6 +368,12 @@ tp_status tp_noalloc_device_status(cudaStream_t stream);
  *   TP_DEBUG_NO_BWD_FUSION: 0 (default) lets a backward call run its dX and
  *     dW products as one CTA-pair launch where that is planned to finish
  *     sooner; 1 always runs them as two launches (bit-identical results).
+ *   TP_DEBUG_K_ALTERNATE: 1 (default) lets CTA-pair launches whose
+ *     contraction is 8192 or deeper run the whole tiles of every other wave
+ *     last k-block first (rank p-1's segment first), which re-reads from L2
+ *     what the previous wave read last; 0 runs every tile first to last.
+ *     The order changes the fp32 rounding of non-integer sums (both orders
+ *     are deterministic), not exact ones.
  * Returns TP_ERR_INVALID_ARG for an unknown key or a bad value.            */
 typedef enum {
   TP_DEBUG_TIMEOUT_MS = 0,
@@ -377,7 +383,8 @@ typedef enum {
   TP_DEBUG_SPLIT_K = 4,
   TP_DEBUG_L2_HINTS = 5,
   TP_DEBUG_TMA_STORE = 6,
-  TP_DEBUG_NO_BWD_FUSION = 7
+  TP_DEBUG_NO_BWD_FUSION = 7,
+  TP_DEBUG_K_ALTERNATE = 8
 } tp_debug_key;
 tp_status tp_debug_set(tp_debug_key key, int64_t value);
 

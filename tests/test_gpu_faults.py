@@ -90,7 +90,8 @@ def test_timeout_on_cta_pairs_then_next_call_succeeds(tp, shape, tile_mode):
 
 
 def test_debug_hook_argument_checks(tp):
-    assert tp.tp_debug_set(8, 0) == tp.TP_ERR_INVALID_ARG
+    assert tp.tp_debug_set(9, 0) == tp.TP_ERR_INVALID_ARG
+    assert tp.tp_debug_set(tp.TP_DEBUG_K_ALTERNATE, 2) == tp.TP_ERR_INVALID_ARG
     assert tp.tp_debug_set(tp.TP_DEBUG_NO_BWD_FUSION, 2) == tp.TP_ERR_INVALID_ARG
     assert tp.tp_debug_set(tp.TP_DEBUG_TMA_STORE, 2) == tp.TP_ERR_INVALID_ARG
     assert tp.tp_debug_set(tp.TP_DEBUG_L2_HINTS, -1) == tp.TP_ERR_INVALID_ARG

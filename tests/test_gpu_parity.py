@@ -1282,3 +1282,43 @@ def test_long_backward_fused_launch_bitwise(tp, no_fusion):
     for r in range(p):
         assert np.array_equal(host_bits(dx[r])[rows], oracle.round_bf16(ref_dx[r]))
         assert np.array_equal(host_bits(dw[r])[rows], oracle.round_bf16(ref_dw[r]))
+
+
+@pytest.fixture
+def k_forward(tp):
+    yield
+    tp.tp_debug_set(tp.TP_DEBUG_K_ALTERNATE, 1)
+
+
+def test_alternating_direction_is_taken_and_within_tolerance(tp, k_forward):
+    """The reversed waves really run: on normal-valued inputs the planned
+    AllReduce over 4 x 2048 (16 x 11 pair tiles, 2.3 waves) differs in its
+    rounding from the same call with every tile forward
+    (TP_DEBUG_K_ALTERNATE = 0), only in tiles of the second wave, while
+    both stay within the bf16 tolerance of the oracle; each order is
+    reproducible bit for bit."""
+    import torch
+    p, M, N, K = 4, 4096, 2816, 2048
+    xs = [synth.normal_bf16((M, K), synth.seed_for(810, r), 1.0 / np.sqrt(p * K)) for r in range(p)]
+    ws = [synth.normal_bf16((K, N), synth.seed_for(811, r)) for r in range(p)]
+    X, W = [dev(a) for a in xs], [dev(b) for b in ws]
+    wsp = ws_for(tp, tp.TP_OP_ROW_AR, p, M, N, K, 0)
+
+    def run():
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        tp.tp_row_linear_fwd_allreduce(X, W, [y], wsp)
+        return host_bits(y)
+
+    planned = [run(), run()]
+    assert tp.tp_debug_set(tp.TP_DEBUG_K_ALTERNATE, 0) == tp.TP_OK
+    forward = [run(), run()]
+    assert np.array_equal(planned[0], planned[1]) and np.array_equal(forward[0], forward[1])
+    diff = planned[0] != forward[0]
+    assert diff.any(), "no tile ran in the other order"
+    # 256 x 256 tiles in which the two differ: only whole tiles of odd waves reverse
+    tiles = {(int(i) // 256, int(j) // 256) for i, j in zip(*np.nonzero(diff))}
+    assert len(tiles) <= 76
+    ref = oracle.row_fwd_allreduce(xs, ws)
+    for b in (planned[0], forward[0]):
+        got = b.astype(np.uint32) << np.uint32(16)
+        assert_close(got.view(np.float32).astype(np.float64), ref, False, "AllReduce")
